@@ -1,0 +1,413 @@
+#!/usr/bin/env python
+"""Benchmark of the Gated DeltaNet mixer hot path on one GB300 (or N replicas).
+
+A step is one pass of the whole prefill path on the prefill workload
+(B=1, T=4096, Nk=16 -> Nv=32, Dk=Dv=128, C=8192, bf16, fp32 gates/state):
+gdn_conv_gating (+ conv-state output) -> gdn_chunk_prefill -> gdn_gated_rmsnorm.
+The fused decode step (B=256, one token each, fp32 state in place) is timed in
+the same run and reported under "decode".
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle (the reference arm of this
+project) on a bounded sample of the same workload.  Under torchrun (N > 1)
+every rank runs its own replica (the path has no exchange step); rank 0
+prints one JSON line.
+"""
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = 'GDN prefill tokens/s & % bf16 TC peak; decode tokens/s & HBM GB/s vs ~8TB/s'
+CHUNK = 64
+L2_FLUSH_BYTES = 512 << 20
+NOMINAL_HBM_GBS = 8000.0
+
+
+def chunk_flops_per_chunk_head(Dk, Dv, C=CHUNK):
+    """Algorithmic flops of one chunk of one value head: KK^T, QK^T, W, U~ and
+    P.U over full 64x64 tiles, W.S, Q.S and K^T.U, and the triangular inverse."""
+    return 2 * C * C * (3 * Dk + 2 * Dv) + 6 * C * Dk * Dv + C ** 3 / 3.0
+
+
+def chunk_flops(lengths, Nv, Dk, Dv):
+    return sum(math.ceil(L / CHUNK) for L in lengths) * Nv * chunk_flops_per_chunk_head(Dk, Dv)
+
+
+def chunk_bytes(tokens, Nk, Nv, Dk, Dv, act=2, out=2):
+    # q, k read once per key head, v once, g and beta fp32, o written once
+    return tokens * (2 * Nk * Dk * act + Nv * Dv * act + 2 * Nv * 4 + Nv * Dv * out)
+
+
+def conv_gating_bytes(tokens, num_seqs, C, Nk, Nv, Dk, Dv, act=2):
+    return (tokens * (C * act + 2 * Nv * act)            # mixed_qkv, a, b
+            + tokens * (2 * Nk * Dk + Nv * Dv) * act      # q, k, v out
+            + tokens * Nv * 2 * 4                         # g, beta out
+            + C * 4 * act + num_seqs * C * 3 * act)       # weights, conv state out
+
+
+def rmsnorm_bytes(rows, dim, act=2, out=2):
+    return rows * dim * (act + act + out) + dim * 4
+
+
+def decode_bytes(B, Nk, Nv, Dk, Dv, act=2, out=2):
+    C = 2 * Nk * Dk + Nv * Dv
+    return (2 * B * Nv * Dk * Dv * 4            # state read + write
+            + 2 * B * C * 3 * act               # conv state read + write
+            + B * C * act                       # mixed_qkv
+            + B * Nv * Dv * act                 # z
+            + 2 * B * Nv * act                  # a, b
+            + B * Nv * Dv * out                 # y
+            + C * 4 * act + 2 * Nv * 4 + Dv * 4)  # weights
+
+
+def load_peaks():
+    p = os.path.join(ROOT, 'MEASURED_PEAKS.json')
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d['hbm_gbs'], d['bf16_tflops'], d.get('bf16_tflops_sustained', d['bf16_tflops']), 'measured'
+    return 6800.0, 1900.0, 1700.0, 'fallback'
+
+
+class ClockSampler:
+    FIELDS = ('index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,'
+              'clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,'
+              'clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap')
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix='.csv')
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ['nvidia-smi', '-i', str(self.gpu), '--query-gpu=' + self.FIELDS,
+                 '--format=csv,noheader,nounits', '-lms', '100'],
+                stdout=open(self.path, 'w'), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {'sm_mhz': None, 'sm_max_mhz': None, 'reasons': ['nvidia-smi unavailable']}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(',')]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {'sm_mhz': None, 'sm_max_mhz': None, 'reasons': [], 'samples': 0}
+        names = ['hw_slowdown', 'hw_thermal_slowdown', 'sw_thermal_slowdown', 'sw_power_cap']
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3]) if v.lower() == 'active'})
+        loaded = [r for r in rows if r[2] > 250.0] or rows
+        return {'sm_mhz': statistics.median(r[0] for r in loaded), 'sm_max_mhz': max(r[1] for r in rows),
+                'reasons': reasons, 'samples': len(rows), 'samples_under_load': len(loaded),
+                'power_w_max': max(r[2] for r in rows)}
+
+
+def dist_setup():
+    ws = int(os.environ.get('WORLD_SIZE', '1'))
+    rank = int(os.environ.get('RANK', '0'))
+    local = int(os.environ.get('LOCAL_RANK', '0'))
+    return ws, rank, local
+
+
+# ------------------------------------------------------------------ reference arm
+
+def cpu_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_prefill_sample(inp, ntok):
+    """The oracle's prefill over the first ntok tokens of the workload (all heads)."""
+    import numpy as np
+    import oracle as O
+    sh = inp.shape
+    f = lambda t: t[:ntok].to(dtype=__import__('torch').float64).numpy()  # noqa: E731
+    g = lambda t: t.to(dtype=__import__('torch').float64).numpy()  # noqa: E731
+    r = O.mixer_prefill(f(inp.mixed_qkv), g(inp.conv_w), f(inp.a), f(inp.b), g(inp.A_log),
+                        g(inp.dt_bias), f(inp.z), g(inp.norm_w), sh.Nk, sh.Nv, sh.Dk, sh.Dv)
+    return np.asarray(r['y']).shape[0]
+
+
+def cpu_baseline(inp, budget_s=12.0):
+    """Oracle tokens/s on a bounded prefix of the prefill workload."""
+    n = 32
+    t0 = time.perf_counter()
+    oracle_prefill_sample(inp, n)
+    dt = time.perf_counter() - t0
+    ntok = int(max(32, min(inp.total_tokens, n * budget_s / max(dt, 1e-3))))
+    t0 = time.perf_counter()
+    oracle_prefill_sample(inp, ntok)
+    dt = time.perf_counter() - t0
+    return {'value': ntok / dt, 'unit': 'tokens/s', 'cores': cpu_threads(), 'kind': 'oracle',
+            'sample': 'fp64 NumPy oracle prefill (conv_gating + token-by-token recurrence + gated '
+                      'RMSNorm) over the first %d of 4096 tokens, all 32 heads, %.1f s' % (ntok, dt)}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    from gated_deltanet_linear_conv_gb300 import inputs as I
+    inp = I.workload('prefill_t4096')
+    ntok = 64
+    for _ in range(args.warmup):
+        oracle_prefill_sample(inp, ntok)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_prefill_sample(inp, ntok)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = ntok / dt
+    line = {'impl': 'reference', 'metric': METRIC, 'value': value, 'unit': 'tokens/s',
+            'n_gpus': ws, 'steps': args.steps, 'warmup': args.warmup, 'ms_per_step': dt * 1e3,
+            'higher_is_better': True, 'scaling': 'weak', 'vs_baseline': None, 'dtype': 'f64',
+            'data': 'synthetic',
+            'config': {'workload': 'prefill_t4096', 'B': 1, 'T': 4096, 'Nk': 16, 'Nv': 32, 'Dk': 128,
+                       'Dv': 128, 'chunk': CHUNK, 'sample_tokens_per_step': ntok},
+            'cpu_baseline': {'value': value, 'unit': 'tokens/s', 'cores': cpu_threads(), 'kind': 'oracle',
+                             'sample': 'first %d tokens of the prefill workload per step' % ntok},
+            'e2e': {'value': value, 'unit': 'tokens/s', 'h2d_bytes_per_step': 0, 'd2h_bytes_per_step': 0}}
+    print(json.dumps(line))
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args):
+    import torch
+    from gated_deltanet_linear_conv_gb300 import gdn
+    from gated_deltanet_linear_conv_gb300 import inputs as I
+
+    ws, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group('nccl', device_id=torch.device('cuda', local))
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(x):
+        if dist is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device='cuda')
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    hbm_peak, tc_peak, tc_sust, peak_src = load_peaks()
+    sampler = ClockSampler(local)
+
+    # ---------------- prefill workload, resident in HBM
+    inp = I.workload('prefill_t4096')
+    sh = inp.shape
+    T = inp.total_tokens
+    dev = lambda t: t.cuda()  # noqa: E731
+    x, w, a, b = dev(inp.mixed_qkv), dev(inp.conv_w), dev(inp.a), dev(inp.b)
+    A_log, dt_bias, z, nw = dev(inp.A_log), dev(inp.dt_bias), dev(inp.z), dev(inp.norm_w)
+    bf = torch.bfloat16
+    bufs = dict(q=torch.empty(T, sh.Nk, sh.Dk, dtype=bf, device='cuda'),
+                k=torch.empty(T, sh.Nk, sh.Dk, dtype=bf, device='cuda'),
+                v=torch.empty(T, sh.Nv, sh.Dv, dtype=bf, device='cuda'),
+                g=torch.empty(T, sh.Nv, device='cuda'), beta=torch.empty(T, sh.Nv, device='cuda'),
+                o=torch.empty(T, sh.Nv, sh.Dv, dtype=bf, device='cuda'),
+                y=torch.empty(T, sh.Nv, sh.Dv, dtype=bf, device='cuda'))
+    ws_bytes = gdn.chunk_prefill_workspace_size(1, T, sh.Nk, sh.Nv, sh.Dk, sh.Dv)
+    if ws_bytes:
+        bufs['workspace'] = torch.empty(ws_bytes, dtype=torch.uint8, device='cuda')
+    conv_state_out = torch.empty(1, sh.C, 3, dtype=bf, device='cuda')
+    final_state = torch.empty(1, sh.Nv, sh.Dk, sh.Dv, device='cuda')
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device='cuda')
+    stream = torch.cuda.current_stream()
+
+    def prefill_step(ev=None):
+        q, k, v, g, beta = gdn.conv_gating(x, w, a, b, A_log, dt_bias, sh.Nk, sh.Nv, sh.Dk, sh.Dv,
+                                           num_seqs=1, conv_state_out=conv_state_out,
+                                           out=(bufs['q'], bufs['k'], bufs['v'], bufs['g'], bufs['beta']))
+        if ev:
+            ev[1].record(stream)
+        gdn.chunk_prefill(q, k, v, g, beta, 1.0, None, final_state, None, 1, bf, bufs['o'],
+                          bufs.get('workspace'))
+        if ev:
+            ev[2].record(stream)
+        gdn.gated_rmsnorm(bufs['o'], z, nw, 1e-6, bf, bufs['y'])
+
+    sampler.start()
+    for _ in range(args.warmup):
+        prefill_step()
+    barrier()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.fill_(float(i))                      # evict the inputs from L2 between steps
+        evs[i][0].record(stream)
+        prefill_step(evs[i])
+        evs[i][3].record(stream)
+    barrier()
+    t_conv = [e[0].elapsed_time(e[1]) for e in evs]
+    t_chunk = [e[1].elapsed_time(e[2]) for e in evs]
+    t_norm = [e[2].elapsed_time(e[3]) for e in evs]
+    t_step = [e[0].elapsed_time(e[3]) for e in evs]
+    ms_step = max_over_ranks(statistics.mean(t_step))
+    launches_prefill = 4 * args.steps          # conv, conv-state, chunk, rmsnorm
+
+    # ---------------- decode workload (fused step, state in place; 512 MiB state > L2)
+    del flush
+    dinp = I.workload('decode_b256')
+    B = dinp.num_seqs
+    dx, dw, da, db = dev(dinp.mixed_qkv), dev(dinp.conv_w), dev(dinp.a), dev(dinp.b)
+    dA, ddt, dz, dnw = dev(dinp.A_log), dev(dinp.dt_bias), dev(dinp.z), dev(dinp.norm_w)
+    dcs, dS = dev(dinp.conv_state), dev(dinp.S0)
+    dy = torch.empty(B, sh.Nv, sh.Dv, dtype=bf, device='cuda')
+
+    def decode_step():
+        gdn.decode_fused(dx, dw, dcs, da, db, dA, ddt, dS, dz, dnw, sh.Nk, sh.Nv, sh.Dk, sh.Dv,
+                         out_dtype=bf, y=dy)
+
+    dsteps = max(args.steps, 20)
+    for _ in range(args.warmup):
+        decode_step()
+    barrier()
+    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    d0.record(stream)
+    for _ in range(dsteps):
+        decode_step()
+    d1.record(stream)
+    barrier()
+    ms_dec = max_over_ranks(d0.elapsed_time(d1) / dsteps)
+    del dS, dcs
+
+    # ---------------- end to end through the public API with host buffers
+    pin = lambda t: t.pin_memory()  # noqa: E731
+    hx, ha, hb, hz = pin(inp.mixed_qkv), pin(inp.a), pin(inp.b), pin(inp.z)
+    hy = torch.empty(T, sh.Nv, sh.Dv, dtype=bf).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hx, ha, hb, hz))
+    d2h = hy.numel() * hy.element_size()
+
+    def e2e_step():
+        x.copy_(hx, non_blocking=True)
+        a.copy_(ha, non_blocking=True)
+        b.copy_(hb, non_blocking=True)
+        z.copy_(hz, non_blocking=True)
+        prefill_step()
+        hy.copy_(bufs['y'], non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1) / args.steps)
+    clocks = sampler.stop()
+    gdn.check_device_error()
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    flops = chunk_flops(inp.lengths, sh.Nv, sh.Dk, sh.Dv)
+    us_chunk = statistics.mean(t_chunk) * 1e3
+    us_conv = statistics.mean(t_conv) * 1e3
+    us_norm = statistics.mean(t_norm) * 1e3
+    tflops = flops / (us_chunk * 1e-6) / 1e12
+    cb = conv_gating_bytes(T, 1, sh.C, sh.Nk, sh.Nv, sh.Dk, sh.Dv)
+    nb = rmsnorm_bytes(T * sh.Nv, sh.Dv)
+    kb = chunk_bytes(T, sh.Nk, sh.Nv, sh.Dk, sh.Dv)
+    dbytes = decode_bytes(B, sh.Nk, sh.Nv, sh.Dk, sh.Dv)
+    dec_gbs = dbytes / (ms_dec * 1e-3) / 1e9
+    traffic = None
+    tp = os.path.join(ROOT, 'profiles', 'traffic.json')
+    if os.path.exists(tp):
+        traffic = json.load(open(tp)).get('chunk_prefill_t4096')
+    line = {
+        'metric': METRIC,
+        'value': ws * T / (ms_step * 1e-3),
+        'unit': 'tokens/s',
+        'n_gpus': ws, 'steps': args.steps, 'warmup': args.warmup,
+        'ms_per_step': ms_step,
+        'higher_is_better': True, 'scaling': 'weak', 'vs_baseline': None,
+        'dtype': 'bf16', 'data': 'synthetic',
+        'config': {'workload': 'prefill_t4096', 'B': 1, 'T': T, 'Nk': sh.Nk, 'Nv': sh.Nv, 'Dk': sh.Dk,
+                   'Dv': sh.Dv, 'C': sh.C, 'chunk': CHUNK, 'state': 'fp32', 'gates': 'fp32',
+                   'l2': 'flushed between timed steps (512 MiB write)', 'parallelism': 'replicas'},
+        'roofline': {'kernel': 'gdn_chunk_prefill', 'bound': 'tensor', 'achieved': tflops,
+                     'peak': tc_peak, 'unit': 'TFLOP/s', 'frac': tflops / tc_peak,
+                     'traffic': traffic, 'peak_source': peak_src + ' bf16 dense (burst)',
+                     'algorithmic_flops_per_launch': flops, 'us_per_launch': us_chunk,
+                     'hbm_gbs': kb / (us_chunk * 1e-6) / 1e9},
+        'kernels': {
+            'conv_gating': {'us': us_conv, 'GB/s': cb / (us_conv * 1e-6) / 1e9,
+                            'frac_hbm': cb / (us_conv * 1e-6) / 1e9 / hbm_peak, 'bytes': cb},
+            'chunk_prefill': {'us': us_chunk, 'TFLOP/s': tflops, 'frac_tc': tflops / tc_peak},
+            'gated_rmsnorm': {'us': us_norm, 'GB/s': nb / (us_norm * 1e-6) / 1e9,
+                              'frac_hbm': nb / (us_norm * 1e-6) / 1e9 / hbm_peak, 'bytes': nb}},
+        'decode': {'workload': 'decode_b256', 'kernel': 'gdn_decode_fused', 'steps': dsteps,
+                   'us_per_step': ms_dec * 1e3, 'tokens_per_s': ws * B / (ms_dec * 1e-3),
+                   'roofline': {'bound': 'hbm', 'achieved': dec_gbs, 'peak': hbm_peak, 'unit': 'GB/s',
+                                'frac': dec_gbs / hbm_peak, 'frac_of_8tbs': dec_gbs / NOMINAL_HBM_GBS,
+                                'bytes_per_launch': dbytes}},
+        'e2e': {'value': ws * T / (ms_e2e * 1e-3), 'unit': 'tokens/s', 'h2d_bytes_per_step': h2d,
+                'd2h_bytes_per_step': d2h, 'ms_per_step': ms_e2e},
+        'gpu_launches': launches_prefill + dsteps + 4 * args.steps,
+        'clocks': clocks,
+    }
+    if ws == 1 and not args.no_cpu_baseline:
+        line['cpu_baseline'] = cpu_baseline(inp)
+    print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument('--gpus', type=int, default=1)
+    ap.add_argument('--steps', type=int, default=20)
+    ap.add_argument('--warmup', type=int, default=5)
+    ap.add_argument('--impl', default='ours', choices=['ours', 'reference'])
+    ap.add_argument('--no-cpu-baseline', action='store_true')
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == 'ours':
+        print('note: warmup raised to 3', file=sys.stderr)
+        args.warmup = 3
+    if args.impl == 'reference':
+        run_reference(args)
+    else:
+        from gated_deltanet_linear_conv_gb300 import _build
+        _build.build()
+        run_ours(args)
+
+
+if __name__ == '__main__':
+    main()

@@ -1,0 +1,85 @@
+// Internal launcher interface between the C-ABI layer (api.cu) and the
+// kernel translation units.  Arguments are already validated by the caller.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace gdn {
+
+struct ConvGatingArgs {
+  const void* x;          // mixed_qkv [T, C]
+  const void* w;          // [C, 4]
+  const void* bias;       // [C] or null
+  const void* state_in;   // [N, C, 3] or null
+  void* state_out;        // [N, C, 3] or null
+  const void* a;          // [T, Nv]
+  const void* b;          // [T, Nv]
+  const float* A_log;     // [Nv]
+  const float* dt_bias;   // [Nv]
+  void* q;                // [T, Nk, Dk]
+  void* k;                // [T, Nk, Dk]
+  void* v;                // [T, Nv, Dv]
+  float* g;               // [T, Nv]
+  float* beta;            // [T, Nv]
+  const int32_t* cu;      // [N + 1] or null
+  int num_seqs, total, Nk, Nv, Dk, Dv, C;
+  float q_scale, l2_eps;
+  int in_bf16, out_bf16;
+  int* err;
+};
+cudaError_t launch_conv_gating(const ConvGatingArgs& p, cudaStream_t s);
+
+struct GatingArgs {
+  const void* a; const void* b; const float* A_log; const float* dt_bias;
+  float* g; float* beta; int64_t rows; int Nv; int in_bf16;
+};
+cudaError_t launch_gating(const GatingArgs& p, cudaStream_t s);
+
+struct RmsNormArgs {
+  const void* x; const void* z; const float* w; void* y;
+  int64_t rows; int dim; float eps; int x_bf16, z_bf16, out_bf16;
+};
+cudaError_t launch_gated_rmsnorm(const RmsNormArgs& p, cudaStream_t s);
+
+struct DecodeArgs {
+  const void* q; const void* k; const void* v;   // [T, Nk, Dk] / [T, Nv, Dv]
+  const float* g; const float* beta;             // [T, Nv]
+  float* state;                                  // [N, Nv, Dk, Dv]
+  void* o;                                       // [T, Nv, Dv]
+  const int32_t* cu;
+  int num_seqs, total, Nk, Nv, Dk, Dv;
+  float scale;
+  int in_bf16, out_bf16;
+  int* err;
+};
+cudaError_t launch_recurrent_decode(const DecodeArgs& p, cudaStream_t s);
+
+struct DecodeFusedArgs {
+  const void* x; const void* w; const void* bias; void* conv_state;
+  const void* a; const void* b; const float* A_log; const float* dt_bias;
+  float* state; const void* z; const float* norm_w; void* y;
+  int B, Nk, Nv, Dk, Dv, C;
+  float q_scale, l2_eps, norm_eps;
+  int in_bf16, out_bf16;
+};
+cudaError_t launch_decode_fused(const DecodeFusedArgs& p, cudaStream_t s);
+
+struct ChunkArgs {
+  const void* q; const void* k; const void* v;   // [T, Nk, Dk] / [T, Nv, Dv]
+  const float* g; const float* beta;             // [T, Nv]
+  const float* S0;                               // [N, Nv, Dk, Dv] or null
+  float* ST;                                     // [N, Nv, Dk, Dv] or null
+  void* o;                                       // [T, Nv, Dv]
+  const int32_t* cu;
+  int num_seqs, total, Nk, Nv, Dk, Dv;
+  float scale;
+  int in_bf16, out_bf16;
+  void* workspace; size_t workspace_bytes;
+  int* err;
+};
+// Portable fp32 CUDA-core implementation of the chunk form.
+cudaError_t launch_chunk_simt(const ChunkArgs& p, cudaStream_t s);
+
+}  // namespace gdn

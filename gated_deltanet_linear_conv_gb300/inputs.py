@@ -195,3 +195,19 @@ def workload(name):
                                  S0_std=0.02)
     return make_mixer_inputs(spec['seed'], spec['lengths'],
                              A_log_range=spec.get('A_log_range', (0.0, math.log(16.0))))
+
+
+# ---------------------------------------------------------------------------
+# generic seeded draws for tests of single steps
+# ---------------------------------------------------------------------------
+
+def draw_normal(seed, shape, mean=0.0, std=1.0, dtype=torch.float32):
+    """N(mean, std) of the given shape from a generator seeded with ``seed``."""
+    gen = torch.Generator().manual_seed(seed)
+    return _normal(gen, tuple(shape), mean, std).to(dtype)
+
+
+def draw_uniform(seed, shape, lo, hi, dtype=torch.float32):
+    """U(lo, hi) of the given shape from a generator seeded with ``seed``."""
+    gen = torch.Generator().manual_seed(seed)
+    return _uniform(gen, tuple(shape), lo, hi).to(dtype)

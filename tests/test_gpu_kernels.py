@@ -1,0 +1,296 @@
+"""Parity of every CUDA entry point with the fp64 oracle at small sizes that
+still span several tiles, ragged tails, empty sequences and both head sizes.
+All calls go through the C ABI (libgdn.so via the ctypes binding)."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from gated_deltanet_linear_conv_gb300 import gdn
+from gated_deltanet_linear_conv_gb300 import inputs as I
+from helpers import TOL_BF16, TOL_F32, np64, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [I.MixerShape(2, 4, 128, 128), I.MixerShape(2, 2, 64, 64)]
+
+
+def cuda(t):
+    return None if t is None else t.cuda()
+
+
+# ------------------------------------------------------------------ rmsnorm
+
+@pytest.mark.parametrize('dim', [64, 128])
+@pytest.mark.parametrize('xdt', [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize('rows', [0, 1, 1237])
+def test_gated_rmsnorm(dim, xdt, rows):
+    x = I.draw_normal(1, (rows, dim), dtype=xdt)
+    z = I.draw_normal(2, (rows, dim), dtype=xdt)
+    w = I.draw_normal(3, (dim,), 1.0, 0.1)
+    y = gdn.gated_rmsnorm(cuda(x), cuda(z), cuda(w), 1e-6, torch.float32)
+    torch.cuda.synchronize()
+    if rows == 0:
+        return
+    ref = O.gated_rmsnorm(np64(x), np64(z), np64(w), 1e-6)
+    assert rel_l2(np64(y), ref) <= TOL_F32
+    yb = gdn.gated_rmsnorm(cuda(x), cuda(z), cuda(w), 1e-6, torch.bfloat16)
+    assert rel_l2(np64(yb), ref) <= TOL_BF16
+
+
+# ------------------------------------------------------------------ gating
+
+@pytest.mark.parametrize('dt', [torch.float32, torch.bfloat16])
+def test_gating(dt):
+    rows, Nv = 777, 6
+    a = I.draw_normal(4, (rows, Nv), 0.0, 3.0, dtype=dt)
+    b = I.draw_normal(5, (rows, Nv), 0.0, 3.0, dtype=dt)
+    A_log = I.draw_uniform(6, (Nv,), -4.0, math.log(16.0))
+    dt_bias = I.draw_uniform(7, (Nv,), -1.0, 1.0)
+    g, beta = gdn.gating(cuda(a), cuda(b), cuda(A_log), cuda(dt_bias))
+    rg, rb = O.gating(np64(a), np64(b), np64(A_log), np64(dt_bias))
+    assert rel_l2(np64(g), rg) <= TOL_F32
+    assert rel_l2(np64(beta), rb) <= TOL_F32
+
+
+# ------------------------------------------------------------------ conv + gating
+
+def _conv_case(shape, dt, lengths, seed=11, state=True, bias=True):
+    return I.make_mixer_inputs(seed, lengths, shape, dtype=dt,
+                               conv_state_std=1.0 if state else None,
+                               conv_bias_std=0.1 if bias else None)
+
+
+def _run_conv(inp, cu, out_dtype, in_place=False, state=True):
+    sh = inp.shape
+    cs_in = cuda(inp.conv_state) if state else None
+    if in_place:
+        cs_out = cs_in
+    else:
+        cs_out = torch.empty(inp.num_seqs, sh.C, 3, dtype=inp.mixed_qkv.dtype, device='cuda')
+    res = gdn.conv_gating(cuda(inp.mixed_qkv), cuda(inp.conv_w), cuda(inp.a), cuda(inp.b),
+                          cuda(inp.A_log), cuda(inp.dt_bias), sh.Nk, sh.Nv, sh.Dk, sh.Dv,
+                          cu_seqlens=cuda(cu), num_seqs=inp.num_seqs,
+                          conv_bias=cuda(inp.extra.get('conv_bias')), conv_state_in=cs_in,
+                          conv_state_out=cs_out, out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    return res, cs_out
+
+
+def _oracle_conv(inp, cu, state=True):
+    sh = inp.shape
+    return O.conv_gating(np64(inp.mixed_qkv), np64(inp.conv_w), np64(inp.a), np64(inp.b),
+                         np64(inp.A_log), np64(inp.dt_bias), sh.Nk, sh.Nv, sh.Dk, sh.Dv,
+                         cu_seqlens=None if cu is None else cu.numpy(), num_seqs=inp.num_seqs,
+                         conv_bias=np64(inp.extra.get('conv_bias')),
+                         conv_state=np64(inp.conv_state) if state else None)
+
+
+@pytest.mark.parametrize('shape', SHAPES, ids=['d128', 'd64'])
+@pytest.mark.parametrize('dt', [torch.float32, torch.bfloat16], ids=['f32', 'bf16'])
+def test_conv_gating_varlen(shape, dt):
+    lengths = [1, 2, 5, 0, 37, 64, 130, 3]
+    inp = _conv_case(shape, dt, lengths)
+    cu = inp.cu_seqlens()
+    (q, k, v, g, beta), cs_out = _run_conv(inp, cu, torch.float32)
+    ref = _oracle_conv(inp, cu)
+    for name, got in (('q', q), ('k', k), ('v', v), ('g', g), ('beta', beta)):
+        assert rel_l2(np64(got), ref[name]) <= TOL_F32, name
+    np.testing.assert_array_equal(np64(cs_out), ref['conv_state'])
+    gdn.check_device_error()
+
+
+@pytest.mark.parametrize('shape', SHAPES, ids=['d128', 'd64'])
+def test_conv_gating_in_place_state_and_bf16_out(shape):
+    lengths = [2, 70, 1, 19]
+    inp = _conv_case(shape, torch.bfloat16, lengths, seed=12)
+    cu = inp.cu_seqlens()
+    ref = _oracle_conv(inp, cu)
+    (q, k, v, g, beta), cs = _run_conv(inp, cu, torch.bfloat16, in_place=True)
+    np.testing.assert_array_equal(np64(cs), ref['conv_state'])
+    for name, got in (('q', q), ('k', k), ('v', v)):
+        assert rel_l2(np64(got), ref[name]) <= TOL_BF16, name
+
+
+def test_conv_gating_equal_batches_no_state():
+    shape = SHAPES[0]
+    inp = _conv_case(shape, torch.bfloat16, [33, 33, 33], seed=13, state=False, bias=False)
+    (q, k, v, g, beta), cs_out = _run_conv(inp, None, torch.float32, state=False)
+    ref = _oracle_conv(inp, None, state=False)
+    for name, got in (('q', q), ('k', k), ('v', v), ('g', g), ('beta', beta)):
+        assert rel_l2(np64(got), ref[name]) <= TOL_F32, name
+    np.testing.assert_array_equal(np64(cs_out), ref['conv_state'])
+
+
+# ------------------------------------------------------------------ recurrent decode
+
+@pytest.mark.parametrize('shape', SHAPES + [I.MixerShape(1, 2, 128, 64), I.MixerShape(2, 2, 64, 128)],
+                         ids=['d128', 'd64', 'k128v64', 'k64v128'])
+def test_recurrent_decode_multi_token(shape):
+    lengths = [1, 4, 2, 3]                   # one-token decode and multi-token verify
+    c = I.make_core_inputs(21, lengths, shape, S0_std=0.5)
+    g, beta = O.gating(np64(c.a), np64(c.b), np64(c.A_log), np64(c.dt_bias))
+    gt, bt = torch.tensor(g, dtype=torch.float32), torch.tensor(beta, dtype=torch.float32)
+    cu = c.cu_seqlens()
+    state = cuda(c.S0.clone())
+    o = gdn.recurrent_decode(cuda(c.q), cuda(c.k), cuda(c.v), cuda(gt), cuda(bt), state, 0.3,
+                             cu_seqlens=cuda(cu), out_dtype=torch.float32)
+    ro, rS = O.recurrent_gated_delta_rule(np64(c.q), np64(c.k), np64(c.v), np64(gt), np64(bt), 0.3,
+                                          np64(c.S0), cu.numpy())
+    assert rel_l2(np64(o), ro) <= TOL_F32
+    assert rel_l2(np64(state), rS) <= TOL_F32
+
+
+def test_gpu_gating_feeds_decode():
+    """gdn_gating + gdn_recurrent_decode on the tiny workload vs the oracle."""
+    c = I.workload('tiny_core_t256')
+    sh = c.shape
+    g, beta = gdn.gating(cuda(c.a), cuda(c.b), cuda(c.A_log), cuda(c.dt_bias))
+    state = torch.zeros(1, sh.Nv, sh.Dk, sh.Dv, device='cuda')
+    o = gdn.recurrent_decode(cuda(c.q), cuda(c.k), cuda(c.v), g, beta, state, 1 / 8,
+                             num_seqs=1, out_dtype=torch.float32)
+    rg, rb = O.gating(np64(c.a), np64(c.b), np64(c.A_log), np64(c.dt_bias))
+    ro, rS = O.recurrent_gated_delta_rule(np64(c.q), np64(c.k), np64(c.v), rg, rb, 1 / 8)
+    assert rel_l2(np64(o), ro) <= TOL_F32
+    assert rel_l2(np64(state), rS) <= TOL_F32
+
+
+# ------------------------------------------------------------------ fused decode
+
+@pytest.mark.parametrize('shape', SHAPES + [I.MixerShape(1, 4, 128, 128)], ids=['d128', 'd64', 'r4'])
+def test_decode_fused_two_steps(shape):
+    B = 5
+    inp = I.make_mixer_inputs(31, [2] * B, shape, conv_state_std=1.0, S0_std=0.05)
+    sh = inp.shape
+    mixed = inp.mixed_qkv.view(B, 2, sh.C)
+    a = inp.a.view(B, 2, sh.Nv)
+    b = inp.b.view(B, 2, sh.Nv)
+    z = inp.z.view(B, 2, sh.Nv, sh.Dv)
+    cs, S = cuda(inp.conv_state.clone()), cuda(inp.S0.clone())
+    rcs, rS = np64(inp.conv_state), np64(inp.S0)
+    for step in range(2):
+        y = gdn.decode_fused(cuda(mixed[:, step].contiguous()), cuda(inp.conv_w), cs,
+                             cuda(a[:, step].contiguous()), cuda(b[:, step].contiguous()),
+                             cuda(inp.A_log), cuda(inp.dt_bias), S, cuda(z[:, step].contiguous()),
+                             cuda(inp.norm_w), sh.Nk, sh.Nv, sh.Dk, sh.Dv, out_dtype=torch.float32)
+        ref = O.decode_step(np64(mixed[:, step]), np64(inp.conv_w), rcs, np64(a[:, step]),
+                            np64(b[:, step]), np64(inp.A_log), np64(inp.dt_bias), rS,
+                            np64(z[:, step]), np64(inp.norm_w), sh.Nk, sh.Nv, sh.Dk, sh.Dv)
+        rcs, rS = ref['conv_state'], ref['state']
+        assert rel_l2(np64(y), ref['y']) <= TOL_F32, step
+        assert rel_l2(np64(S), rS) <= TOL_F32, step
+        np.testing.assert_array_equal(np64(cs), rcs)
+
+
+# ------------------------------------------------------------------ chunk prefill
+
+CHUNK_LENGTHS = [[1], [63], [64], [65], [200], [0, 5, 0, 70, 128, 1]]
+
+
+def _core_gates(c):
+    g, beta = O.gating(np64(c.a), np64(c.b), np64(c.A_log), np64(c.dt_bias))
+    return torch.tensor(g, dtype=torch.float32), torch.tensor(beta, dtype=torch.float32)
+
+
+@pytest.mark.parametrize('fp32', [True, False], ids=['fp32', 'tc'])
+@pytest.mark.parametrize('shape', SHAPES, ids=['d128', 'd64'])
+@pytest.mark.parametrize('lengths', CHUNK_LENGTHS, ids=lambda L: 'L' + '_'.join(map(str, L)))
+def test_chunk_prefill_varlen(fp32, shape, lengths):
+    c = I.make_core_inputs(41, lengths, shape, S0_std=0.1)
+    gt, bt = _core_gates(c)
+    cu = c.cu_seqlens()
+    o, ST = gdn.chunk_prefill(cuda(c.q), cuda(c.k), cuda(c.v), cuda(gt), cuda(bt), 0.2,
+                              initial_state=cuda(c.S0), cu_seqlens=cuda(cu),
+                              out_dtype=torch.float32, fp32=fp32)
+    torch.cuda.synchronize()
+    ro, rS = O.recurrent_gated_delta_rule(np64(c.q), np64(c.k), np64(c.v), np64(gt), np64(bt), 0.2,
+                                          np64(c.S0), cu.numpy())
+    tol = TOL_F32 if fp32 else TOL_BF16
+    if sum(lengths) > 0:
+        assert rel_l2(np64(o), ro) <= tol
+    assert rel_l2(np64(ST), rS) <= tol
+    gdn.check_device_error()
+
+
+@pytest.mark.parametrize('fp32', [True, False], ids=['fp32', 'tc'])
+def test_chunk_prefill_zero_state_bf16_io(fp32):
+    shape = SHAPES[0]
+    c = I.make_core_inputs(42, [300], shape, dtype=torch.bfloat16)
+    gt, bt = _core_gates(c)
+    o, ST = gdn.chunk_prefill(cuda(c.q), cuda(c.k), cuda(c.v), cuda(gt), cuda(bt), 1 / math.sqrt(128),
+                              out_dtype=torch.bfloat16, fp32=fp32)
+    ro, rS = O.recurrent_gated_delta_rule(np64(c.q), np64(c.k), np64(c.v), np64(gt), np64(bt),
+                                          1 / math.sqrt(128))
+    assert rel_l2(np64(o), ro) <= TOL_BF16
+    assert rel_l2(np64(ST), rS) <= TOL_BF16 if not fp32 else TOL_F32
+
+
+def test_chunk_in_place_state():
+    shape = SHAPES[0]
+    c = I.make_core_inputs(43, [100, 150], shape, S0_std=0.1)
+    gt, bt = _core_gates(c)
+    cu = c.cu_seqlens()
+    S = cuda(c.S0.clone())
+    o, _ = gdn.chunk_prefill(cuda(c.q), cuda(c.k), cuda(c.v), cuda(gt), cuda(bt), 0.2,
+                             initial_state=S, final_state=S, cu_seqlens=cuda(cu), out_dtype=torch.float32)
+    ro, rS = O.recurrent_gated_delta_rule(np64(c.q), np64(c.k), np64(c.v), np64(gt), np64(bt), 0.2,
+                                          np64(c.S0), cu.numpy())
+    assert rel_l2(np64(S), rS) <= TOL_BF16
+    assert rel_l2(np64(o), ro) <= TOL_BF16
+
+
+def test_tiny_workload_chunked_vs_recurrent():
+    """The tiny fp32 workload: GPU chunk path vs GPU recurrent path vs the oracle."""
+    c = I.workload('tiny_core_t256')
+    sh = c.shape
+    g, beta = gdn.gating(cuda(c.a), cuda(c.b), cuda(c.A_log), cuda(c.dt_bias))
+    o_c, S_c = gdn.chunk_prefill(cuda(c.q), cuda(c.k), cuda(c.v), g, beta, 1 / 8, out_dtype=torch.float32)
+    o_f, S_f = gdn.chunk_prefill(cuda(c.q), cuda(c.k), cuda(c.v), g, beta, 1 / 8,
+                                 out_dtype=torch.float32, fp32=True)
+    state = torch.zeros(1, sh.Nv, sh.Dk, sh.Dv, device='cuda')
+    o_r = gdn.recurrent_decode(cuda(c.q), cuda(c.k), cuda(c.v), g, beta, state, 1 / 8, num_seqs=1,
+                               out_dtype=torch.float32)
+    rg, rb = O.gating(np64(c.a), np64(c.b), np64(c.A_log), np64(c.dt_bias))
+    ro, rS = O.recurrent_gated_delta_rule(np64(c.q), np64(c.k), np64(c.v), rg, rb, 1 / 8)
+    assert rel_l2(np64(o_c), ro) <= TOL_BF16 and rel_l2(np64(S_c), rS) <= TOL_BF16
+    assert rel_l2(np64(o_f), ro) <= TOL_F32 and rel_l2(np64(S_f), rS) <= TOL_F32
+    assert rel_l2(np64(o_r), ro) <= TOL_F32 and rel_l2(np64(state), rS) <= TOL_F32
+    assert rel_l2(np64(o_c), np64(o_r)) <= TOL_BF16
+
+
+# ------------------------------------------------------------------ whole prefill path
+
+def test_mixer_prefill_small_end_to_end():
+    shape = SHAPES[0]
+    inp = I.make_mixer_inputs(51, [90, 1, 200], shape, conv_state_std=1.0, S0_std=0.05)
+    sh = inp.shape
+    cu = inp.cu_seqlens()
+    cs_out = torch.empty(inp.num_seqs, sh.C, 3, dtype=torch.bfloat16, device='cuda')
+    y, S = gdn.mixer_prefill(cuda(inp.mixed_qkv), cuda(inp.conv_w), cuda(inp.a), cuda(inp.b),
+                             cuda(inp.A_log), cuda(inp.dt_bias), cuda(inp.z), cuda(inp.norm_w),
+                             sh.Nk, sh.Nv, sh.Dk, sh.Dv, cu_seqlens=cuda(cu),
+                             conv_state_in=cuda(inp.conv_state), conv_state_out=cs_out,
+                             initial_state=cuda(inp.S0), out_dtype=torch.float32)
+    ref = O.mixer_prefill(np64(inp.mixed_qkv), np64(inp.conv_w), np64(inp.a), np64(inp.b),
+                          np64(inp.A_log), np64(inp.dt_bias), np64(inp.z), np64(inp.norm_w),
+                          sh.Nk, sh.Nv, sh.Dk, sh.Dv, cu_seqlens=cu.numpy(),
+                          conv_state=np64(inp.conv_state), initial_state=np64(inp.S0))
+    assert rel_l2(np64(y), ref['y']) <= TOL_BF16
+    assert rel_l2(np64(S), ref['state']) <= TOL_BF16
+    np.testing.assert_array_equal(np64(cs_out), ref['conv_state'])
+
+
+def test_device_error_flag_on_bad_cu_seqlens():
+    """A non-monotone cu_seqlens is caught on the device, skipped and reported."""
+    shape = SHAPES[1]
+    c = I.make_core_inputs(44, [10, 10], shape)
+    gt, bt = _core_gates(c)
+    bad = torch.tensor([0, 15, 12], dtype=torch.int32)     # second sequence ends before it starts
+    gdn.chunk_prefill(cuda(c.q), cuda(c.k), cuda(c.v), cuda(gt), cuda(bt), 1.0,
+                      cu_seqlens=cuda(bad), out_dtype=torch.float32)
+    with pytest.raises(RuntimeError, match='device error'):
+        gdn.check_device_error()
+    gdn.check_device_error()      # the flag was cleared
