@@ -234,7 +234,10 @@ int gdn_chunk_prefill(const gdn_dims* dims, const int32_t* cu_seqlens, const voi
   p.scale = scale;
   p.workspace = workspace;
   p.workspace_bytes = workspace_bytes;
-  cudaError_t e = gdn::launch_chunk_simt(p, static_cast<cudaStream_t>(stream));
+  // bf16 q/k/v with 128-wide heads run on the tensor cores; fp32 inputs and
+  // other head sizes run the fp32 CUDA-core kernel.
+  cudaError_t e = gdn::chunk_tc_supported(p) ? gdn::launch_chunk_tc(p, static_cast<cudaStream_t>(stream))
+                                             : gdn::launch_chunk_simt(p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, fn);
   return GDN_OK;
 }

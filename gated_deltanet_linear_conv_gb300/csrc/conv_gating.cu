@@ -4,12 +4,12 @@
 // ("Qwen3.5 Dense Model Architecture", section Linear Attention, forward
 // listing; "Qwen3.5 Simulation Support Design Document", section 2.2 ops 2-3.)
 //
-// Memory-bound.  One warp owns a strip of 128 channels (4 per lane, 8-byte
-// bf16 / 16-byte fp32 loads) over a block of TB tokens; the 3-token left halo
-// is read from the previous rows (L2 hits) or, for the first 3 tokens of a
-// sequence, from the conv state.  A strip never straddles a q/k/v region and
-// holds whole heads, so the per-head L2-norm is a shuffle reduction over
-// Dk/4 lanes.
+// Memory-bound.  One warp owns a strip of 32*CPL channels (CPL per lane:
+// 16-byte accesses) over a block of TB tokens and slides a 4-row window down
+// the block; the 3-row left halo is re-read from the previous rows (L2 hits)
+// or, for the first 3 tokens of a sequence, from the conv state.  A strip
+// never straddles a q/k/v region and holds whole heads, so the per-head
+// L2-norm is a shuffle reduction over Dk/CPL lanes.
 
 #include "common.cuh"
 #include "launch.h"
@@ -17,103 +17,137 @@
 namespace gdn {
 namespace {
 
-constexpr int TB = 16;          // tokens per warp work item
 constexpr int WARPS = 8;
 
-template <typename Tin, typename Tout>
+template <int CPL> struct Vec;
+template <> struct Vec<4> {
+  template <typename T> static __device__ __forceinline__ void ld(const T* p, float (&f)[4]) { load4(p, f); }
+  template <typename T> static __device__ __forceinline__ void st(T* p, const float (&f)[4]) { store4(p, f); }
+};
+template <> struct Vec<8> {
+  template <typename T> static __device__ __forceinline__ void ld(const T* p, float (&f)[8]) { load8(p, f); }
+  template <typename T> static __device__ __forceinline__ void st(T* p, const float (&f)[8]) { store8(p, f); }
+};
+
+template <typename Tin, typename Tout, int CPL, int TB>
 __global__ void __launch_bounds__(WARPS * 32)
 conv_gating_kernel(ConvGatingArgs p) {
+  constexpr int STRIP = 32 * CPL;
   const int lane = threadIdx.x & 31;
   const int warp_global = blockIdx.x * WARPS + (threadIdx.x >> 5);
-  const int nstrips = p.C / 128;
+  const int nstrips = p.C / STRIP;
   const int ntb = (p.total + TB - 1) / TB;
   if (warp_global >= nstrips * ntb) return;
   const int strip = warp_global % nstrips;
   const int tb = warp_global / nstrips;
   const int t0 = tb * TB;
   const int t_end = min(t0 + TB, p.total);
-  const int c0 = strip * 128 + lane * 4;       // first of my 4 channels
+  const int c0 = strip * STRIP + lane * CPL;       // first of my CPL channels
 
   const Tin* x = static_cast<const Tin*>(p.x);
-  const Tin* w = static_cast<const Tin*>(p.w);
-  float wt[4][4];                              // [channel][tap]
-#pragma unroll
-  for (int c = 0; c < 4; ++c) load4(w + (size_t)(c0 + c) * 4, wt[c]);
-  float bias[4] = {0.f, 0.f, 0.f, 0.f};
-  if (p.bias) load4(static_cast<const Tin*>(p.bias) + c0, bias);
-
-  // rows t0-3 .. t0+TB-1 of my 4 channels
-  float win[TB + 3][4];
+  // rows t0-3 .. t0+TB-1, all loads issued before any use
+  float win[TB + 3][CPL];
 #pragma unroll
   for (int r = 0; r < TB + 3; ++r) {
-    int t = t0 - 3 + r;
+    const int t = t0 - 3 + r;
     if (t >= 0 && t < t_end) {
-      load4(x + (size_t)t * p.C + c0, win[r]);
+      Vec<CPL>::ld(x + (size_t)t * p.C + c0, win[r]);
     } else {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) win[r][c] = 0.f;
+      for (int c = 0; c < CPL; ++c) win[r][c] = 0.f;
+    }
+  }
+  float wt[4][CPL];                              // [tap][channel]
+  {
+    const Tin* w = static_cast<const Tin*>(p.w) + (size_t)c0 * 4;
+#pragma unroll
+    for (int c = 0; c < CPL; c += 2) {
+      float tmp[8];
+      load8(w + c * 4, tmp);                     // taps of channels c and c + 1
+#pragma unroll
+      for (int j = 0; j < 4; ++j) { wt[j][c] = tmp[j]; wt[j][c + 1] = tmp[4 + j]; }
+    }
+  }
+  float bias[CPL];
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) bias[c] = 0.f;
+  if (p.bias) Vec<CPL>::ld(static_cast<const Tin*>(p.bias) + c0, bias);
+
+  // Tokens of this block in the first 3 positions of their sequence take part
+  // of their left context from the conv state (bitmask of those tokens).
+  const int kd = p.Nk * p.Dk;
+  const int region = c0 < kd ? 0 : (c0 < 2 * kd ? 1 : 2);   // q, k, v
+  uint32_t near_start = 0;                                   // bit r: token t0 + r has pos < 3
+  {
+    int seq = find_seq(p.cu, p.num_seqs, p.total, max(t0 - 3, 0));
+    for (int s = seq; s < p.num_seqs; ++s) {
+      const int st = seq_start(p.cu, p.num_seqs, p.total, s);
+      if (st >= t_end) break;
+      for (int r = max(st - t0, 0); r < min(st + 3 - t0, TB); ++r) near_start |= 1u << r;
     }
   }
 
-  const int kd = p.Nk * p.Dk;
-  const int region = c0 < kd ? 0 : (c0 < 2 * kd ? 1 : 2);   // q, k, v
   const Tin* st_in = static_cast<const Tin*>(p.state_in);
-
-  int seq = find_seq(p.cu, p.num_seqs, p.total, t0);
-  int sstart = seq_start(p.cu, p.num_seqs, p.total, seq);
-  int snext = seq + 1 < p.num_seqs ? seq_start(p.cu, p.num_seqs, p.total, seq + 1) : p.total;
-
+  Tout* qout = static_cast<Tout*>(p.q);
+  Tout* kout = static_cast<Tout*>(p.k);
+  Tout* vout = static_cast<Tout*>(p.v);
+  const int vd = p.Nv * p.Dv;
 #pragma unroll
   for (int r = 0; r < TB; ++r) {
     const int t = t0 + r;
     if (t >= t_end) break;
-    while (t >= snext && seq + 1 < p.num_seqs) {
-      ++seq;
-      sstart = snext;
-      snext = seq + 1 < p.num_seqs ? seq_start(p.cu, p.num_seqs, p.total, seq + 1) : p.total;
-    }
-    const int pos = t - sstart;             // position inside the sequence
-    float y[4];
+    float y[CPL];
+    if (!(near_start >> r & 1u)) {
 #pragma unroll
-    for (int c = 0; c < 4; ++c) y[c] = bias[c];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {          // tap j reads xpad[pos + j]
-      float xv[4];
-      if (pos + j >= 3) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) xv[c] = win[r + j][c];
-      } else {
-        const int si = pos + j;            // 0..2, inside the cached context
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          xv[c] = (st_in != nullptr && si >= 0)
-                      ? to_f32(st_in[((size_t)seq * p.C + c0 + c) * 3 + si]) : 0.f;
+      for (int c = 0; c < CPL; ++c) {
+        float acc = bias[c];
+        acc = fmaf(wt[0][c], win[r][c], acc);
+        acc = fmaf(wt[1][c], win[r + 1][c], acc);
+        acc = fmaf(wt[2][c], win[r + 2][c], acc);
+        acc = fmaf(wt[3][c], win[r + 3][c], acc);
+        y[c] = acc;
       }
+    } else {
+      // first 3 tokens of a sequence: taps before the sequence start read the state
+      const int seq = find_seq(p.cu, p.num_seqs, p.total, t);
+      const int pos = t - seq_start(p.cu, p.num_seqs, p.total, seq);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) y[c] = fmaf(wt[c][j], xv[c], y[c]);
+      for (int c = 0; c < CPL; ++c) {
+        float acc = bias[c];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float xv = win[r + j][c];
+          if (pos + j < 3) {
+            const int si = pos + j;
+            xv = (st_in != nullptr && si >= 0) ? to_f32(st_in[((size_t)seq * p.C + c0 + c) * 3 + si]) : 0.f;
+          }
+          acc = fmaf(wt[j][c], xv, acc);
+        }
+        y[c] = acc;
+      }
     }
 #pragma unroll
-    for (int c = 0; c < 4; ++c) y[c] = siluf_(y[c]);
-
+    for (int c = 0; c < CPL; ++c) y[c] = silu_fast(y[c]);
     if (region < 2) {
-      float ss = y[0] * y[0] + y[1] * y[1] + y[2] * y[2] + y[3] * y[3];
-      ss = group_sum(ss, p.Dk / 4);
-      float inv = 1.0f / sqrtf(ss + p.l2_eps);
+      float ss = 0.f;
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) ss = fmaf(y[c], y[c], ss);
+      ss = group_sum(ss, p.Dk / CPL);
+      float inv = rsqrtf(ss + p.l2_eps);
       if (region == 0) inv *= p.q_scale;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) y[c] *= inv;
-      Tout* dst = static_cast<Tout*>(region == 0 ? p.q : p.k);
-      store4(dst + (size_t)t * kd + (c0 - region * kd), y);
+      for (int c = 0; c < CPL; ++c) y[c] *= inv;
+      Tout* dst = region == 0 ? qout : kout;
+      Vec<CPL>::st(dst + (size_t)t * kd + (c0 - region * kd), y);
     } else {
-      const int vd = p.Nv * p.Dv;
-      store4(static_cast<Tout*>(p.v) + (size_t)t * vd + (c0 - 2 * kd), y);
+      Vec<CPL>::st(vout + (size_t)t * vd + (c0 - 2 * kd), y);
     }
   }
 
   // gates: the warps of v strips also produce g and beta of their heads
   if (region == 2) {
-    const int hps = 128 / p.Dv;                      // heads per strip
-    const int h0 = (strip * 128 - 2 * kd) / p.Dv;
+    const int hps = STRIP / p.Dv;                      // heads per strip
+    const int h0 = (strip * STRIP - 2 * kd) / p.Dv;
     const Tin* a = static_cast<const Tin*>(p.a);
     const Tin* b = static_cast<const Tin*>(p.b);
     for (int idx = lane; idx < TB * hps; idx += 32) {
@@ -160,16 +194,26 @@ __global__ void conv_state_kernel(ConvGatingArgs p) {
   for (int i = 0; i < 3; ++i) sout[((size_t)s * p.C + c) * 3 + i] = nw[i];
 }
 
-template <typename Tin, typename Tout>
-cudaError_t launch_typed(const ConvGatingArgs& p, cudaStream_t s) {
-  const int nstrips = p.C / 128;
+template <typename Tin, typename Tout, int CPL, int TB>
+cudaError_t launch_main(const ConvGatingArgs& p, cudaStream_t s) {
+  const int nstrips = p.C / (32 * CPL);
   const long long items = (long long)nstrips * ((p.total + TB - 1) / TB);
   if (items > 0) {
     const int blocks = (int)((items + WARPS - 1) / WARPS);
-    conv_gating_kernel<Tin, Tout><<<blocks, WARPS * 32, 0, s>>>(p);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    conv_gating_kernel<Tin, Tout, CPL, TB><<<blocks, WARPS * 32, 0, s>>>(p);
+    return cudaGetLastError();
   }
+  return cudaSuccess;
+}
+
+template <typename Tin, typename Tout>
+cudaError_t launch_typed(const ConvGatingArgs& p, cudaStream_t s) {
+  const int kd = p.Nk * p.Dk, vd = p.Nv * p.Dv;
+  cudaError_t e;
+  // 8 channels per lane when every region holds whole 256-channel strips
+  if (kd % 256 == 0 && vd % 256 == 0) e = launch_main<Tin, Tout, 8, 8>(p, s);
+  else e = launch_main<Tin, Tout, 4, 16>(p, s);
+  if (e != cudaSuccess) return e;
   if (p.state_out != nullptr) {
     dim3 grid((p.C + 255) / 256, p.num_seqs);
     conv_state_kernel<Tin><<<grid, 256, 0, s>>>(p);

@@ -81,5 +81,8 @@ struct ChunkArgs {
 };
 // Portable fp32 CUDA-core implementation of the chunk form.
 cudaError_t launch_chunk_simt(const ChunkArgs& p, cudaStream_t s);
+// tcgen05 tensor-core implementation (bf16 q/k/v, Dk = Dv = 128).
+bool chunk_tc_supported(const ChunkArgs& p);
+cudaError_t launch_chunk_tc(const ChunkArgs& p, cudaStream_t s);
 
 }  // namespace gdn

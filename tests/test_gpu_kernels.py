@@ -199,7 +199,10 @@ def _core_gates(c):
 @pytest.mark.parametrize('shape', SHAPES, ids=['d128', 'd64'])
 @pytest.mark.parametrize('lengths', CHUNK_LENGTHS, ids=lambda L: 'L' + '_'.join(map(str, L)))
 def test_chunk_prefill_varlen(fp32, shape, lengths):
-    c = I.make_core_inputs(41, lengths, shape, S0_std=0.1)
+    # the main entry point takes bf16 q/k/v (tensor cores at 128-wide heads);
+    # the fp32 entry point takes fp32 q/k/v.  The oracle sees the same values.
+    c = I.make_core_inputs(41, lengths, shape, dtype=torch.float32 if fp32 else torch.bfloat16,
+                           S0_std=0.1)
     gt, bt = _core_gates(c)
     cu = c.cu_seqlens()
     o, ST = gdn.chunk_prefill(cuda(c.q), cuda(c.k), cuda(c.v), cuda(gt), cuda(bt), 0.2,
