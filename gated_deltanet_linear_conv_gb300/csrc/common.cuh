@@ -79,9 +79,9 @@ __device__ __forceinline__ void store8(float* p, const float (&f)[8]) {
   *reinterpret_cast<float4*>(p + 4) = make_float4(f[4], f[5], f[6], f[7]);
 }
 
-// x * sigmoid(x) with the fast exponential and a rounded reciprocal (a few
-// ulp; for very negative x the denominator overflows to inf and the result is -0).
-__device__ __forceinline__ float silu_fast(float x) { return x * __frcp_rn(1.0f + __expf(-x)); }
+// x * sigmoid(x) with the fast exponential and divide (a few ulp; for very
+// negative x the denominator overflows to inf and the fast divide returns 0).
+__device__ __forceinline__ float silu_fast(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
 
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(bf16 x) { return __bfloat162float(x); }

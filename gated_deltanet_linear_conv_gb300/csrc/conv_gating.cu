@@ -4,12 +4,14 @@
 // ("Qwen3.5 Dense Model Architecture", section Linear Attention, forward
 // listing; "Qwen3.5 Simulation Support Design Document", section 2.2 ops 2-3.)
 //
-// Memory-bound.  One warp owns a strip of 32*CPL channels (CPL per lane:
-// 16-byte accesses) over a block of TB tokens and slides a 4-row window down
-// the block; the 3-row left halo is re-read from the previous rows (L2 hits)
-// or, for the first 3 tokens of a sequence, from the conv state.  A strip
-// never straddles a q/k/v region and holds whole heads, so the per-head
-// L2-norm is a shuffle reduction over Dk/CPL lanes.
+// Memory-bound.  One warp owns a strip of 128 channels (4 per lane) over TB
+// consecutive tokens and walks down them with the three previous rows in
+// registers and the next PF rows already in flight, so each input row is read
+// once from DRAM (plus a 3-row halo per TB tokens) with few registers and many
+// resident warps.  Tokens in the first 3 positions of a sequence take their
+// left context from the conv state.  A strip never straddles a q/k/v region
+// and holds whole heads, so the per-head L2-norm is a shuffle reduction over
+// Dk/4 lanes.
 
 #include "common.cuh"
 #include "launch.h"
@@ -18,68 +20,71 @@ namespace gdn {
 namespace {
 
 constexpr int WARPS = 8;
+constexpr int TB = 32;      // tokens per warp work item
 
-template <int CPL> struct Vec;
-template <> struct Vec<4> {
-  template <typename T> static __device__ __forceinline__ void ld(const T* p, float (&f)[4]) { load4(p, f); }
-  template <typename T> static __device__ __forceinline__ void st(T* p, const float (&f)[4]) { store4(p, f); }
+template <typename T> struct Row4;
+template <> struct Row4<bf16> {
+  static constexpr int PF = 8;        // rows prefetched ahead
+  using R = uint2;
+  static __device__ __forceinline__ R load(const bf16* p) { return *reinterpret_cast<const uint2*>(p); }
+  static __device__ __forceinline__ R zero() { return make_uint2(0u, 0u); }
+  static __device__ __forceinline__ void unpack(R u, float (&f)[4]) {
+    float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+    float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+  }
 };
-template <> struct Vec<8> {
-  template <typename T> static __device__ __forceinline__ void ld(const T* p, float (&f)[8]) { load8(p, f); }
-  template <typename T> static __device__ __forceinline__ void st(T* p, const float (&f)[8]) { store8(p, f); }
+template <> struct Row4<float> {
+  static constexpr int PF = 4;
+  using R = float4;
+  static __device__ __forceinline__ R load(const float* p) { return *reinterpret_cast<const float4*>(p); }
+  static __device__ __forceinline__ R zero() { return make_float4(0.f, 0.f, 0.f, 0.f); }
+  static __device__ __forceinline__ void unpack(R u, float (&f)[4]) { f[0] = u.x; f[1] = u.y; f[2] = u.z; f[3] = u.w; }
 };
 
-template <typename Tin, typename Tout, int CPL, int TB>
-__global__ void __launch_bounds__(WARPS * 32)
+template <typename Tin, typename Tout>
+__global__ void __launch_bounds__(WARPS * 32, 2)
 conv_gating_kernel(ConvGatingArgs p) {
-  constexpr int STRIP = 32 * CPL;
+  using RW = Row4<Tin>;
+  constexpr int PF = RW::PF;
   const int lane = threadIdx.x & 31;
   const int warp_global = blockIdx.x * WARPS + (threadIdx.x >> 5);
-  const int nstrips = p.C / STRIP;
+  const int nstrips = p.C / 128;
   const int ntb = (p.total + TB - 1) / TB;
   if (warp_global >= nstrips * ntb) return;
   const int strip = warp_global % nstrips;
   const int tb = warp_global / nstrips;
   const int t0 = tb * TB;
   const int t_end = min(t0 + TB, p.total);
-  const int c0 = strip * STRIP + lane * CPL;       // first of my CPL channels
+  const int c0 = strip * 128 + lane * 4;           // first of my 4 channels
+  const Tin* x = static_cast<const Tin*>(p.x) + c0;
+  const size_t C = (size_t)p.C;
 
-  const Tin* x = static_cast<const Tin*>(p.x);
-  // rows t0-3 .. t0+TB-1, all loads issued before any use
-  float win[TB + 3][CPL];
+  // the next PF rows go in flight first
+  typename RW::R buf[PF];
 #pragma unroll
-  for (int r = 0; r < TB + 3; ++r) {
-    const int t = t0 - 3 + r;
-    if (t >= 0 && t < t_end) {
-      Vec<CPL>::ld(x + (size_t)t * p.C + c0, win[r]);
-    } else {
+  for (int i = 0; i < PF; ++i) buf[i] = (t0 + i < t_end) ? RW::load(x + (size_t)(t0 + i) * C) : RW::zero();
+  // the three rows before the block (a sequence start inside the window is patched below)
+  float xm[3][4];
 #pragma unroll
-      for (int c = 0; c < CPL; ++c) win[r][c] = 0.f;
+  for (int j = 0; j < 3; ++j) {
+    const int t = t0 - 3 + j;
+    if (t >= 0) RW::unpack(RW::load(x + (size_t)t * C), xm[j]);
+    else {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) xm[j][c] = 0.f;
     }
   }
-  float wt[4][CPL];                              // [tap][channel]
-  {
-    const Tin* w = static_cast<const Tin*>(p.w) + (size_t)c0 * 4;
+  float wt[4][4];                                  // [channel][tap]
 #pragma unroll
-    for (int c = 0; c < CPL; c += 2) {
-      float tmp[8];
-      load8(w + c * 4, tmp);                     // taps of channels c and c + 1
-#pragma unroll
-      for (int j = 0; j < 4; ++j) { wt[j][c] = tmp[j]; wt[j][c + 1] = tmp[4 + j]; }
-    }
-  }
-  float bias[CPL];
-#pragma unroll
-  for (int c = 0; c < CPL; ++c) bias[c] = 0.f;
-  if (p.bias) Vec<CPL>::ld(static_cast<const Tin*>(p.bias) + c0, bias);
+  for (int c = 0; c < 4; ++c) load4(static_cast<const Tin*>(p.w) + (size_t)(c0 + c) * 4, wt[c]);
+  float bias[4] = {0.f, 0.f, 0.f, 0.f};
+  if (p.bias) load4(static_cast<const Tin*>(p.bias) + c0, bias);
 
-  // Tokens of this block in the first 3 positions of their sequence take part
-  // of their left context from the conv state (bitmask of those tokens).
-  const int kd = p.Nk * p.Dk;
-  const int region = c0 < kd ? 0 : (c0 < 2 * kd ? 1 : 2);   // q, k, v
-  uint32_t near_start = 0;                                   // bit r: token t0 + r has pos < 3
+  // tokens of this block in the first 3 positions of their sequence (bit r)
+  uint32_t near_start = 0;
   {
-    int seq = find_seq(p.cu, p.num_seqs, p.total, max(t0 - 3, 0));
+    const int seq = find_seq(p.cu, p.num_seqs, p.total, max(t0 - 3, 0));
     for (int s = seq; s < p.num_seqs; ++s) {
       const int st = seq_start(p.cu, p.num_seqs, p.total, s);
       if (st >= t_end) break;
@@ -87,67 +92,102 @@ conv_gating_kernel(ConvGatingArgs p) {
     }
   }
 
+  const int kd = p.Nk * p.Dk;
+  const int region = c0 < kd ? 0 : (c0 < 2 * kd ? 1 : 2);   // q, k, v
   const Tin* st_in = static_cast<const Tin*>(p.state_in);
-  Tout* qout = static_cast<Tout*>(p.q);
-  Tout* kout = static_cast<Tout*>(p.k);
-  Tout* vout = static_cast<Tout*>(p.v);
-  const int vd = p.Nv * p.Dv;
+  Tout* dst;
+  size_t row_stride;
+  if (region < 2) {
+    dst = static_cast<Tout*>(region == 0 ? p.q : p.k) + (c0 - region * kd);
+    row_stride = (size_t)kd;
+  } else {
+    dst = static_cast<Tout*>(p.v) + (c0 - 2 * kd);
+    row_stride = (size_t)p.Nv * p.Dv;
+  }
+  const int lanes_per_head = p.Dk / 4;
+  const float qs = region == 0 ? p.q_scale : 1.0f;
+
+  const Tin* xnext = x + (size_t)(t0 + PF) * C;     // row t + PF, advanced one row per token
+  Tout* const dst0 = dst;
+  dst += (size_t)t0 * row_stride;                   // row t
+#pragma unroll 1
+  for (int tt = 0; tt < TB; tt += PF) {
 #pragma unroll
-  for (int r = 0; r < TB; ++r) {
-    const int t = t0 + r;
-    if (t >= t_end) break;
-    float y[CPL];
-    if (!(near_start >> r & 1u)) {
+    for (int i = 0; i < PF; ++i) {
+      const int r = tt + i;
+      const int t = t0 + r;
+      float cur[4];
+      RW::unpack(buf[i], cur);
+      buf[i] = (r + PF < TB && t + PF < t_end) ? RW::load(xnext) : RW::zero();
+      xnext += C;
+      if (t < t_end) {
+        float y[4];
 #pragma unroll
-      for (int c = 0; c < CPL; ++c) {
-        float acc = bias[c];
-        acc = fmaf(wt[0][c], win[r][c], acc);
-        acc = fmaf(wt[1][c], win[r + 1][c], acc);
-        acc = fmaf(wt[2][c], win[r + 2][c], acc);
-        acc = fmaf(wt[3][c], win[r + 3][c], acc);
-        y[c] = acc;
-      }
-    } else {
-      // first 3 tokens of a sequence: taps before the sequence start read the state
-      const int seq = find_seq(p.cu, p.num_seqs, p.total, t);
-      const int pos = t - seq_start(p.cu, p.num_seqs, p.total, seq);
-#pragma unroll
-      for (int c = 0; c < CPL; ++c) {
-        float acc = bias[c];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          float xv = win[r + j][c];
-          if (pos + j < 3) {
-            const int si = pos + j;
-            xv = (st_in != nullptr && si >= 0) ? to_f32(st_in[((size_t)seq * p.C + c0 + c) * 3 + si]) : 0.f;
-          }
-          acc = fmaf(wt[j][c], xv, acc);
+        for (int c = 0; c < 4; ++c) {
+          float acc = bias[c];
+          acc = fmaf(wt[c][0], xm[0][c], acc);
+          acc = fmaf(wt[c][1], xm[1][c], acc);
+          acc = fmaf(wt[c][2], xm[2][c], acc);
+          y[c] = silu_fast(fmaf(wt[c][3], cur[c], acc));
         }
-        y[c] = acc;
+        if (region < 2) {
+          float ss = y[0] * y[0] + y[1] * y[1] + y[2] * y[2] + y[3] * y[3];
+          ss = group_sum(ss, lanes_per_head);
+          const float inv = rsqrtf(ss + p.l2_eps) * qs;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) y[c] *= inv;
+        }
+        store4(dst, y);
       }
+      dst += row_stride;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) { xm[0][c] = xm[1][c]; xm[1][c] = xm[2][c]; xm[2][c] = cur[c]; }
+    }
+  }
+
+  // Tokens in the first 3 positions of a sequence were computed above with
+  // the previous sequence's rows as left context; redo them with the conv state.
+  while (near_start) {
+    const int r = __ffs(near_start) - 1;
+    near_start &= near_start - 1;
+    const int t = t0 + r;
+    const int seq = find_seq(p.cu, p.num_seqs, p.total, t);
+    const int pos = t - seq_start(p.cu, p.num_seqs, p.total, seq);
+    float y[4];
+    float cur[4];
+    RW::unpack(RW::load(x + (size_t)t * C), cur);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) y[c] = fmaf(wt[c][3], cur[c], bias[c]);
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+      const int si = pos + j;                 // index into [state(3) ; sequence]
+      float xv[4];
+      if (si < 3) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          xv[c] = (st_in != nullptr && si >= 0) ? to_f32(st_in[((size_t)seq * C + c0 + c) * 3 + si]) : 0.f;
+      } else {
+        RW::unpack(RW::load(x + (size_t)(t - 3 + j) * C), xv);
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) y[c] = fmaf(wt[c][j], xv[c], y[c]);
     }
 #pragma unroll
-    for (int c = 0; c < CPL; ++c) y[c] = silu_fast(y[c]);
+    for (int c = 0; c < 4; ++c) y[c] = silu_fast(y[c]);
     if (region < 2) {
-      float ss = 0.f;
+      float ss = y[0] * y[0] + y[1] * y[1] + y[2] * y[2] + y[3] * y[3];
+      ss = group_sum(ss, lanes_per_head);
+      const float inv = rsqrtf(ss + p.l2_eps) * qs;
 #pragma unroll
-      for (int c = 0; c < CPL; ++c) ss = fmaf(y[c], y[c], ss);
-      ss = group_sum(ss, p.Dk / CPL);
-      float inv = rsqrtf(ss + p.l2_eps);
-      if (region == 0) inv *= p.q_scale;
-#pragma unroll
-      for (int c = 0; c < CPL; ++c) y[c] *= inv;
-      Tout* dst = region == 0 ? qout : kout;
-      Vec<CPL>::st(dst + (size_t)t * kd + (c0 - region * kd), y);
-    } else {
-      Vec<CPL>::st(vout + (size_t)t * vd + (c0 - 2 * kd), y);
+      for (int c = 0; c < 4; ++c) y[c] *= inv;
     }
+    store4(dst0 + (size_t)t * row_stride, y);
   }
 
   // gates: the warps of v strips also produce g and beta of their heads
   if (region == 2) {
-    const int hps = STRIP / p.Dv;                      // heads per strip
-    const int h0 = (strip * STRIP - 2 * kd) / p.Dv;
+    const int hps = 128 / p.Dv;                      // heads per strip
+    const int h0 = (strip * 128 - 2 * kd) / p.Dv;
     const Tin* a = static_cast<const Tin*>(p.a);
     const Tin* b = static_cast<const Tin*>(p.b);
     for (int idx = lane; idx < TB * hps; idx += 32) {
@@ -194,26 +234,15 @@ __global__ void conv_state_kernel(ConvGatingArgs p) {
   for (int i = 0; i < 3; ++i) sout[((size_t)s * p.C + c) * 3 + i] = nw[i];
 }
 
-template <typename Tin, typename Tout, int CPL, int TB>
-cudaError_t launch_main(const ConvGatingArgs& p, cudaStream_t s) {
-  const int nstrips = p.C / (32 * CPL);
-  const long long items = (long long)nstrips * ((p.total + TB - 1) / TB);
-  if (items > 0) {
-    const int blocks = (int)((items + WARPS - 1) / WARPS);
-    conv_gating_kernel<Tin, Tout, CPL, TB><<<blocks, WARPS * 32, 0, s>>>(p);
-    return cudaGetLastError();
-  }
-  return cudaSuccess;
-}
-
 template <typename Tin, typename Tout>
 cudaError_t launch_typed(const ConvGatingArgs& p, cudaStream_t s) {
-  const int kd = p.Nk * p.Dk, vd = p.Nv * p.Dv;
-  cudaError_t e;
-  // 8 channels per lane when every region holds whole 256-channel strips
-  if (kd % 256 == 0 && vd % 256 == 0) e = launch_main<Tin, Tout, 8, 8>(p, s);
-  else e = launch_main<Tin, Tout, 4, 16>(p, s);
-  if (e != cudaSuccess) return e;
+  const long long items = (long long)(p.C / 128) * ((p.total + TB - 1) / TB);
+  if (items > 0) {
+    const int blocks = (int)((items + WARPS - 1) / WARPS);
+    conv_gating_kernel<Tin, Tout><<<blocks, WARPS * 32, 0, s>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   if (p.state_out != nullptr) {
     dim3 grid((p.C + 255) / 256, p.num_seqs);
     conv_state_kernel<Tin><<<grid, 256, 0, s>>>(p);

@@ -14,10 +14,10 @@
 namespace gdn {
 namespace {
 
-constexpr int UNROLL = 4;
+constexpr int UNROLL = 2;
 
 template <typename Tx, typename Tz, typename Ty>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 3)
 gated_rmsnorm_kernel(RmsNormArgs p) {
   const int lanes_per_row = p.dim / 8;
   const int rows_per_step = 32 / lanes_per_row;          // rows per warp per unrolled step
