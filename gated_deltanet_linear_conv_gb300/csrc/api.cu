@@ -185,7 +185,11 @@ int gdn_gating(int64_t rows, int32_t num_v_heads, const void* a, const void* b, 
 int gdn_chunk_prefill_workspace_size(const gdn_dims* dims, size_t* bytes) {
   const char* fn = "gdn_chunk_prefill_workspace_size";
   if (dims == nullptr || bytes == nullptr) return fail(GDN_ERR_INVALID_ARG, "%s: NULL argument", fn);
-  *bytes = 0;
+  int st = check_dims(fn, dims, nullptr);
+  if (st != GDN_OK && st != GDN_ERR_INVALID_ARG) return st;   // equal split not required here
+  *bytes = (dims->head_k_dim == 128 && dims->head_v_dim == 128)
+               ? gdn::chunk_tc_workspace_bytes(dims->num_seqs, dims->total_tokens, dims->num_v_heads)
+               : 0;
   return GDN_OK;
 }
 
@@ -236,8 +240,15 @@ int gdn_chunk_prefill(const gdn_dims* dims, const int32_t* cu_seqlens, const voi
   p.workspace_bytes = workspace_bytes;
   // bf16 q/k/v with 128-wide heads run on the tensor cores; fp32 inputs and
   // other head sizes run the fp32 CUDA-core kernel.
-  cudaError_t e = gdn::chunk_tc_supported(p) ? gdn::launch_chunk_tc(p, static_cast<cudaStream_t>(stream))
-                                             : gdn::launch_chunk_simt(p, static_cast<cudaStream_t>(stream));
+  const bool tc = gdn::chunk_tc_supported(p);
+  if (tc && dims->total_tokens > 0) {
+    const size_t need = gdn::chunk_tc_workspace_bytes(dims->num_seqs, dims->total_tokens, dims->num_v_heads);
+    if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))
+      return fail(GDN_ERR_INVALID_ARG, "%s: workspace of %zu bytes (16-byte aligned) required, got %zu", fn,
+                  need, workspace_bytes);
+  }
+  cudaError_t e = tc ? gdn::launch_chunk_tc(p, static_cast<cudaStream_t>(stream))
+                     : gdn::launch_chunk_simt(p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, fn);
   return GDN_OK;
 }

@@ -5,22 +5,30 @@
 // "Qwen3.5 Dense Model Architecture", section Linear Attention:
 // chunk_gated_delta_rule with initial and final state.)
 //
-// Per chunk of L <= 64 tokens with entry state S (fp32, [Dk, Dv], resident in
-// tensor memory) and G = cumsum(g), gamma = exp(G):
-//   D1   = [Q; K] K^T                             (128 x 64 x 128)
-//   P    = M o QK^T,  A = diag(beta) (M' o KK^T)   (M: exp(G_r - G_j), j <= r / j < r)
-//   T    = (I + A)^-1                             (fp32, CUDA cores)
-//   U~^T = V^T (T diag beta)^T,  W^T = K^T (T diag(beta gamma))^T    (128 x 64 x 64 each)
-//   U^T  = U~^T - S^T W^T                         (128 x 64 x 128, negated A operand)
-//   O    = diag(gamma) Q S + P U                  (64 x 128 x 128 + 64 x 128 x 64)
-//   S   <- gamma_L S + (diag(exp(G_L - G)) K)^T U (128 x 128 x 64, accumulated on the
-//          gamma_L-scaled state in tensor memory)
+// Per chunk of L <= 64 tokens with entry state S (fp32, [Dk, Dv]) and
+// G = cumsum(g), gamma = exp(G):
+//   A    = diag(beta) (M' o K K^T)                 M'[r,j] = exp(G_r - G_j), j < r
+//   T    = (I + A)^-1
+//   U~^T = V^T (T diag beta)^T,  W^T = K^T (T diag(beta gamma))^T
+//   U^T  = U~^T - S^T W^T
+//   O^T  = S^T (diag(gamma) Q)^T + U^T P^T,  P = M o Q K^T   (M[r,j] = exp(G_r - G_j), j <= r)
+//   S   <- gamma_L S + (diag(exp(G_L - G)) K)^T U
 // Padding rows beyond L get beta = g = 0, which makes them exact identities.
 //
-// One CTA (128 threads) per (sequence, value head).  Thread 0 issues the TMA
-// loads and the MMAs; all four warps run the tensor-memory epilogues and the
-// triangular inverse.  Every mbarrier wait is bounded; on a timeout the CTA
-// raises the device error flag, drains and releases its tensor memory.
+// Two launches:
+//  * chunk_solve_kernel, parallel over every (chunk, value head): K K^T on
+//    the tensor core, A, and T = (I + A)^-1 in fp32 on CUDA cores; writes
+//    T diag(beta) and T diag(beta gamma) as bf16 128-byte-swizzled tiles to
+//    the workspace (16 KB per chunk and head).
+//  * chunk_scan_kernel, one CTA per (sequence, value head), walks the chunks
+//    with the state resident in tensor memory.  Three warpgroups run as a
+//    pipeline: PREP (TMA, Q K^T and the T products, P, the scaled Q and K
+//    tiles, W) works one chunk ahead of STATE (the S-dependent products and
+//    their epilogues), and OUT stores each chunk's output rows.  Every product
+//    is an M = 128 tcgen05.mma with Dv or Dk on the tensor-memory lanes.
+// Every mbarrier wait is bounded; on a timeout the CTA raises the device
+// error flag, lets its outstanding copies and products land, releases its
+// tensor memory and exits.
 
 #include <cuda.h>
 
@@ -36,37 +44,13 @@ using namespace tc;
 constexpr int CT = 64;        // chunk length
 constexpr int DK = 128;
 constexpr int DV = 128;
-constexpr int NT = 128;
 constexpr uint32_t WAIT_LIMIT = 1u << 22;
 constexpr int FS = 68;        // fp32 matrix row stride (16-byte aligned rows)
+constexpr uint32_t TILE_T_BYTES = 16384;   // T diag(beta) | T diag(beta gamma), bf16
 
-// shared memory map (bytes from a 1024-aligned base)
-constexpr uint32_t OFF_QK0 = 0;          // [Q box0 | K box0 | Q box1 | K box1], 8 KB each
-constexpr uint32_t OFF_QK1 = 32768;
-constexpr uint32_t OFF_V = 65536;        // [V box0 | V box1]
-constexpr uint32_t OFF_KT = 81920;       // K scaled by exp(G_L - G_j), same layout as the K boxes
-constexpr uint32_t OFF_P = 98304;        // P [r][j] K-major
-constexpr uint32_t OFF_TB = 106496;      // T diag(beta) [r][j]
-constexpr uint32_t OFF_TBG = 114688;     // T diag(beta gamma) [r][j]
-constexpr uint32_t OFF_WMN = 122880;     // W as [dk rows][r], MN-major B
-constexpr uint32_t OFF_UK = 139264;      // U^T as [dv rows][j], K-major
-constexpr uint32_t OFF_SMN = 155648;     // S as [dk rows][dv], two 64-column blocks of 16 KB
-constexpr uint32_t OFF_AF = 188416;      // A fp32 [64][FS]
-constexpr uint32_t OFF_TF = OFF_AF + 64 * FS * 4;   // T fp32 [64][FS]
-constexpr uint32_t OFF_VEC = OFF_TF + 64 * FS * 4;  // G, gamma, beta, dec, beta*gamma (5 x 64 floats)
-constexpr uint32_t OFF_BAR = OFF_VEC + 5 * 64 * 4;  // mbarriers + tmem slot
-constexpr uint32_t SMEM_BYTES = OFF_BAR + 128 + 1024;
-static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-
-// tensor memory columns
-constexpr uint32_t TM_D1 = 0, TM_UT = 64, TM_WT = 128, TM_O = 192, TM_S = 320;
-
-struct Bars {
-  uint64_t qk[2];
-  uint64_t v;
-  uint64_t mma;
-  uint32_t tslot;
-};
+// ---------------------------------------------------------------------------
+// shared helpers
+// ---------------------------------------------------------------------------
 
 // Write 64 bf16 values (v[0..63]) as one 128-byte swizzled row `row` of a
 // 64-column block at byte offset `base`.
@@ -94,12 +78,11 @@ __device__ __forceinline__ void tm_ld64(uint32_t taddr, float (&v)[64]) {
   for (int i = 0; i < 32; ++i) { v[i] = a[i]; v[32 + i] = b[i]; }
 }
 
-// Scale every 16-byte chunk of a swizzled bf16 tile: rows of 128 bytes, the
-// factor of row r is f[r & 63].  `src` may equal `dst`.
-__device__ __forceinline__ void scale_rows(uint8_t* sm, uint32_t src, uint32_t dst, int nbytes, const float* f) {
-  for (int off = threadIdx.x * 16; off < nbytes; off += NT * 16) {
-    const int row = (off >> 7) & 63;
-    uint4 u = *reinterpret_cast<const uint4*>(sm + src + off);
+// Scale the 64 rows of a swizzled 8 KB bf16 box in place: row r times f[r].
+__device__ __forceinline__ void scale_box(uint8_t* sm, uint32_t box, const float* f, int t, int nt) {
+  for (int off = t * 16; off < 8192; off += nt * 16) {
+    const int row = off >> 7;
+    uint4 u = *reinterpret_cast<const uint4*>(sm + box + off);
     const float sc = f[row];
     uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -108,21 +91,41 @@ __device__ __forceinline__ void scale_rows(uint8_t* sm, uint32_t src, uint32_t d
       __nv_bfloat162 y = __floats2bfloat162_rn(x.x * sc, x.y * sc);
       w[i] = *reinterpret_cast<uint32_t*>(&y);
     }
-    *reinterpret_cast<uint4*>(sm + dst + off) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(sm + box + off) = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 
-// Block-uniform bounded wait: every thread polls, then the CTA agrees.
-__device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity) {
-  const bool ok = mbar_wait(bar, parity, WAIT_LIMIT);
-  return __syncthreads_and(ok ? 1 : 0) != 0;
+// Inclusive prefix sum of g over the chunk by one warp (lane l owns l, l+32);
+// writes G, gamma = exp(G) and dec = exp(G_L - G).
+__device__ __forceinline__ void chunk_cumsum(float* Gs, float* Gam, float* Dec, int lane) {
+  float a0 = Gs[lane], a1 = Gs[lane + 32];
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float t0 = __shfl_up_sync(0xffffffffu, a0, off);
+    const float t1 = __shfl_up_sync(0xffffffffu, a1, off);
+    if (lane >= off) { a0 += t0; a1 += t1; }
+  }
+  a1 += __shfl_sync(0xffffffffu, a0, 31);
+  const float gl = __shfl_sync(0xffffffffu, a1, 31);
+  Gs[lane] = a0;
+  Gs[lane + 32] = a1;
+  Gam[lane] = __expf(a0);
+  Gam[lane + 32] = __expf(a1);
+  Dec[lane] = __expf(gl - a0);
+  Dec[lane + 32] = __expf(gl - a1);
 }
 
-// C[i][j] (rows i0 + 2*ti + {0,1}, cols j0 + 4*tj + {0..3}) = sum_k X[xr + i][xc + k] * Y[yr + k][yc + j]
-// over k < K, for a 32 x 32 output split over 128 threads (16 x 8 tiles of 2 x 4).
+// Workspace slot of chunk c of sequence s: floor(bos_s / 64) + s + c.  Slots
+// of different sequences never collide and stay below total / 64 + num_seqs.
+__device__ __forceinline__ int slot_base(const ChunkArgs& p, int s) {
+  return seq_start(p.cu, p.num_seqs, p.total, s) / CT + s;
+}
+
+// C[i][j] (rows 2*ti + {0,1}, cols 4*tj + {0..3}) = sum_k X[xr + i][xc + k] * Y[yr + k][yc + j]
+// over k < K, a 32 x 32 output split over 128 threads (16 x 8 tiles of 2 x 4).
 __device__ __forceinline__ void gemm32_tile(const float* X, int xr, int xc, const float* Y, int yr, int yc,
-                                            int K, float (&acc)[2][4]) {
-  const int ti = threadIdx.x >> 3, tj = threadIdx.x & 7;
+                                            int K, float (&acc)[2][4], int tid) {
+  const int ti = tid >> 3, tj = tid & 7;
 #pragma unroll
   for (int a = 0; a < 2; ++a)
 #pragma unroll
@@ -139,13 +142,12 @@ __device__ __forceinline__ void gemm32_tile(const float* X, int xr, int xc, cons
   }
 }
 
-// T = (I + A)^-1 for a 64 x 64 strictly lower A (fp32, stride FS); T is fully
-// written (zeros above the diagonal).  16 x 16 diagonal blocks by right-looking
-// substitution, then the two 16 -> 32 merges and the 32 -> 64 merge, each
-// T21 = -T22 A21 T11.
-__device__ void invert_unit_lower(const float* AF, float* TF) {
-  const int tid = threadIdx.x;
-  for (int i = tid * 4; i < 64 * FS; i += NT * 4)
+// T = (I + A)^-1 for a 64 x 64 strictly lower A (fp32, stride FS), by 128
+// threads; T is fully written (zeros above the diagonal).  16 x 16 diagonal
+// blocks by right-looking substitution, then the two 16 -> 32 merges and the
+// 32 -> 64 merge, each T21 = -T22 A21 T11.
+__device__ void invert_unit_lower(const float* AF, float* TF, int tid) {
+  for (int i = tid * 4; i < 64 * FS; i += 128 * 4)
     *reinterpret_cast<float4*>(TF + i) = make_float4(0.f, 0.f, 0.f, 0.f);
   __syncthreads();
   if (tid < 64) {
@@ -194,13 +196,13 @@ __device__ void invert_unit_lower(const float* AF, float* TF) {
   {   // 32 -> 64: T[32:64][0:32] = -T[32:64][32:64] (A[32:64][0:32] T[0:32][0:32])
     const int ti = tid >> 3, tj = tid & 7;
     float acc[2][4];
-    gemm32_tile(AF, 32, 0, TF, 0, 0, 32, acc);
+    gemm32_tile(AF, 32, 0, TF, 0, 0, 32, acc, tid);
 #pragma unroll
     for (int a = 0; a < 2; ++a)
       *reinterpret_cast<float4*>(TF + (32 + 2 * ti + a) * FS + 4 * tj) =
           make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
     __syncthreads();
-    gemm32_tile(TF, 32, 32, TF, 32, 0, 32, acc);
+    gemm32_tile(TF, 32, 32, TF, 32, 0, 32, acc, tid);
     __syncthreads();
 #pragma unroll
     for (int a = 0; a < 2; ++a)
@@ -210,207 +212,86 @@ __device__ void invert_unit_lower(const float* AF, float* TF) {
   }
 }
 
-template <typename Tout>
-__global__ void __launch_bounds__(NT, 1)
-chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                const __grid_constant__ CUtensorMap tmv, ChunkArgs p) {
+// ---------------------------------------------------------------------------
+// kernel 1: T tiles, parallel over (chunk slot, value head)
+// ---------------------------------------------------------------------------
+constexpr uint32_t S1_K = 0;                        // K box0 | K box1 (16 KB)
+constexpr uint32_t S1_AF = 16384;                   // A fp32 [64][FS]
+constexpr uint32_t S1_TF = S1_AF + 64 * FS * 4;     // T fp32 [64][FS]
+constexpr uint32_t S1_VEC = S1_TF + 64 * FS * 4;    // G, beta, beta*gamma (3 x 64 floats)
+constexpr uint32_t S1_BAR = S1_VEC + 3 * 64 * 4;
+constexpr uint32_t S1_SMEM = S1_BAR + 64 + 1024;
+
+__global__ void __launch_bounds__(128)
+chunk_solve_kernel(const __grid_constant__ CUtensorMap tmk, ChunkArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* Gs = reinterpret_cast<float*>(sm + OFF_VEC);
-  float* Gam = Gs + CT;
-  float* Bet = Gam + CT;
-  float* Dec = Bet + CT;
-  float* BG = Dec + CT;
-  float* AF = reinterpret_cast<float*>(sm + OFF_AF);
-  float* TF = reinterpret_cast<float*>(sm + OFF_TF);
-  Bars* bars = reinterpret_cast<Bars*>(sm + OFF_BAR);
-
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5;
-  const int lane = tid & 31;
-  const int h = blockIdx.x;
-  const int s = blockIdx.y;
+  float* AF = reinterpret_cast<float*>(sm + S1_AF);
+  float* TF = reinterpret_cast<float*>(sm + S1_TF);
+  float* Gs = reinterpret_cast<float*>(sm + S1_VEC);
+  float* Bet = Gs + CT;
+  float* BG = Bet + CT;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + S1_BAR);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S1_BAR + 16);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int slot = blockIdx.x, h = blockIdx.y;
   const int hk = h / (p.Nv / p.Nk);
-  int bos, eos;
-  if (!seq_bounds(p.cu, p.num_seqs, p.total, s, bos, eos)) {
-    if (tid == 0 && h == 0) raise_error(p.err, kDevErrSeqlens);
-    return;
+
+  // slot -> (sequence, chunk)
+  int lo = 0, hi = p.num_seqs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (slot_base(p, mid) <= slot) lo = mid; else hi = mid - 1;
   }
-  const int nchunks = (eos - bos + CT - 1) / CT;
+  const int s = lo, c = slot - slot_base(p, s);
+  int bos, eos;
+  if (!seq_bounds(p.cu, p.num_seqs, p.total, s, bos, eos)) return;   // reported by the scan kernel
+  if (c < 0 || c * CT >= eos - bos) return;                           // slot not used
+  const int c0 = bos + c * CT, len = min(CT, eos - c0);
 
   if (tid == 0) {
-    mbar_init(&bars->qk[0], 1);
-    mbar_init(&bars->qk[1], 1);
-    mbar_init(&bars->v, 1);
-    mbar_init(&bars->mma, 1);
+    mbar_init(bar, 1);
     fence_barrier_init();
-    prefetch_tmap(&tmq);
-    prefetch_tmap(&tmk);
-    prefetch_tmap(&tmv);
+    mbar_arrive_expect_tx(bar, 16384);
+    tma_load_2d(sm + S1_K, &tmk, bar, hk * DK, c0);
+    tma_load_2d(sm + S1_K + 8192, &tmk, bar, hk * DK + 64, c0);
   }
-  if (warp == 0) tmem_alloc(&bars->tslot, 512);
+  if (warp == 0) tmem_alloc(tslot, 64);
+  if (tid < CT) {
+    Gs[tid] = tid < len ? p.g[(size_t)(c0 + tid) * p.Nv + h] : 0.f;
+    Bet[tid] = tid < len ? p.beta[(size_t)(c0 + tid) * p.Nv + h] : 0.f;
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tbase = bars->tslot;
-  const uint32_t lane_base = tbase + ((uint32_t)(warp * 32) << 16);   // this warp's 32 lanes
-  const uint32_t s_base = smem_u32(sm);
-
-  auto issue_qk = [&](int chunk, int stage) {
-    const int t = bos + chunk * CT;
-    const uint32_t base = (stage ? OFF_QK1 : OFF_QK0);
-    uint64_t* bar = &bars->qk[stage];
-    mbar_arrive_expect_tx(bar, 4 * 8192);
-    tma_load_2d(sm + base, &tmq, bar, hk * DK, t);
-    tma_load_2d(sm + base + 8192, &tmk, bar, hk * DK, t);
-    tma_load_2d(sm + base + 16384, &tmq, bar, hk * DK + 64, t);
-    tma_load_2d(sm + base + 24576, &tmk, bar, hk * DK + 64, t);
-  };
-  auto issue_v = [&](int chunk) {
-    const int t = bos + chunk * CT;
-    mbar_arrive_expect_tx(&bars->v, 2 * 8192);
-    tma_load_2d(sm + OFF_V, &tmv, &bars->v, h * DV, t);
-    tma_load_2d(sm + OFF_V + 8192, &tmv, &bars->v, h * DV + 64, t);
-  };
-  if (tid == 0 && nchunks > 0) {
-    issue_qk(0, 0);
-    issue_v(0);
+  const uint32_t tbase = *tslot;
+  if (warp == 0) {
+    float* Gam = TF;            // scratch for the cumsum helper (TF is rewritten later)
+    float* Dec = TF + 64;
+    chunk_cumsum(Gs, Gam, Dec, lane);
+    BG[lane] = Bet[lane] * Gam[lane];
+    BG[lane + 32] = Bet[lane + 32] * Gam[lane + 32];
   }
-
-  // initial state -> tensor memory (lane = dk row, 128 columns = dv)
-  {
-    const int dk = tid;
-    const float* src = p.S0 ? p.S0 + (((size_t)s * p.Nv + h) * DK + dk) * DV : nullptr;
-#pragma unroll
-    for (int c0 = 0; c0 < DV; c0 += 32) {
-      float v[32];
-#pragma unroll
-      for (int i = 0; i < 32; i += 4) {
-        float4 t4 = src ? *reinterpret_cast<const float4*>(src + c0 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-        v[i] = t4.x; v[i + 1] = t4.y; v[i + 2] = t4.z; v[i + 3] = t4.w;
-      }
-      tmem_st32(lane_base + TM_S + c0, v);
-    }
-    tmem_st_wait();
-  }
-
-  uint32_t ph_qk0 = 0u, ph_qk1 = 0u, ph_v = 0u, ph_mma = 0u;
-  bool ok = true;
-  Tout* o = static_cast<Tout*>(p.o);
-
-  // gates of chunk 0, then always one chunk ahead (threads 0..63 own one token each)
-  float g_next = 0.f, b_next = 0.f;
-  if (tid < CT && nchunks > 0 && tid < eos - bos) {
-    g_next = p.g[(size_t)(bos + tid) * p.Nv + h];
-    b_next = p.beta[(size_t)(bos + tid) * p.Nv + h];
-  }
-
-  for (int c = 0; c < nchunks && ok; ++c) {
-    const int c0 = bos + c * CT;
-    const int len = min(CT, eos - c0);
-    const int stage = c & 1;
-    const uint32_t qk_off = stage ? OFF_QK1 : OFF_QK0;
-
-    // ---- (1) gates of the chunk, cumulative log-decay; prefetch the next chunk's
-    if (tid < CT) {
-      Gs[tid] = g_next;
-      Bet[tid] = b_next;
-      g_next = 0.f;
-      b_next = 0.f;
-      if (c + 1 < nchunks && c0 + CT + tid < eos) {
-        g_next = p.g[(size_t)(c0 + CT + tid) * p.Nv + h];
-        b_next = p.beta[(size_t)(c0 + CT + tid) * p.Nv + h];
-      }
-    }
-    __syncthreads();
-    if (warp == 0) {
-      float a0 = Gs[lane], a1 = Gs[lane + 32];
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const float t0 = __shfl_up_sync(0xffffffffu, a0, off);
-        const float t1 = __shfl_up_sync(0xffffffffu, a1, off);
-        if (lane >= off) { a0 += t0; a1 += t1; }
-      }
-      a1 += __shfl_sync(0xffffffffu, a0, 31);
-      const float gl = __shfl_sync(0xffffffffu, a1, 31);
-      Gs[lane] = a0;
-      Gs[lane + 32] = a1;
-      const float e0 = __expf(a0), e1 = __expf(a1);
-      Gam[lane] = e0;
-      Gam[lane + 32] = e1;
-      BG[lane] = Bet[lane] * e0;
-      BG[lane + 32] = Bet[lane + 32] * e1;
-      Dec[lane] = __expf(gl - a0);
-      Dec[lane + 32] = __expf(gl - a1);
-    }
-    __syncthreads();
-    const float gamma_L = Gam[CT - 1];
-
-    // ---- (2) state epilogue: bf16 S -> smem (MMA operand), gamma_L * S -> tensor memory
-    {
-      const int dk = tid;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        float v[64];
-        tm_ld64(lane_base + TM_S + half * 64, v);
-        st_row64(sm, OFF_SMN + half * 16384, dk, v);
-        float a[32], b[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) { a[i] = v[i] * gamma_L; b[i] = v[32 + i] * gamma_L; }
-        tmem_st32(lane_base + TM_S + half * 64, a);
-        tmem_st32(lane_base + TM_S + half * 64 + 32, b);
-      }
-      tmem_st_wait();
-    }
-
-    // ---- (3) this chunk's q / k tiles
-    if (!wait_all(&bars->qk[stage], stage ? ph_qk1 : ph_qk0)) { ok = false; break; }
-    if (stage) ph_qk1 ^= 1u; else ph_qk0 ^= 1u;
-    if (tid == 0 && c + 1 < nchunks) issue_qk(c + 1, stage ^ 1);
-
-    // ---- (4) D1 = [Q; K] K^T, while K~ = diag(exp(G_L - G)) K is formed
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
+  const bool loaded = mbar_wait(bar, 0, WAIT_LIMIT);
+  if (__syncthreads_and(loaded ? 1 : 0)) {
     tc_fence_after();
     if (tid == 0) {
-      const uint32_t id = idesc_bf16(128, 64, false, false);
+      // K K^T: 64 x 64 x 128, rows of the result on lanes 16 w + (0..15)
+      const uint32_t id = idesc_bf16(64, 64, false, false);
+      const uint32_t kb = smem_u32(sm + S1_K);
       for (int ks = 0; ks < DK / 16; ++ks) {
-        const uint64_t ad = sdesc_sw128(s_base + qk_off + kstep_offset(true, ks, 16384), 16, 1024);
-        const uint64_t bd = sdesc_sw128(s_base + qk_off + 8192 + kstep_offset(true, ks, 16384), 16, 1024);
-        mma_bf16(tbase + TM_D1, ad, bd, id, ks > 0);
+        const uint64_t d = sdesc_sw128(kb + kstep_offset(true, ks, 8192), 16, 1024);
+        mma_bf16(tbase, d, d, id, ks > 0);
       }
-      mma_commit(&bars->mma);
+      mma_commit(bar);
     }
-    scale_rows(sm, qk_off + 8192, OFF_KT, 8192, Dec);
-    scale_rows(sm, qk_off + 24576, OFF_KT + 8192, 8192, Dec);
-    if (!wait_all(&bars->mma, ph_mma)) { ok = false; break; }
-    ph_mma ^= 1u;
-    tc_fence_after();
-    // Q is not read raw again: scale it in place to diag(gamma) Q for the output product
-    scale_rows(sm, qk_off, qk_off, 8192, Gam);
-    scale_rows(sm, qk_off + 16384, qk_off + 16384, 8192, Gam);
-
-    // ---- (5) P (lanes 0-63) and the lower triangle of A (lanes 64-127) from D1
-    {
+    const bool done = mbar_wait(bar, 1, WAIT_LIMIT);
+    if (__syncthreads_and(done ? 1 : 0)) {
+      tc_fence_after();
       float v[64];
-      tm_ld64(lane_base + TM_D1, v);
-      if (tid < CT) {
-        const int r = tid;
-        const float gr = Gs[r];
-#pragma unroll
-        for (int jb = 0; jb < 4; ++jb) {
-          if (jb * 16 <= r) {
-#pragma unroll
-            for (int j = jb * 16; j < jb * 16 + 16; ++j) v[j] = j <= r ? __expf(gr - Gs[j]) * v[j] : 0.f;
-          } else {
-#pragma unroll
-            for (int j = jb * 16; j < jb * 16 + 16; ++j) v[j] = 0.f;
-          }
-        }
-        st_row64(sm, OFF_P, r, v);
-      } else {
-        const int r = tid - CT;
+      tm_ld64(tbase + ((uint32_t)(warp * 32) << 16), v);
+      if (lane < 16) {
+        const int r = warp * 16 + lane;
         const float gr = Gs[r], br = Bet[r];
 #pragma unroll
         for (int jb = 0; jb < 4; ++jb) {
@@ -421,172 +302,394 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__
           }
         }
       }
-    }
-    tc_fence_before();
-    __syncthreads();
-
-    // ---- (6) T = (I + A)^-1, then T diag(beta) and T diag(beta gamma) as bf16 [r][j] tiles
-    invert_unit_lower(AF, TF);
-    for (int idx = tid; idx < CT * 8; idx += NT) {
-      const int r = idx >> 3, ch = idx & 7;
-      const float4 t0 = *reinterpret_cast<const float4*>(TF + r * FS + ch * 8);
-      const float4 t1 = *reinterpret_cast<const float4*>(TF + r * FS + ch * 8 + 4);
-      const float4 b0 = *reinterpret_cast<const float4*>(Bet + ch * 8);
-      const float4 b1 = *reinterpret_cast<const float4*>(Bet + ch * 8 + 4);
-      const float4 g0 = *reinterpret_cast<const float4*>(BG + ch * 8);
-      const float4 g1 = *reinterpret_cast<const float4*>(BG + ch * 8 + 4);
-      const float t[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
-      const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-      const float bg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-      uint32_t wa[4], wb[4];
+      tc_fence_before();
+      __syncthreads();
+      invert_unit_lower(AF, TF, tid);
+      uint8_t* dst = static_cast<uint8_t*>(p.workspace) + ((size_t)slot * p.Nv + h) * TILE_T_BYTES;
+      for (int idx = tid; idx < CT * 8; idx += 128) {
+        const int r = idx >> 3, ch = idx & 7;
+        const float4 t0 = *reinterpret_cast<const float4*>(TF + r * FS + ch * 8);
+        const float4 t1 = *reinterpret_cast<const float4*>(TF + r * FS + ch * 8 + 4);
+        const float t[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+        uint32_t wa[4], wb[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        __nv_bfloat162 ha = __floats2bfloat162_rn(t[2 * i] * bb[2 * i], t[2 * i + 1] * bb[2 * i + 1]);
-        __nv_bfloat162 hb = __floats2bfloat162_rn(t[2 * i] * bg[2 * i], t[2 * i + 1] * bg[2 * i + 1]);
-        wa[i] = *reinterpret_cast<uint32_t*>(&ha);
-        wb[i] = *reinterpret_cast<uint32_t*>(&hb);
+        for (int i = 0; i < 4; ++i) {
+          const int j = ch * 8 + 2 * i;
+          __nv_bfloat162 ha = __floats2bfloat162_rn(t[2 * i] * Bet[j], t[2 * i + 1] * Bet[j + 1]);
+          __nv_bfloat162 hb = __floats2bfloat162_rn(t[2 * i] * BG[j], t[2 * i + 1] * BG[j + 1]);
+          wa[i] = *reinterpret_cast<uint32_t*>(&ha);
+          wb[i] = *reinterpret_cast<uint32_t*>(&hb);
+        }
+        const uint32_t sw = r * 128u + ((((uint32_t)ch ^ (uint32_t)(r & 7)) & 7u) << 4);
+        *reinterpret_cast<uint4*>(dst + sw) = make_uint4(wa[0], wa[1], wa[2], wa[3]);
+        *reinterpret_cast<uint4*>(dst + 8192 + sw) = make_uint4(wb[0], wb[1], wb[2], wb[3]);
       }
-      const uint32_t sw = r * 128u + ((((uint32_t)ch ^ (uint32_t)(r & 7)) & 7u) << 4);
-      *reinterpret_cast<uint4*>(sm + OFF_TB + sw) = make_uint4(wa[0], wa[1], wa[2], wa[3]);
-      *reinterpret_cast<uint4*>(sm + OFF_TBG + sw) = make_uint4(wb[0], wb[1], wb[2], wb[3]);
+    } else if (tid == 0) {
+      raise_error(p.err, kDevErrTimeout);
     }
+  } else if (tid == 0) {
+    raise_error(p.err, kDevErrTimeout);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tbase, 64);
+}
 
-    // ---- (7) U~^T = V^T (T diag beta)^T, W^T = K^T (T diag(beta gamma))^T
-    if (!wait_all(&bars->v, ph_v)) { ok = false; break; }
-    ph_v ^= 1u;
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (tid == 0) {
-      const uint32_t id = idesc_bf16(128, 64, true, false);
-      for (int ks = 0; ks < CT / 16; ++ks) {
-        const uint64_t ad = sdesc_sw128(s_base + OFF_V + ks * 2048, 8192, 1024);
-        const uint64_t bd = sdesc_sw128(s_base + OFF_TB + ks * 32, 16, 1024);
-        mma_bf16(tbase + TM_UT, ad, bd, id, ks > 0);
-      }
-      for (int ks = 0; ks < CT / 16; ++ks) {
-        const uint64_t ad = sdesc_sw128(s_base + qk_off + 8192 + ks * 2048, 16384, 1024);
-        const uint64_t bd = sdesc_sw128(s_base + OFF_TBG + ks * 32, 16, 1024);
-        mma_bf16(tbase + TM_WT, ad, bd, id, ks > 0);
-      }
-      mma_commit(&bars->mma);
+// ---------------------------------------------------------------------------
+// kernel 2: the scan over chunks, three warpgroups
+// ---------------------------------------------------------------------------
+constexpr int NT2 = 384;
+constexpr uint32_t K2_QK = 0;          // 3 stages x [Q box0 | K box0 | Q box1 | K box1] (32 KB)
+constexpr uint32_t K2_V = 98304;       // V box0 | V box1 (16 KB)
+constexpr uint32_t K2_TB = 114688;     // T diag(beta) | T diag(beta gamma) (16 KB)
+constexpr uint32_t K2_P = 131072;      // 2 x P [r][j] (8 KB)
+constexpr uint32_t K2_WMN = 147456;    // W as [dk rows][r] (16 KB)
+constexpr uint32_t K2_UK = 163840;     // U^T as [dv rows][j] (16 KB)
+constexpr uint32_t K2_SMN = 180224;    // S as [dk rows][dv], two 64-column blocks (32 KB)
+constexpr uint32_t K2_VEC = 212992;    // 3 stages x (G, gamma, dec) (768 B each)
+constexpr uint32_t K2_BAR = K2_VEC + 3 * 768;
+constexpr uint32_t K2_SMEM = K2_BAR + 256 + 1024;
+static_assert(K2_SMEM <= 232448, "shared memory budget");
+
+// tensor memory columns
+constexpr uint32_t TM_D1 = 0, TM_WT = 64, TM_UT = 128, TM_OT = 256, TM_S = 384;
+
+struct ScanBars {
+  uint64_t qk[3];   // q/k tiles of a stage landed
+  uint64_t vt;      // v and T tiles landed
+  uint64_t p;       // PREP products done
+  uint64_t ready[2];// PREP of a chunk done
+  uint64_t fg;      // U^T - S^T W^T and S^T Q~^T done
+  uint64_t gh[2];   // U^T P^T and the state update done
+  uint64_t st[2];   // U^T of a chunk read out of tensor memory
+  uint64_t of[2];   // output of a chunk stored
+  uint32_t tslot;
+  int abort;
+};
+
+// Bounded wait that also gives up when another warpgroup aborted.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 1023u) == 1023u && *abort) return false;
+  }
+  *abort = 1;
+  return false;
+}
+
+template <typename Tout>
+__global__ void __launch_bounds__(NT2, 1)
+chunk_scan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                  const __grid_constant__ CUtensorMap tmv, ChunkArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  ScanBars* B = reinterpret_cast<ScanBars*>(sm + K2_BAR);
+  volatile int* abort = &B->abort;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int wg = warp >> 2;                   // 0 PREP, 1 STATE, 2 OUT
+  const int wt = tid & 127;                   // thread index in the warpgroup = its tensor-memory lane
+  const int h = blockIdx.x, s = blockIdx.y;
+  const int hk = h / (p.Nv / p.Nk);
+  int bos, eos;
+  if (!seq_bounds(p.cu, p.num_seqs, p.total, s, bos, eos)) {
+    if (tid == 0 && h == 0) raise_error(p.err, kDevErrSeqlens);
+    return;
+  }
+  const int n = (eos - bos + CT - 1) / CT;
+  const int slot0 = slot_base(p, s);
+
+  if (tid == 0) {
+    for (int i = 0; i < 3; ++i) mbar_init(&B->qk[i], 1);
+    mbar_init(&B->vt, 1);
+    mbar_init(&B->p, 1);
+    mbar_init(&B->fg, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&B->ready[i], 1);
+      mbar_init(&B->gh[i], 1);
+      mbar_init(&B->st[i], 1);
+      mbar_init(&B->of[i], 1);
     }
-    if (!wait_all(&bars->mma, ph_mma)) { ok = false; break; }
-    ph_mma ^= 1u;
-    tc_fence_after();
-    if (tid == 0 && c + 1 < nchunks) issue_v(c + 1);
+    B->abort = 0;
+    fence_barrier_init();
+    prefetch_tmap(&tmq);
+    prefetch_tmap(&tmk);
+    prefetch_tmap(&tmv);
+  }
+  if (warp == 0) tmem_alloc(&B->tslot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = B->tslot;
+  const uint32_t lane_base = tbase + ((uint32_t)((warp & 3) * 32) << 16);
+  const uint32_t sb = smem_u32(sm);
 
-    // ---- (8) W^T (lane dk, columns r) -> bf16 [dk rows][r] MN-major B
-    {
-      float v[64];
-      tm_ld64(lane_base + TM_WT, v);
-      st_row64(sm, OFF_WMN, tid, v);
+  auto issue_qk = [&](int c) {
+    const int t = bos + c * CT;
+    const uint32_t base = K2_QK + (c % 3) * 32768;
+    uint64_t* bar = &B->qk[c % 3];
+    mbar_arrive_expect_tx(bar, 4 * 8192);
+    tma_load_2d(sm + base, &tmq, bar, hk * DK, t);
+    tma_load_2d(sm + base + 8192, &tmk, bar, hk * DK, t);
+    tma_load_2d(sm + base + 16384, &tmq, bar, hk * DK + 64, t);
+    tma_load_2d(sm + base + 24576, &tmk, bar, hk * DK + 64, t);
+  };
+  auto issue_vt = [&](int c) {
+    const int t = bos + c * CT;
+    mbar_arrive_expect_tx(&B->vt, 2 * 8192 + TILE_T_BYTES);
+    tma_load_2d(sm + K2_V, &tmv, &B->vt, h * DV, t);
+    tma_load_2d(sm + K2_V + 8192, &tmv, &B->vt, h * DV + 64, t);
+    const uint8_t* src = static_cast<const uint8_t*>(p.workspace) + ((size_t)(slot0 + c) * p.Nv + h) * TILE_T_BYTES;
+    bulk_load(sm + K2_TB, src, TILE_T_BYTES, &B->vt);
+  };
+
+  if (wg == 0) {
+    // ============================== PREP ==============================
+    int issued_qk = 0, issued_vt = 0;     // chunks whose loads were issued (thread 0)
+    if (wt == 0 && n > 0) {
+      issue_qk(0);
+      if (n > 1) issue_qk(1);
+      issue_vt(0);
+      issued_qk = n > 1 ? 2 : 1;
+      issued_vt = 1;
     }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-
-    // ---- (9) U^T = U~^T - S^T W^T ;  O = (diag(gamma) Q) S
-    if (tid == 0) {
-      const uint32_t idf = idesc_bf16(128, 64, true, true, true);
-      for (int ks = 0; ks < DK / 16; ++ks) {
-        const uint64_t ad = sdesc_sw128(s_base + OFF_SMN + ks * 2048, 16384, 1024);
-        const uint64_t bd = sdesc_sw128(s_base + OFF_WMN + ks * 2048, 16384, 1024);
-        mma_bf16(tbase + TM_UT, ad, bd, idf, 1u);
+    float g_next = 0.f;
+    if (wt < CT && n > 0 && wt < eos - bos) g_next = p.g[(size_t)(bos + wt) * p.Nv + h];
+    int c = 0;
+    bool fail = false;
+    for (; c < n; ++c) {
+      const int st3 = c % 3, b = c & 1;
+      const uint32_t qk = K2_QK + st3 * 32768;
+      float* Gs = reinterpret_cast<float*>(sm + K2_VEC + st3 * 768);
+      float* Gam = Gs + CT;
+      float* Dec = Gam + CT;
+      const int c0 = bos + c * CT;
+      // gates of this chunk (prefetched one chunk ahead)
+      if (wt < CT) {
+        Gs[wt] = g_next;
+        g_next = 0.f;
+        if (c + 1 < n && c0 + CT + wt < eos) g_next = p.g[(size_t)(c0 + CT + wt) * p.Nv + h];
       }
-      const uint32_t ido = idesc_bf16(64, 128, false, true);
-      for (int ks = 0; ks < DK / 16; ++ks) {
-        const uint64_t ad = sdesc_sw128(s_base + qk_off + kstep_offset(true, ks, 16384), 16, 1024);
-        const uint64_t bd = sdesc_sw128(s_base + OFF_SMN + ks * 2048, 16384, 1024);
-        mma_bf16(tbase + TM_O, ad, bd, ido, ks > 0);
+      named_sync(1, 128);
+      if (warp == 0) chunk_cumsum(Gs, Gam, Dec, lane);
+      bool ok = wait_bar(&B->qk[st3], (c / 3) & 1, abort) && wait_bar(&B->vt, c & 1, abort);
+      if (ok && c >= 2) ok = wait_bar(&B->st[b], ((c >> 1) - 1) & 1, abort);   // U~^T buffer free
+      if (named_sync_or(1, 128, !ok)) { fail = true; break; }
+      tc_fence_after();
+      if (wt == 0) {
+        // D1 = [Q; K] K^T ; U~^T = V^T (T diag beta)^T ; W^T = K^T (T diag(beta gamma))^T
+        const uint32_t id1 = idesc_bf16(128, 64, false, false);
+        for (int ks = 0; ks < DK / 16; ++ks) {
+          const uint64_t ad = sdesc_sw128(sb + qk + kstep_offset(true, ks, 16384), 16, 1024);
+          const uint64_t bd = sdesc_sw128(sb + qk + 8192 + kstep_offset(true, ks, 16384), 16, 1024);
+          mma_bf16(tbase + TM_D1, ad, bd, id1, ks > 0);
+        }
+        const uint32_t id2 = idesc_bf16(128, 64, true, false);
+        for (int ks = 0; ks < CT / 16; ++ks) {
+          const uint64_t ad = sdesc_sw128(sb + K2_V + ks * 2048, 8192, 1024);
+          const uint64_t bd = sdesc_sw128(sb + K2_TB + ks * 32, 16, 1024);
+          mma_bf16(tbase + TM_UT + b * 64, ad, bd, id2, ks > 0);
+        }
+        for (int ks = 0; ks < CT / 16; ++ks) {
+          const uint64_t ad = sdesc_sw128(sb + qk + 8192 + ks * 2048, 16384, 1024);
+          const uint64_t bd = sdesc_sw128(sb + K2_TB + 8192 + ks * 32, 16, 1024);
+          mma_bf16(tbase + TM_WT, ad, bd, id2, ks > 0);
+        }
+        mma_commit(&B->p);
       }
-      mma_commit(&bars->mma);
-    }
-    if (!wait_all(&bars->mma, ph_mma)) { ok = false; break; }
-    ph_mma ^= 1u;
-    tc_fence_after();
-
-    // ---- (10) U^T (lane dv, columns j) -> bf16 [dv rows][j] K-major
-    {
-      float v[64];
-      tm_ld64(lane_base + TM_UT, v);
-      st_row64(sm, OFF_UK, tid, v);
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-
-    // ---- (11) O += P U ;  S += K~^T U
-    if (tid == 0) {
-      const uint32_t idp = idesc_bf16(64, 128, false, false);
-      for (int ks = 0; ks < CT / 16; ++ks) {
-        const uint64_t ad = sdesc_sw128(s_base + OFF_P + ks * 32, 16, 1024);
-        const uint64_t bd = sdesc_sw128(s_base + OFF_UK + ks * 32, 16, 1024);
-        mma_bf16(tbase + TM_O, ad, bd, idp, 1u);
-      }
-      const uint32_t ids = idesc_bf16(128, 128, true, false);
-      for (int ks = 0; ks < CT / 16; ++ks) {
-        const uint64_t ad = sdesc_sw128(s_base + OFF_KT + ks * 2048, 8192, 1024);
-        const uint64_t bd = sdesc_sw128(s_base + OFF_UK + ks * 32, 16, 1024);
-        mma_bf16(tbase + TM_S, ad, bd, ids, 1u);
-      }
-      mma_commit(&bars->mma);
-    }
-    if (!wait_all(&bars->mma, ph_mma)) { ok = false; break; }
-    ph_mma ^= 1u;
-    tc_fence_after();
-
-    // ---- (12) O rows -> o[c0 + r][h][:].  The 64-row accumulator holds row
-    // r = 16 * warp + lane in lanes 0-15 of each warp's lane quarter.
-    {
-      const int r = warp * 16 + lane;
-      const bool valid = lane < 16 && r < len;
-      Tout* dst = o + ((size_t)(c0 + r) * p.Nv + h) * DV;
+      ok = wait_bar(&B->p, c & 1, abort);
+      if (ok && c >= 2) ok = wait_bar(&B->gh[b], ((c >> 1) - 1) & 1, abort);   // P[b] free
+      if (named_sync_or(1, 128, !ok)) { fail = true; break; }
+      tc_fence_after();
+      if (wt == 0 && c + 1 < n) { issue_vt(c + 1); issued_vt = c + 2; }
+      // diag(gamma) Q and diag(exp(G_L - G)) K in place (raw tiles are no longer read)
+      scale_box(sm, qk, Gam, wt, 128);
+      scale_box(sm, qk + 16384, Gam, wt, 128);
+      scale_box(sm, qk + 8192, Dec, wt, 128);
+      scale_box(sm, qk + 24576, Dec, wt, 128);
+      {
+        float v[64];
+        tm_ld64(lane_base + TM_D1, v);          // warps 0, 1: rows r = wt of Q K^T
+        if (wt < CT) {
+          const int r = wt;
+          const float gr = Gs[r];
 #pragma unroll
-      for (int c32 = 0; c32 < DV; c32 += 32) {
-        float v[32];
-        tmem_ld32(lane_base + TM_O + c32, v);
-        tmem_ld_wait();
-        if (valid) {
+          for (int jb = 0; jb < 4; ++jb) {
+            if (jb * 16 <= r) {
 #pragma unroll
-          for (int i = 0; i < 32; i += 8) {
-            float w8[8];
+              for (int j = jb * 16; j < jb * 16 + 16; ++j) v[j] = j <= r ? __expf(gr - Gs[j]) * v[j] : 0.f;
+            } else {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) w8[e] = p.scale * v[i + e];
-            store8(dst + c32 + i, w8);
+              for (int j = jb * 16; j < jb * 16 + 16; ++j) v[j] = 0.f;
+            }
+          }
+          st_row64(sm, K2_P + b * 8192, r, v);
+        }
+      }
+      ok = c < 1 || wait_bar(&B->fg, (c - 1) & 1, abort);   // W buffer free
+      if (named_sync_or(1, 128, !ok)) { fail = true; break; }
+      tc_fence_after();
+      {
+        float v[64];
+        tm_ld64(lane_base + TM_WT, v);          // lane dk holds W[0..63][dk]
+        st_row64(sm, K2_WMN, wt, v);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_sync(1, 128);
+      if (wt == 0) {
+        mbar_arrive(&B->ready[b]);
+        // q/k tiles of chunk c + 2 go to the stage of chunk c - 1 once its last product ran
+        if (c + 2 < n) {
+          if (c < 1 || wait_bar(&B->gh[(c - 1) & 1], ((c - 1) >> 1) & 1, abort)) {
+            issue_qk(c + 2);
+            issued_qk = c + 3;
           }
         }
       }
     }
-    tc_fence_before();
-    __syncthreads();
+    if (fail && wt == 0) {
+      // let the copies and products this warpgroup issued land before the exit
+      for (int k = max(c, 0); k < issued_qk; ++k) mbar_wait(&B->qk[k % 3], (k / 3) & 1, WAIT_LIMIT);
+      for (int k = max(c, 0); k < issued_vt; ++k) mbar_wait(&B->vt, k & 1, WAIT_LIMIT);
+      mbar_wait(&B->p, c & 1, WAIT_LIMIT);
+    }
+  } else if (wg == 1) {
+    // ============================== STATE ==============================
+    {
+      // initial state -> tensor memory (lane = dk, 128 columns = dv)
+      const int dk = wt;
+      const float* src = p.S0 ? p.S0 + (((size_t)s * p.Nv + h) * DK + dk) * DV : nullptr;
+#pragma unroll
+      for (int c0 = 0; c0 < DV; c0 += 32) {
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          float4 t4 = src ? *reinterpret_cast<const float4*>(src + c0 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+          v[i] = t4.x; v[i + 1] = t4.y; v[i + 2] = t4.z; v[i + 3] = t4.w;
+        }
+        tmem_st32(lane_base + TM_S + c0, v);
+      }
+      tmem_st_wait();
+    }
+    bool fail = false;
+    int c = 0;
+    for (; c < n; ++c) {
+      const int st3 = c % 3, b = c & 1;
+      const uint32_t qk = K2_QK + st3 * 32768;
+      const float* Gam = reinterpret_cast<const float*>(sm + K2_VEC + st3 * 768) + CT;
+      bool ok = wait_bar(&B->ready[b], (c >> 1) & 1, abort);
+      if (named_sync_or(2, 128, !ok)) { fail = true; break; }
+      tc_fence_after();
+      const float gamma_L = Gam[CT - 1];
+      // bf16 S -> shared memory (operand), gamma_L S -> tensor memory (accumulator)
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float v[64];
+        tm_ld64(lane_base + TM_S + half * 64, v);
+        st_row64(sm, K2_SMN + half * 16384, wt, v);
+        float a[32], bb[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) { a[i] = v[i] * gamma_L; bb[i] = v[32 + i] * gamma_L; }
+        tmem_st32(lane_base + TM_S + half * 64, a);
+        tmem_st32(lane_base + TM_S + half * 64 + 32, bb);
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      ok = c < 2 || wait_bar(&B->of[b], ((c >> 1) - 1) & 1, abort);    // O^T buffer free
+      if (named_sync_or(2, 128, !ok)) { fail = true; break; }
+      tc_fence_after();
+      if (wt == 0) {
+        // U^T = U~^T - S^T W^T ;  O^T = S^T (diag(gamma) Q)^T
+        const uint32_t idf = idesc_bf16(128, 64, true, true, true);
+        for (int ks = 0; ks < DK / 16; ++ks) {
+          const uint64_t ad = sdesc_sw128(sb + K2_SMN + ks * 2048, 16384, 1024);
+          const uint64_t bd = sdesc_sw128(sb + K2_WMN + ks * 2048, 16384, 1024);
+          mma_bf16(tbase + TM_UT + b * 64, ad, bd, idf, 1u);
+        }
+        const uint32_t idq = idesc_bf16(128, 64, true, false);
+        for (int ks = 0; ks < DK / 16; ++ks) {
+          const uint64_t ad = sdesc_sw128(sb + K2_SMN + ks * 2048, 16384, 1024);
+          const uint64_t bd = sdesc_sw128(sb + qk + kstep_offset(true, ks, 16384), 16, 1024);
+          mma_bf16(tbase + TM_OT + b * 64, ad, bd, idq, ks > 0);
+        }
+        mma_commit(&B->fg);
+      }
+      ok = wait_bar(&B->fg, c & 1, abort);
+      if (named_sync_or(2, 128, !ok)) { fail = true; break; }
+      tc_fence_after();
+      {
+        float v[64];
+        tm_ld64(lane_base + TM_UT + b * 64, v);   // lane dv holds U[0..63][dv]
+        st_row64(sm, K2_UK, wt, v);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_sync(2, 128);
+      tc_fence_after();
+      if (wt == 0) {
+        mbar_arrive(&B->st[b]);
+        // O^T += U^T P^T ;  S += (diag(exp(G_L - G)) K)^T U
+        const uint32_t idp = idesc_bf16(128, 64, false, false);
+        for (int ks = 0; ks < CT / 16; ++ks) {
+          const uint64_t ad = sdesc_sw128(sb + K2_UK + ks * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(sb + K2_P + b * 8192 + ks * 32, 16, 1024);
+          mma_bf16(tbase + TM_OT + b * 64, ad, bd, idp, 1u);
+        }
+        const uint32_t ids = idesc_bf16(128, 128, true, false);
+        for (int ks = 0; ks < CT / 16; ++ks) {
+          const uint64_t ad = sdesc_sw128(sb + qk + 8192 + ks * 2048, 16384, 1024);
+          const uint64_t bd = sdesc_sw128(sb + K2_UK + ks * 32, 16, 1024);
+          mma_bf16(tbase + TM_S, ad, bd, ids, 1u);
+        }
+        mma_commit(&B->gh[b]);
+      }
+      ok = wait_bar(&B->gh[b], (c >> 1) & 1, abort);
+      if (named_sync_or(2, 128, !ok)) { fail = true; break; }
+      tc_fence_after();
+    }
+    if (fail) {
+      if (wt == 0) {
+        mbar_wait(&B->fg, c & 1, WAIT_LIMIT);
+        mbar_wait(&B->gh[c & 1], (c >> 1) & 1, WAIT_LIMIT);
+      }
+    } else if (p.ST) {
+      const int dk = wt;
+      float* dst = p.ST + (((size_t)s * p.Nv + h) * DK + dk) * DV;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float v[64];
+        tm_ld64(lane_base + TM_S + half * 64, v);
+#pragma unroll
+        for (int i = 0; i < 64; i += 4)
+          *reinterpret_cast<float4*>(dst + half * 64 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+      }
+    }
+  } else {
+    // ============================== OUT ==============================
+    Tout* o = static_cast<Tout*>(p.o);
+    const int dv = wt;
+    for (int c = 0; c < n; ++c) {
+      const int b = c & 1;
+      const int c0 = bos + c * CT, len = min(CT, eos - c0);
+      const bool ok = wait_bar(&B->gh[b], (c >> 1) & 1, abort);
+      if (named_sync_or(3, 128, !ok)) break;
+      tc_fence_after();
+      float v[64];
+      tm_ld64(lane_base + TM_OT + b * 64, v);   // lane dv holds O[0..63][dv]
+      Tout* dst = o + ((size_t)c0 * p.Nv + h) * DV + dv;
+#pragma unroll
+      for (int r = 0; r < CT; ++r)
+        if (r < len) dst[(size_t)r * p.Nv * DV] = from_f32<Tout>(p.scale * v[r]);
+      tc_fence_before();
+      named_sync(3, 128);
+      if (wt == 0) mbar_arrive(&B->of[b]);
+    }
   }
 
-  if (!ok) {
-    // a bounded wait ran out: report, let outstanding copies and products land, release TMEM
-    if (tid == 0) {
-      raise_error(p.err, kDevErrTimeout);
-      mbar_wait(&bars->mma, ph_mma, WAIT_LIMIT);
-      mbar_wait(&bars->qk[0], ph_qk0, WAIT_LIMIT);
-      mbar_wait(&bars->qk[1], ph_qk1, WAIT_LIMIT);
-      mbar_wait(&bars->v, ph_v, WAIT_LIMIT);
-    }
-  } else if (p.ST) {
-    tc_fence_after();
-    const int dk = tid;
-    float* dst = p.ST + (((size_t)s * p.Nv + h) * DK + dk) * DV;
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      float v[64];
-      tm_ld64(lane_base + TM_S + half * 64, v);
-#pragma unroll
-      for (int i = 0; i < 64; i += 4)
-        *reinterpret_cast<float4*>(dst + half * 64 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-    }
-  }
+  if (*abort && tid == 0) raise_error(p.err, kDevErrTimeout);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tbase, 512);
@@ -624,13 +727,13 @@ bool make_map(CUtensorMap* map, const void* base, int rows, int cols) {
 }
 
 template <typename Tout>
-cudaError_t launch_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const ChunkArgs& p,
-                     cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(chunk_tc_kernel<Tout>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)SMEM_BYTES);
+cudaError_t launch_scan(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const ChunkArgs& p,
+                        cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(chunk_scan_kernel<Tout>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)K2_SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid(p.Nv, p.num_seqs);
-  chunk_tc_kernel<Tout><<<grid, NT, SMEM_BYTES, s>>>(mq, mk, mv, p);
+  chunk_scan_kernel<Tout><<<grid, NT2, K2_SMEM, s>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 
@@ -638,6 +741,10 @@ cudaError_t launch_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
 
 bool chunk_tc_supported(const ChunkArgs& p) {
   return p.Dk == DK && p.Dv == DV && p.in_bf16 && get_encoder() != nullptr;
+}
+
+size_t chunk_tc_workspace_bytes(int num_seqs, int total, int Nv) {
+  return ((size_t)(total / CT) + (size_t)num_seqs) * (size_t)Nv * TILE_T_BYTES;
 }
 
 cudaError_t launch_chunk_tc(const ChunkArgs& p, cudaStream_t s) {
@@ -654,7 +761,15 @@ cudaError_t launch_chunk_tc(const ChunkArgs& p, cudaStream_t s) {
   if (!make_map(&mq, p.q, p.total, p.Nk * DK) || !make_map(&mk, p.k, p.total, p.Nk * DK) ||
       !make_map(&mv, p.v, p.total, p.Nv * DV))
     return cudaErrorInvalidValue;
-  return p.out_bf16 ? launch_t<bf16>(mq, mk, mv, p, s) : launch_t<float>(mq, mk, mv, p, s);
+  cudaError_t e = cudaFuncSetAttribute(chunk_solve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)S1_SMEM);
+  if (e != cudaSuccess) return e;
+  const int slots = p.total / CT + p.num_seqs;
+  dim3 g1(slots, p.Nv);
+  chunk_solve_kernel<<<g1, 128, S1_SMEM, s>>>(mk, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return p.out_bf16 ? launch_scan<bf16>(mq, mk, mv, p, s) : launch_scan<float>(mq, mk, mv, p, s);
 }
 
 }  // namespace gdn

@@ -83,6 +83,7 @@ struct ChunkArgs {
 cudaError_t launch_chunk_simt(const ChunkArgs& p, cudaStream_t s);
 // tcgen05 tensor-core implementation (bf16 q/k/v, Dk = Dv = 128).
 bool chunk_tc_supported(const ChunkArgs& p);
+size_t chunk_tc_workspace_bytes(int num_seqs, int total, int Nv);
 cudaError_t launch_chunk_tc(const ChunkArgs& p, cudaStream_t s);
 
 }  // namespace gdn
