@@ -276,7 +276,7 @@ def run_ours(args):
     t_norm = [e[2].elapsed_time(e[3]) for e in evs]
     t_step = [e[0].elapsed_time(e[3]) for e in evs]
     ms_step = max_over_ranks(statistics.mean(t_step))
-    launches_prefill = 4 * args.steps          # conv, conv-state, chunk, rmsnorm
+    launches_prefill = 5 * args.steps          # conv, conv-state, chunk solve, chunk scan, rmsnorm
 
     # ---------------- decode workload (fused step, state in place; 512 MiB state > L2)
     del flush
@@ -362,7 +362,7 @@ def run_ours(args):
         'config': {'workload': 'prefill_t4096', 'B': 1, 'T': T, 'Nk': sh.Nk, 'Nv': sh.Nv, 'Dk': sh.Dk,
                    'Dv': sh.Dv, 'C': sh.C, 'chunk': CHUNK, 'state': 'fp32', 'gates': 'fp32',
                    'l2': 'flushed between timed steps (512 MiB write)', 'parallelism': 'replicas'},
-        'roofline': {'kernel': 'gdn_chunk_prefill', 'bound': 'tensor', 'achieved': tflops,
+        'roofline': {'kernel': 'gdn_chunk_prefill (T-solve + scan launches)', 'bound': 'tensor', 'achieved': tflops,
                      'peak': tc_peak, 'unit': 'TFLOP/s', 'frac': tflops / tc_peak,
                      'traffic': traffic, 'peak_source': peak_src + ' bf16 dense (burst)',
                      'algorithmic_flops_per_launch': flops, 'us_per_launch': us_chunk,
@@ -380,7 +380,7 @@ def run_ours(args):
                                 'bytes_per_launch': dbytes}},
         'e2e': {'value': ws * T / (ms_e2e * 1e-3), 'unit': 'tokens/s', 'h2d_bytes_per_step': h2d,
                 'd2h_bytes_per_step': d2h, 'ms_per_step': ms_e2e},
-        'gpu_launches': launches_prefill + dsteps + 4 * args.steps,
+        'gpu_launches': launches_prefill + dsteps + 5 * args.steps,
         'clocks': clocks,
     }
     if ws == 1 and not args.no_cpu_baseline:

@@ -35,6 +35,7 @@
 #include "common.cuh"
 #include "launch.h"
 #include "tc_util.cuh"
+#include "tmap.cuh"
 
 namespace gdn {
 namespace {
@@ -358,6 +359,8 @@ struct ScanBars {
   uint64_t qk[3];   // q/k tiles of a stage landed
   uint64_t vt;      // v and T tiles landed
   uint64_t p;       // PREP products done
+  uint64_t pv;      // PREP gates of a chunk written (G, gamma, dec)
+  uint64_t sc;      // OUT scaled Q and K of a chunk in place and wrote W
   uint64_t ready[2];// PREP of a chunk done
   uint64_t fg;      // U^T - S^T W^T and S^T Q~^T done
   uint64_t gh[2];   // U^T P^T and the state update done
@@ -404,6 +407,8 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
     for (int i = 0; i < 3; ++i) mbar_init(&B->qk[i], 1);
     mbar_init(&B->vt, 1);
     mbar_init(&B->p, 1);
+    mbar_init(&B->pv, 1);
+    mbar_init(&B->sc, 1);
     mbar_init(&B->fg, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&B->ready[i], 1);
@@ -478,24 +483,21 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
       if (named_sync_or(1, 128, !ok)) { fail = true; break; }
       tc_fence_after();
       if (wt == 0) {
+        mbar_arrive(&B->pv);                  // gates of chunk c are in shared memory
         // D1 = [Q; K] K^T ; U~^T = V^T (T diag beta)^T ; W^T = K^T (T diag(beta gamma))^T
         const uint32_t id1 = idesc_bf16(128, 64, false, false);
+        const uint64_t a1 = sdesc_sw128(sb + qk, 16, 1024), b1 = sdesc_sw128(sb + qk + 8192, 16, 1024);
         for (int ks = 0; ks < DK / 16; ++ks) {
-          const uint64_t ad = sdesc_sw128(sb + qk + kstep_offset(true, ks, 16384), 16, 1024);
-          const uint64_t bd = sdesc_sw128(sb + qk + 8192 + kstep_offset(true, ks, 16384), 16, 1024);
-          mma_bf16(tbase + TM_D1, ad, bd, id1, ks > 0);
+          const uint32_t o = kstep_offset(true, ks, 16384) >> 4;
+          mma_bf16(tbase + TM_D1, a1 + o, b1 + o, id1, ks > 0);
         }
         const uint32_t id2 = idesc_bf16(128, 64, true, false);
-        for (int ks = 0; ks < CT / 16; ++ks) {
-          const uint64_t ad = sdesc_sw128(sb + K2_V + ks * 2048, 8192, 1024);
-          const uint64_t bd = sdesc_sw128(sb + K2_TB + ks * 32, 16, 1024);
-          mma_bf16(tbase + TM_UT + b * 64, ad, bd, id2, ks > 0);
-        }
-        for (int ks = 0; ks < CT / 16; ++ks) {
-          const uint64_t ad = sdesc_sw128(sb + qk + 8192 + ks * 2048, 16384, 1024);
-          const uint64_t bd = sdesc_sw128(sb + K2_TB + 8192 + ks * 32, 16, 1024);
-          mma_bf16(tbase + TM_WT, ad, bd, id2, ks > 0);
-        }
+        const uint64_t av = sdesc_sw128(sb + K2_V, 8192, 1024), bt = sdesc_sw128(sb + K2_TB, 16, 1024);
+        const uint64_t ak = sdesc_sw128(sb + qk + 8192, 16384, 1024), bg = sdesc_sw128(sb + K2_TB + 8192, 16, 1024);
+        for (int ks = 0; ks < CT / 16; ++ks)
+          mma_bf16(tbase + TM_UT + b * 64, av + ks * (2048 >> 4), bt + ks * (32 >> 4), id2, ks > 0);
+        for (int ks = 0; ks < CT / 16; ++ks)
+          mma_bf16(tbase + TM_WT, ak + ks * (2048 >> 4), bg + ks * (32 >> 4), id2, ks > 0);
         mma_commit(&B->p);
       }
       ok = wait_bar(&B->p, c & 1, abort);
@@ -503,11 +505,6 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
       if (named_sync_or(1, 128, !ok)) { fail = true; break; }
       tc_fence_after();
       if (wt == 0 && c + 1 < n) { issue_vt(c + 1); issued_vt = c + 2; }
-      // diag(gamma) Q and diag(exp(G_L - G)) K in place (raw tiles are no longer read)
-      scale_box(sm, qk, Gam, wt, 128);
-      scale_box(sm, qk + 16384, Gam, wt, 128);
-      scale_box(sm, qk + 8192, Dec, wt, 128);
-      scale_box(sm, qk + 24576, Dec, wt, 128);
       {
         float v[64];
         tm_ld64(lane_base + TM_D1, v);          // warps 0, 1: rows r = wt of Q K^T
@@ -527,17 +524,10 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
           st_row64(sm, K2_P + b * 8192, r, v);
         }
       }
-      ok = c < 1 || wait_bar(&B->fg, (c - 1) & 1, abort);   // W buffer free
-      if (named_sync_or(1, 128, !ok)) { fail = true; break; }
-      tc_fence_after();
-      {
-        float v[64];
-        tm_ld64(lane_base + TM_WT, v);          // lane dk holds W[0..63][dk]
-        st_row64(sm, K2_WMN, wt, v);
-      }
       fence_proxy_async_smem();
       tc_fence_before();
-      named_sync(1, 128);
+      ok = wait_bar(&B->sc, c & 1, abort);      // OUT scaled Q, K and wrote W
+      if (named_sync_or(1, 128, !ok)) { fail = true; break; }
       if (wt == 0) {
         mbar_arrive(&B->ready[b]);
         // q/k tiles of chunk c + 2 go to the stage of chunk c - 1 once its last product ran
@@ -604,17 +594,14 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
       if (wt == 0) {
         // U^T = U~^T - S^T W^T ;  O^T = S^T (diag(gamma) Q)^T
         const uint32_t idf = idesc_bf16(128, 64, true, true, true);
-        for (int ks = 0; ks < DK / 16; ++ks) {
-          const uint64_t ad = sdesc_sw128(sb + K2_SMN + ks * 2048, 16384, 1024);
-          const uint64_t bd = sdesc_sw128(sb + K2_WMN + ks * 2048, 16384, 1024);
-          mma_bf16(tbase + TM_UT + b * 64, ad, bd, idf, 1u);
-        }
+        const uint64_t as = sdesc_sw128(sb + K2_SMN, 16384, 1024), bw = sdesc_sw128(sb + K2_WMN, 16384, 1024);
+        for (int ks = 0; ks < DK / 16; ++ks)
+          mma_bf16(tbase + TM_UT + b * 64, as + ks * (2048 >> 4), bw + ks * (2048 >> 4), idf, 1u);
         const uint32_t idq = idesc_bf16(128, 64, true, false);
-        for (int ks = 0; ks < DK / 16; ++ks) {
-          const uint64_t ad = sdesc_sw128(sb + K2_SMN + ks * 2048, 16384, 1024);
-          const uint64_t bd = sdesc_sw128(sb + qk + kstep_offset(true, ks, 16384), 16, 1024);
-          mma_bf16(tbase + TM_OT + b * 64, ad, bd, idq, ks > 0);
-        }
+        const uint64_t bq = sdesc_sw128(sb + qk, 16, 1024);
+        for (int ks = 0; ks < DK / 16; ++ks)
+          mma_bf16(tbase + TM_OT + b * 64, as + ks * (2048 >> 4), bq + (kstep_offset(true, ks, 16384) >> 4), idq,
+                   ks > 0);
         mma_commit(&B->fg);
       }
       ok = wait_bar(&B->fg, c & 1, abort);
@@ -633,17 +620,13 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
         mbar_arrive(&B->st[b]);
         // O^T += U^T P^T ;  S += (diag(exp(G_L - G)) K)^T U
         const uint32_t idp = idesc_bf16(128, 64, false, false);
-        for (int ks = 0; ks < CT / 16; ++ks) {
-          const uint64_t ad = sdesc_sw128(sb + K2_UK + ks * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(sb + K2_P + b * 8192 + ks * 32, 16, 1024);
-          mma_bf16(tbase + TM_OT + b * 64, ad, bd, idp, 1u);
-        }
+        const uint64_t au = sdesc_sw128(sb + K2_UK, 16, 1024), bp = sdesc_sw128(sb + K2_P + b * 8192, 16, 1024);
+        for (int ks = 0; ks < CT / 16; ++ks)
+          mma_bf16(tbase + TM_OT + b * 64, au + ks * (32 >> 4), bp + ks * (32 >> 4), idp, 1u);
         const uint32_t ids = idesc_bf16(128, 128, true, false);
-        for (int ks = 0; ks < CT / 16; ++ks) {
-          const uint64_t ad = sdesc_sw128(sb + qk + 8192 + ks * 2048, 16384, 1024);
-          const uint64_t bd = sdesc_sw128(sb + K2_UK + ks * 32, 16, 1024);
-          mma_bf16(tbase + TM_S, ad, bd, ids, 1u);
-        }
+        const uint64_t akt = sdesc_sw128(sb + qk + 8192, 16384, 1024);
+        for (int ks = 0; ks < CT / 16; ++ks)
+          mma_bf16(tbase + TM_S, akt + ks * (2048 >> 4), au + ks * (32 >> 4), ids, 1u);
         mma_commit(&B->gh[b]);
       }
       ok = wait_bar(&B->gh[b], (c >> 1) & 1, abort);
@@ -669,13 +652,16 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
     }
   } else {
     // ============================== OUT ==============================
+    // Per chunk: scale Q by gamma and K by exp(G_L - G) in place once PREP's
+    // products have read them raw, write W for STATE, then store the
+    // previous chunk's output rows.
     Tout* o = static_cast<Tout*>(p.o);
     const int dv = wt;
-    for (int c = 0; c < n; ++c) {
+    auto store_out = [&](int c) -> bool {
       const int b = c & 1;
       const int c0 = bos + c * CT, len = min(CT, eos - c0);
       const bool ok = wait_bar(&B->gh[b], (c >> 1) & 1, abort);
-      if (named_sync_or(3, 128, !ok)) break;
+      if (named_sync_or(3, 128, !ok)) return false;
       tc_fence_after();
       float v[64];
       tm_ld64(lane_base + TM_OT + b * 64, v);   // lane dv holds O[0..63][dv]
@@ -686,7 +672,34 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
       tc_fence_before();
       named_sync(3, 128);
       if (wt == 0) mbar_arrive(&B->of[b]);
+      return true;
+    };
+    bool alive = true;
+    for (int c = 0; c < n && alive; ++c) {
+      const int st3 = c % 3;
+      const uint32_t qk = K2_QK + st3 * 32768;
+      const float* Gam = reinterpret_cast<const float*>(sm + K2_VEC + st3 * 768) + CT;
+      const float* Dec = Gam + CT;
+      bool ok = wait_bar(&B->pv, c & 1, abort) && wait_bar(&B->p, c & 1, abort);
+      if (ok && c >= 1) ok = wait_bar(&B->fg, (c - 1) & 1, abort);   // W buffer free
+      if (named_sync_or(3, 128, !ok)) break;
+      tc_fence_after();
+      scale_box(sm, qk, Gam, wt, 128);
+      scale_box(sm, qk + 16384, Gam, wt, 128);
+      scale_box(sm, qk + 8192, Dec, wt, 128);
+      scale_box(sm, qk + 24576, Dec, wt, 128);
+      {
+        float v[64];
+        tm_ld64(lane_base + TM_WT, v);          // lane dk holds W[0..63][dk]
+        st_row64(sm, K2_WMN, wt, v);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_sync(3, 128);
+      if (wt == 0) mbar_arrive(&B->sc);
+      if (c >= 1) alive = store_out(c - 1);
     }
+    if (alive && n > 0) store_out(n - 1);
   }
 
   if (*abort && tid == 0) raise_error(p.err, kDevErrTimeout);
@@ -696,34 +709,10 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
 }
 
 // ---- host: tensor maps and launch
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn get_encoder() {
-  static EncodeTiledFn fn = nullptr;
-  if (fn == nullptr) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  }
-  return fn;
-}
-
 // 2-D bf16 map over a token-major [rows, cols] matrix with a 64 x 64 box, 128-byte swizzle.
 bool make_map(CUtensorMap* map, const void* base, int rows, int cols) {
-  EncodeTiledFn enc = get_encoder();
-  if (enc == nullptr) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  cuuint32_t box[2] = {64, 64};
-  cuuint32_t es[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return make_tmap_2d(map, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, cols, 64, 64,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 template <typename Tout>
@@ -740,7 +729,7 @@ cudaError_t launch_scan(const CUtensorMap& mq, const CUtensorMap& mk, const CUte
 }  // namespace
 
 bool chunk_tc_supported(const ChunkArgs& p) {
-  return p.Dk == DK && p.Dv == DV && p.in_bf16 && get_encoder() != nullptr;
+  return p.Dk == DK && p.Dv == DV && p.in_bf16 && tmap_encoder() != nullptr;
 }
 
 size_t chunk_tc_workspace_bytes(int num_seqs, int total, int Nv) {

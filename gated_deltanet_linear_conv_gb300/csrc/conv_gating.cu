@@ -13,8 +13,12 @@
 // and holds whole heads, so the per-head L2-norm is a shuffle reduction over
 // Dk/4 lanes.
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "launch.h"
+#include "tc_util.cuh"
+#include "tmap.cuh"
 
 namespace gdn {
 namespace {
@@ -203,6 +207,156 @@ conv_gating_kernel(ConvGatingArgs p) {
   }
 }
 
+// Tiled variant for bf16 inputs with C a multiple of 1024: a CTA stages a
+// [3 + 32 tokens] x [1024 channels] tile of mixed_qkv in shared memory with
+// eight TMA box loads (the rows before the first token, including negative
+// token indices, arrive as zeros), then each warp walks its 128-channel strip
+// down the tile.  The data in flight lives in the copy engine, not in
+// registers, so many warps stay resident.  Tokens in the first 3 positions of
+// a sequence are recomputed with their conv state afterwards.
+constexpr int TT = 32;                       // tokens per tile
+constexpr int TROWS = TT + 3;
+constexpr uint32_t STRIP_BYTES = TROWS * 256;  // 128 bf16 channels per row
+constexpr uint32_t TILE_BYTES = 8 * STRIP_BYTES;
+constexpr uint32_t TILE_SMEM = TILE_BYTES + 64 + 128;
+
+template <typename Tout>
+__global__ void __launch_bounds__(256, 3)
+conv_gating_tile_kernel(const __grid_constant__ CUtensorMap tmx, ConvGatingArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + TILE_BYTES);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nct = p.C / 1024;
+  const int ntiles = ((p.total + TT - 1) / TT) * nct;
+  const int kd = p.Nk * p.Dk;
+  const int lanes_per_head = p.Dk / 4;
+  const bf16* st_in = static_cast<const bf16*>(p.state_in);
+  const bf16* xg = static_cast<const bf16*>(p.x);
+  if (threadIdx.x == 0) {
+    tc::mbar_init(bar, 1);
+    tc::fence_barrier_init();
+  }
+  __syncthreads();
+  uint32_t phase = 0;
+  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, phase ^= 1u) {
+    const int tt = tile / nct, ct = tile % nct;
+    const int t0 = tt * TT, t_end = min(t0 + TT, p.total);
+    if (threadIdx.x == 0) {
+      tc::mbar_arrive_expect_tx(bar, TILE_BYTES);
+      for (int i = 0; i < 8; ++i) tc::tma_load_2d(sm + i * STRIP_BYTES, &tmx, bar, ct * 1024 + i * 128, t0 - 3);
+    }
+    const bool ok = tc::mbar_wait(bar, phase, 1u << 24);
+    if (!__syncthreads_and(ok ? 1 : 0)) {
+      if (threadIdx.x == 0) raise_error(p.err, kDevErrTimeout);
+      return;
+    }
+    const int strip = ct * 8 + warp;
+    const int c0 = strip * 128 + lane * 4;
+    const int region = c0 < kd ? 0 : (c0 < 2 * kd ? 1 : 2);
+    float wt[4][4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) load4(static_cast<const bf16*>(p.w) + (size_t)(c0 + c) * 4, wt[c]);
+    float bias[4] = {0.f, 0.f, 0.f, 0.f};
+    if (p.bias) load4(static_cast<const bf16*>(p.bias) + c0, bias);
+    Tout* dst;
+    size_t row_stride;
+    if (region < 2) {
+      dst = static_cast<Tout*>(region == 0 ? p.q : p.k) + (c0 - region * kd);
+      row_stride = (size_t)kd;
+    } else {
+      dst = static_cast<Tout*>(p.v) + (c0 - 2 * kd);
+      row_stride = (size_t)p.Nv * p.Dv;
+    }
+    const float qs = region == 0 ? p.q_scale : 1.0f;
+    const uint8_t* rows = sm + warp * STRIP_BYTES + lane * 8;
+    float xm[3][4];
+#pragma unroll
+    for (int j = 0; j < 3; ++j) load4(reinterpret_cast<const bf16*>(rows + j * 256), xm[j]);
+    for (int r = 0; r < TT; ++r) {
+      const int t = t0 + r;
+      if (t >= t_end) break;
+      float cur[4];
+      load4(reinterpret_cast<const bf16*>(rows + (r + 3) * 256), cur);
+      float y[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float acc = bias[c];
+        acc = fmaf(wt[c][0], xm[0][c], acc);
+        acc = fmaf(wt[c][1], xm[1][c], acc);
+        acc = fmaf(wt[c][2], xm[2][c], acc);
+        y[c] = silu_fast(fmaf(wt[c][3], cur[c], acc));
+      }
+      if (region < 2) {
+        float ss = y[0] * y[0] + y[1] * y[1] + y[2] * y[2] + y[3] * y[3];
+        ss = group_sum(ss, lanes_per_head);
+        const float inv = rsqrtf(ss + p.l2_eps) * qs;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) y[c] *= inv;
+      }
+      store4(dst + (size_t)t * row_stride, y);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) { xm[0][c] = xm[1][c]; xm[1][c] = xm[2][c]; xm[2][c] = cur[c]; }
+    }
+    // tokens in the first 3 positions of a sequence: redo with the conv state
+    {
+      const int seq0 = find_seq(p.cu, p.num_seqs, p.total, max(t0 - 3, 0));
+      for (int sq = seq0; sq < p.num_seqs; ++sq) {
+        const int st = seq_start(p.cu, p.num_seqs, p.total, sq);
+        if (st >= t_end) break;
+        for (int t = max(st, t0); t < min(st + 3, t_end); ++t) {
+          const int seq = find_seq(p.cu, p.num_seqs, p.total, t);
+          const int pos = t - seq_start(p.cu, p.num_seqs, p.total, seq);
+          float cur[4], y[4];
+          load4(xg + (size_t)t * p.C + c0, cur);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) y[c] = fmaf(wt[c][3], cur[c], bias[c]);
+#pragma unroll
+          for (int j = 0; j < 3; ++j) {
+            const int si = pos + j;
+            float xv[4];
+            if (si < 3) {
+#pragma unroll
+              for (int c = 0; c < 4; ++c)
+                xv[c] = (st_in != nullptr && si >= 0) ? __bfloat162float(st_in[((size_t)seq * p.C + c0 + c) * 3 + si]) : 0.f;
+            } else {
+              load4(xg + (size_t)(t - 3 + j) * p.C + c0, xv);
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) y[c] = fmaf(wt[c][j], xv[c], y[c]);
+          }
+#pragma unroll
+          for (int c = 0; c < 4; ++c) y[c] = silu_fast(y[c]);
+          if (region < 2) {
+            float ss = y[0] * y[0] + y[1] * y[1] + y[2] * y[2] + y[3] * y[3];
+            ss = group_sum(ss, lanes_per_head);
+            const float inv = rsqrtf(ss + p.l2_eps) * qs;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) y[c] *= inv;
+          }
+          store4(dst + (size_t)t * row_stride, y);
+        }
+      }
+    }
+    if (region == 2) {
+      const int hps = 128 / p.Dv;
+      const int h0 = (strip * 128 - 2 * kd) / p.Dv;
+      const bf16* a = static_cast<const bf16*>(p.a);
+      const bf16* b = static_cast<const bf16*>(p.b);
+      for (int idx = lane; idx < TT * hps; idx += 32) {
+        const int t = t0 + idx / hps;
+        const int h = h0 + idx % hps;
+        if (t < t_end) {
+          const size_t o = (size_t)t * p.Nv + h;
+          p.beta[o] = sigmoidf_(__bfloat162float(b[o]));
+          p.g[o] = -expf(p.A_log[h]) * softplusf_(__bfloat162float(a[o]) + p.dt_bias[h]);
+        }
+      }
+    }
+    __syncthreads();     // the tile is read; the next TMA may overwrite it
+  }
+}
+
 // New conv state of each sequence: the last 3 entries of [state_in ; x].
 // One thread per (sequence, channel); it reads its old state before writing,
 // so state_out may alias state_in.
@@ -236,12 +390,30 @@ __global__ void conv_state_kernel(ConvGatingArgs p) {
 
 template <typename Tin, typename Tout>
 cudaError_t launch_typed(const ConvGatingArgs& p, cudaStream_t s) {
-  const long long items = (long long)(p.C / 128) * ((p.total + TB - 1) / TB);
-  if (items > 0) {
-    const int blocks = (int)((items + WARPS - 1) / WARPS);
-    conv_gating_kernel<Tin, Tout><<<blocks, WARPS * 32, 0, s>>>(p);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+  bool tiled = false;
+  if (std::is_same<Tin, bf16>::value && p.C % 1024 == 0 && p.total > 0) {
+    CUtensorMap m;
+    if (make_tmap_2d(&m, p.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.total, p.C, 128, TROWS,
+                     CU_TENSOR_MAP_SWIZZLE_NONE)) {
+      cudaError_t e = cudaFuncSetAttribute(conv_gating_tile_kernel<Tout>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TILE_SMEM);
+      if (e != cudaSuccess) return e;
+      const int ntiles = ((p.total + TT - 1) / TT) * (p.C / 1024);
+      const int blocks = std::min(ntiles, 152 * 3);
+      conv_gating_tile_kernel<Tout><<<blocks, 256, TILE_SMEM, s>>>(m, p);
+      e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+      tiled = true;
+    }
+  }
+  if (!tiled) {
+    const long long items = (long long)(p.C / 128) * ((p.total + TB - 1) / TB);
+    if (items > 0) {
+      const int blocks = (int)((items + WARPS - 1) / WARPS);
+      conv_gating_kernel<Tin, Tout><<<blocks, WARPS * 32, 0, s>>>(p);
+      cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+    }
   }
   if (p.state_out != nullptr) {
     dim3 grid((p.C + 255) / 256, p.num_seqs);
