@@ -268,6 +268,33 @@ int gdn_chunk_prefill_fp32(const gdn_dims* dims, const int32_t* cu_seqlens, cons
   return GDN_OK;
 }
 
+int gdn_chunk_prefill_static(const gdn_dims* dims, const int32_t* cu_seqlens, const void* q,
+                             const void* k, const void* v, int in_dtype, const float* g,
+                             const float* beta, float scale, const float* initial_state,
+                             float* final_state, void* o, int out_dtype, void* stream) {
+  const char* fn = "gdn_chunk_prefill_static";
+  gdn::ChunkArgs p;
+  int st = chunk_common(fn, dims, cu_seqlens, q, k, v, in_dtype, g, beta, initial_state,
+                        final_state, o, out_dtype, &p);
+  if (st != GDN_OK) return st;
+  if (!gdn::chunk_tc_supported(p))
+    return fail(GDN_ERR_UNSUPPORTED, "%s: needs bf16 q/k/v and 128-wide heads", fn);
+  const size_t need = gdn::chunk_tc_workspace_bytes(dims->num_seqs, dims->total_tokens, dims->num_v_heads);
+  if (need > gdn::kStaticScratchBytes)
+    return fail(GDN_ERR_INVALID_ARG,
+                "%s: this problem needs %zu bytes of scratch, more than the library's fixed %zu bytes; "
+                "use gdn_chunk_prefill with a caller workspace", fn, need, gdn::kStaticScratchBytes);
+  void* scratch = nullptr;
+  cudaError_t e = gdn::static_scratch(&scratch);
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  p.scale = scale;
+  p.workspace = scratch;
+  p.workspace_bytes = gdn::kStaticScratchBytes;
+  e = gdn::launch_chunk_tc(p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  return GDN_OK;
+}
+
 int gdn_recurrent_decode(const gdn_dims* dims, const int32_t* cu_seqlens, const void* q,
                          const void* k, const void* v, int in_dtype, const float* g,
                          const float* beta, float scale, float* state, void* o, int out_dtype,

@@ -37,6 +37,8 @@
 #include "tc_util.cuh"
 #include "tmap.cuh"
 
+#include <mutex>
+
 namespace gdn {
 namespace {
 
@@ -759,6 +761,36 @@ cudaError_t launch_chunk_tc(const ChunkArgs& p, cudaStream_t s) {
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return p.out_bf16 ? launch_scan<bf16>(mq, mk, mv, p, s) : launch_scan<float>(mq, mk, mv, p, s);
+}
+
+// ---------------------------------------------------------------------------
+// Library-owned scratch for callers that cannot allocate device memory.
+// A fixed array in the module's device memory replaces the caller-provided
+// workspace of gdn_chunk_prefill.  Every device that loads the library holds
+// it until the process exits; every call shares it.
+// ---------------------------------------------------------------------------
+namespace {
+__device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+std::mutex g_static_mu;
+void* g_static_ptr[64];
+}  // namespace
+
+cudaError_t static_scratch(void** ptr) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (g_static_ptr[dev] == nullptr) {
+    // host code sees only a stand-in for the array: ask the runtime for its
+    // address on the current device (once per device)
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess) return e;
+    g_static_ptr[dev] = p;
+  }
+  *ptr = g_static_ptr[dev];
+  return cudaSuccess;
 }
 
 }  // namespace gdn

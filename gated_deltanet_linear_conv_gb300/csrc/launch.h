@@ -85,5 +85,8 @@ cudaError_t launch_chunk_simt(const ChunkArgs& p, cudaStream_t s);
 bool chunk_tc_supported(const ChunkArgs& p);
 size_t chunk_tc_workspace_bytes(int num_seqs, int total, int Nv);
 cudaError_t launch_chunk_tc(const ChunkArgs& p, cudaStream_t s);
+// Fixed-size device scratch owned by the library (see gdn_chunk_prefill_static).
+constexpr size_t kStaticScratchBytes = (size_t)32 << 20;
+cudaError_t static_scratch(void** ptr);
 
 }  // namespace gdn

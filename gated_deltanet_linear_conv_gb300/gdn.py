@@ -21,8 +21,8 @@ GDN_BF16, GDN_F32 = 0, 1
 
 EXPORTS = ('gdn_version', 'gdn_last_error_string', 'gdn_check_device_error', 'gdn_conv_gating',
            'gdn_gating', 'gdn_chunk_prefill_workspace_size', 'gdn_chunk_prefill',
-           'gdn_chunk_prefill_fp32', 'gdn_recurrent_decode', 'gdn_gated_rmsnorm',
-           'gdn_decode_fused')
+           'gdn_chunk_prefill_fp32', 'gdn_chunk_prefill_static', 'gdn_recurrent_decode',
+           'gdn_gated_rmsnorm', 'gdn_decode_fused')
 
 
 class gdn_dims(ctypes.Structure):
@@ -49,6 +49,7 @@ _SIGS = {
     'gdn_chunk_prefill_workspace_size': ([_DIMS, ctypes.POINTER(_SZ)], _I),
     'gdn_chunk_prefill': ([_DIMS, _P, _P, _P, _P, _I, _P, _P, _F, _P, _P, _P, _I, _P, _SZ, _P], _I),
     'gdn_chunk_prefill_fp32': ([_DIMS, _P, _P, _P, _P, _I, _P, _P, _F, _P, _P, _P, _I, _P], _I),
+    'gdn_chunk_prefill_static': ([_DIMS, _P, _P, _P, _P, _I, _P, _P, _F, _P, _P, _P, _I, _P], _I),
     'gdn_recurrent_decode': ([_DIMS, _P, _P, _P, _P, _I, _P, _P, _F, _P, _P, _I, _P], _I),
     'gdn_gated_rmsnorm': ([_I64, ctypes.c_int32, _P, _I, _P, _I, _P, _F, _P, _I, _P], _I),
     'gdn_decode_fused': ([_DIMS, _P, _I, _P, _P, _P, _P, _P, _P, _P, _F, _F, _P, _P, _P, _F,

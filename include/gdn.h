@@ -175,6 +175,35 @@ int gdn_chunk_prefill_fp32(const gdn_dims* dims, const int32_t* cu_seqlens,
                            const float* initial_state, float* final_state,
                            void* o, int out_dtype, void* stream);
 
+/* gdn_chunk_prefill_static -- gdn_chunk_prefill for callers that cannot
+ * allocate device memory: hosts that reserve the device's memory up front
+ * (a serving engine's arena, another framework's plugin interface) and have
+ * no allocator to hand out a workspace at call time.  No counterpart on the
+ * source pages; this is a packaging choice of the library.
+ *
+ * Same arguments as gdn_chunk_prefill without the workspace: the library uses
+ * its own fixed 32 MiB scratch array in device memory instead, which every
+ * GPU that loads the library holds until the process exits.  This call never
+ * allocates or frees.
+ *   - Supported inputs: bf16 q/k/v with Dk = Dv = 128 (else
+ *     GDN_ERR_UNSUPPORTED).
+ *   - Size limit: the workspace that gdn_chunk_prefill_workspace_size()
+ *     reports for these dims must be at most 32 MiB (for 32 value heads,
+ *     about 2,000 chunks of 64 tokens); larger problems return
+ *     GDN_ERR_INVALID_ARG and should use gdn_chunk_prefill.
+ *   - The first call on a device looks up the scratch array's device address
+ *     (once per device, with that device current); make that first call before
+ *     any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents
+ *     (every call rewrites what it reads, so nothing needs clearing).  Calls
+ *     that overlap on the GPU (different streams, or different host threads)
+ *     race on it: serialise them. */
+int gdn_chunk_prefill_static(const gdn_dims* dims, const int32_t* cu_seqlens,
+                             const void* q, const void* k, const void* v, int in_dtype,
+                             const float* g, const float* beta, float scale,
+                             const float* initial_state, float* final_state,
+                             void* o, int out_dtype, void* stream);
+
 /* ------------------------------------------------------------------------
  * gdn_recurrent_decode -- step a5: the token-by-token gated delta rule with
  * the fp32 state read-modify-written in place ([RFC] 2.2 op 5 and 3.1.3

@@ -1,0 +1,64 @@
+"""gdn_chunk_prefill_static: the chunk prefill for callers that cannot
+allocate device memory (hosts that reserve the device up front and give the
+library no allocator).  It runs on the library's fixed scratch array instead of
+a caller workspace.  This file sorts last so that a stop-at-first-failure run
+has already run every other test; it also passes on its own in a fresh
+process.  Calls go straight through the C ABI."""
+
+import ctypes
+import math
+
+import pytest
+import torch
+
+from gated_deltanet_linear_conv_gb300 import gdn
+from gated_deltanet_linear_conv_gb300 import inputs as I
+from helpers import TOL_BF16, np64, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+
+def _static_call(q, k, v, g, beta, scale, S0, ST, o, cu, num_seqs):
+    T, Nk, Dk = q.shape
+    Nv, Dv = v.shape[1], v.shape[2]
+    d = gdn.gdn_dims(num_seqs, T, Nk, Nv, Dk, Dv)
+    ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+    st = gdn.lib().gdn_chunk_prefill_static(
+        ctypes.byref(d), ptr(cu), q.data_ptr(), k.data_ptr(), v.data_ptr(), gdn.GDN_BF16,
+        g.data_ptr(), beta.data_ptr(), float(scale), ptr(S0), ST.data_ptr(), o.data_ptr(),
+        gdn.GDN_F32, torch.cuda.current_stream().cuda_stream)
+    assert st == gdn.GDN_OK, gdn.lib().gdn_last_error_string()
+
+
+def test_static_scratch_matches_workspace_call_twice():
+    shape = I.MixerShape(2, 4, 128, 128)
+    lengths = [130, 64, 1, 300]
+    cu = I.make_core_inputs(91, lengths, shape, dtype=torch.bfloat16, S0_std=0.1).cu_seqlens().cuda()
+    for call, seed in enumerate((91, 92)):          # two calls in a row, different data
+        c = I.make_core_inputs(seed, lengths, shape, dtype=torch.bfloat16, S0_std=0.1)
+        q, k, v = c.q.cuda(), c.k.cuda(), c.v.cuda()
+        g = (-torch.nn.functional.softplus(c.a.float())).cuda()
+        beta = torch.sigmoid(c.b.float()).cuda()
+        S0 = c.S0.cuda()
+        o_ref, S_ref = gdn.chunk_prefill(q, k, v, g, beta, 1 / math.sqrt(128), initial_state=S0,
+                                         cu_seqlens=cu, out_dtype=torch.float32)
+        o = torch.empty_like(o_ref)
+        ST = torch.empty_like(S_ref)
+        _static_call(q, k, v, g, beta, 1 / math.sqrt(128), S0, ST, o, cu, len(lengths))
+        torch.cuda.synchronize()
+        assert rel_l2(np64(o), np64(o_ref)) <= TOL_BF16, call
+        assert rel_l2(np64(ST), np64(S_ref)) <= TOL_BF16, call
+    gdn.check_device_error()
+
+
+def test_static_scratch_rejects_too_large():
+    T, Nk, Nv, D = 131072, 16, 32, 128
+    d = gdn.gdn_dims(1, T, Nk, Nv, D, D)
+    x = torch.empty(16, dtype=torch.bfloat16, device='cuda')      # never read: rejected before launch
+    f = torch.empty(16, device='cuda')
+    st = gdn.lib().gdn_chunk_prefill_static(
+        ctypes.byref(d), None, x.data_ptr(), x.data_ptr(), x.data_ptr(), gdn.GDN_BF16, f.data_ptr(),
+        f.data_ptr(), 1.0, None, f.data_ptr(), x.data_ptr(), gdn.GDN_BF16,
+        torch.cuda.current_stream().cuda_stream)
+    assert st == gdn.GDN_ERR_INVALID_ARG
+    assert b'scratch' in gdn.lib().gdn_last_error_string()
