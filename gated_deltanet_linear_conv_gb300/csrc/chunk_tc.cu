@@ -49,7 +49,7 @@ constexpr int DK = 128;
 constexpr int DV = 128;
 constexpr uint32_t WAIT_LIMIT = 1u << 22;
 constexpr int FS = 68;        // fp32 matrix row stride (16-byte aligned rows)
-constexpr uint32_t TILE_T_BYTES = 16384;   // T diag(beta) | T diag(beta gamma), bf16
+constexpr uint32_t TILE_T_BYTES = 32768;   // workspace per (chunk, value head): 4 bf16 tiles
 
 // ---------------------------------------------------------------------------
 // shared helpers
@@ -216,17 +216,39 @@ __device__ void invert_unit_lower(const float* AF, float* TF, int tid) {
 }
 
 // ---------------------------------------------------------------------------
-// kernel 1: T tiles, parallel over (chunk slot, value head)
+// kernel 1: per (chunk slot, value head), in parallel over all of them
+//   D1 = [K; Q] K^T (rows 0-63 K K^T, rows 64-127 Q K^T), A and P from it,
+//   T = (I + A)^-1, then W = T diag(beta gamma) K.  Writes T diag(beta), P
+//   and -W as bf16 128-byte-swizzled tiles to the workspace slot.
 // ---------------------------------------------------------------------------
-constexpr uint32_t S1_K = 0;                        // K box0 | K box1 (16 KB)
-constexpr uint32_t S1_AF = 16384;                   // A fp32 [64][FS]
+constexpr uint32_t S1_QK = 0;                       // K box0 | Q box0 | K box1 | Q box1 (32 KB)
+constexpr uint32_t S1_TBG = 32768;                  // T diag(beta gamma) | zeros (16 KB)
+constexpr uint32_t S1_AF = 49152;                   // A fp32 [64][FS]
 constexpr uint32_t S1_TF = S1_AF + 64 * FS * 4;     // T fp32 [64][FS]
 constexpr uint32_t S1_VEC = S1_TF + 64 * FS * 4;    // G, beta, beta*gamma (3 x 64 floats)
 constexpr uint32_t S1_BAR = S1_VEC + 3 * 64 * 4;
 constexpr uint32_t S1_SMEM = S1_BAR + 64 + 1024;
+// workspace slot: [T diag(beta) | P | -W dk 0-63 | -W dk 64-127], 8 KB each
+constexpr uint32_t WS_TB = 0, WS_P = 8192, WS_W = 16384;
+
+// Write 64 bf16 values as swizzled row `row` of a 64-column block in global memory.
+__device__ __forceinline__ void st_row64_global(uint8_t* dst, uint32_t row, const float* v, float sc) {
+#pragma unroll
+  for (int ch = 0; ch < 8; ++ch) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __nv_bfloat162 h = __floats2bfloat162_rn(sc * v[ch * 8 + 2 * i], sc * v[ch * 8 + 2 * i + 1]);
+      w[i] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    const uint32_t off = row * 128u + ((((uint32_t)ch ^ (row & 7u)) & 7u) << 4);
+    *reinterpret_cast<uint4*>(dst + off) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
 
 __global__ void __launch_bounds__(128)
-chunk_solve_kernel(const __grid_constant__ CUtensorMap tmk, ChunkArgs p) {
+chunk_solve_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                   ChunkArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* AF = reinterpret_cast<float*>(sm + S1_AF);
@@ -251,15 +273,20 @@ chunk_solve_kernel(const __grid_constant__ CUtensorMap tmk, ChunkArgs p) {
   if (!seq_bounds(p.cu, p.num_seqs, p.total, s, bos, eos)) return;   // reported by the scan kernel
   if (c < 0 || c * CT >= eos - bos) return;                           // slot not used
   const int c0 = bos + c * CT, len = min(CT, eos - c0);
+  uint8_t* ws = static_cast<uint8_t*>(p.workspace) + ((size_t)slot * p.Nv + h) * TILE_T_BYTES;
 
   if (tid == 0) {
     mbar_init(bar, 1);
     fence_barrier_init();
-    mbar_arrive_expect_tx(bar, 16384);
-    tma_load_2d(sm + S1_K, &tmk, bar, hk * DK, c0);
-    tma_load_2d(sm + S1_K + 8192, &tmk, bar, hk * DK + 64, c0);
+    mbar_arrive_expect_tx(bar, 32768);
+    tma_load_2d(sm + S1_QK, &tmk, bar, hk * DK, c0);
+    tma_load_2d(sm + S1_QK + 8192, &tmq, bar, hk * DK, c0);
+    tma_load_2d(sm + S1_QK + 16384, &tmk, bar, hk * DK + 64, c0);
+    tma_load_2d(sm + S1_QK + 24576, &tmq, bar, hk * DK + 64, c0);
   }
-  if (warp == 0) tmem_alloc(tslot, 64);
+  if (warp == 0) tmem_alloc(tslot, 256);
+  for (int i = tid * 16; i < 8192; i += 128 * 16)       // zero rows 64-127 of the W-product A operand
+    *reinterpret_cast<uint4*>(sm + S1_TBG + 8192 + i) = make_uint4(0u, 0u, 0u, 0u);
   if (tid < CT) {
     Gs[tid] = tid < len ? p.g[(size_t)(c0 + tid) * p.Nv + h] : 0.f;
     Bet[tid] = tid < len ? p.beta[(size_t)(c0 + tid) * p.Nv + h] : 0.f;
@@ -268,6 +295,8 @@ chunk_solve_kernel(const __grid_constant__ CUtensorMap tmk, ChunkArgs p) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tslot;
+  const uint32_t lane_base = tbase + ((uint32_t)(warp * 32) << 16);
+  const uint32_t sb = smem_u32(sm);
   if (warp == 0) {
     float* Gam = TF;            // scratch for the cumsum helper (TF is rewritten later)
     float* Dec = TF + 64;
@@ -275,26 +304,27 @@ chunk_solve_kernel(const __grid_constant__ CUtensorMap tmk, ChunkArgs p) {
     BG[lane] = Bet[lane] * Gam[lane];
     BG[lane + 32] = Bet[lane + 32] * Gam[lane + 32];
   }
-  const bool loaded = mbar_wait(bar, 0, WAIT_LIMIT);
-  if (__syncthreads_and(loaded ? 1 : 0)) {
+  bool ok = mbar_wait(bar, 0, WAIT_LIMIT);
+  if (__syncthreads_and(ok ? 1 : 0)) {
     tc_fence_after();
     if (tid == 0) {
-      // K K^T: 64 x 64 x 128, rows of the result on lanes 16 w + (0..15)
-      const uint32_t id = idesc_bf16(64, 64, false, false);
-      const uint32_t kb = smem_u32(sm + S1_K);
+      const uint32_t id = idesc_bf16(128, 64, false, false);
+      const uint64_t a = sdesc_sw128(sb + S1_QK, 16, 1024);
       for (int ks = 0; ks < DK / 16; ++ks) {
-        const uint64_t d = sdesc_sw128(kb + kstep_offset(true, ks, 8192), 16, 1024);
-        mma_bf16(tbase, d, d, id, ks > 0);
+        const uint32_t o = kstep_offset(true, ks, 16384) >> 4;
+        mma_bf16(tbase, a + o, a + o, id, ks > 0);
       }
       mma_commit(bar);
     }
-    const bool done = mbar_wait(bar, 1, WAIT_LIMIT);
-    if (__syncthreads_and(done ? 1 : 0)) {
-      tc_fence_after();
+    ok = mbar_wait(bar, 1, WAIT_LIMIT);
+  }
+  if (__syncthreads_and(ok ? 1 : 0)) {
+    tc_fence_after();
+    {
       float v[64];
-      tm_ld64(tbase + ((uint32_t)(warp * 32) << 16), v);
-      if (lane < 16) {
-        const int r = warp * 16 + lane;
+      tm_ld64(lane_base, v);
+      if (tid < CT) {                       // K K^T row r -> lower triangle of A
+        const int r = tid;
         const float gr = Gs[r], br = Bet[r];
 #pragma unroll
         for (int jb = 0; jb < 4; ++jb) {
@@ -304,28 +334,63 @@ chunk_solve_kernel(const __grid_constant__ CUtensorMap tmk, ChunkArgs p) {
               if (j < r) AF[r * FS + j] = br * __expf(gr - Gs[j]) * v[j];
           }
         }
-      }
-      tc_fence_before();
-      __syncthreads();
-      invert_unit_lower(AF, TF, tid);
-      uint8_t* dst = static_cast<uint8_t*>(p.workspace) + ((size_t)slot * p.Nv + h) * TILE_T_BYTES;
-      for (int idx = tid; idx < CT * 8; idx += 128) {
-        const int r = idx >> 3, ch = idx & 7;
-        const float4 t0 = *reinterpret_cast<const float4*>(TF + r * FS + ch * 8);
-        const float4 t1 = *reinterpret_cast<const float4*>(TF + r * FS + ch * 8 + 4);
-        const float t[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
-        uint32_t wa[4], wb[4];
+      } else {                              // Q K^T row r -> P = M o Q K^T
+        const int r = tid - CT;
+        const float gr = Gs[r];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int j = ch * 8 + 2 * i;
-          __nv_bfloat162 ha = __floats2bfloat162_rn(t[2 * i] * Bet[j], t[2 * i + 1] * Bet[j + 1]);
-          __nv_bfloat162 hb = __floats2bfloat162_rn(t[2 * i] * BG[j], t[2 * i + 1] * BG[j + 1]);
-          wa[i] = *reinterpret_cast<uint32_t*>(&ha);
-          wb[i] = *reinterpret_cast<uint32_t*>(&hb);
+        for (int jb = 0; jb < 4; ++jb) {
+          if (jb * 16 <= r) {
+#pragma unroll
+            for (int j = jb * 16; j < jb * 16 + 16; ++j) v[j] = j <= r ? __expf(gr - Gs[j]) * v[j] : 0.f;
+          } else {
+#pragma unroll
+            for (int j = jb * 16; j < jb * 16 + 16; ++j) v[j] = 0.f;
+          }
         }
-        const uint32_t sw = r * 128u + ((((uint32_t)ch ^ (uint32_t)(r & 7)) & 7u) << 4);
-        *reinterpret_cast<uint4*>(dst + sw) = make_uint4(wa[0], wa[1], wa[2], wa[3]);
-        *reinterpret_cast<uint4*>(dst + 8192 + sw) = make_uint4(wb[0], wb[1], wb[2], wb[3]);
+        st_row64_global(ws + WS_P, r, v, 1.f);
+      }
+    }
+    tc_fence_before();
+    __syncthreads();
+    invert_unit_lower(AF, TF, tid);
+    for (int idx = tid; idx < CT * 8; idx += 128) {
+      const int r = idx >> 3, ch = idx & 7;
+      const float4 t0 = *reinterpret_cast<const float4*>(TF + r * FS + ch * 8);
+      const float4 t1 = *reinterpret_cast<const float4*>(TF + r * FS + ch * 8 + 4);
+      const float t[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+      uint32_t wa[4], wb[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int j = ch * 8 + 2 * i;
+        __nv_bfloat162 ha = __floats2bfloat162_rn(t[2 * i] * Bet[j], t[2 * i + 1] * Bet[j + 1]);
+        __nv_bfloat162 hb = __floats2bfloat162_rn(t[2 * i] * BG[j], t[2 * i + 1] * BG[j + 1]);
+        wa[i] = *reinterpret_cast<uint32_t*>(&ha);
+        wb[i] = *reinterpret_cast<uint32_t*>(&hb);
+      }
+      const uint32_t sw = r * 128u + ((((uint32_t)ch ^ (uint32_t)(r & 7)) & 7u) << 4);
+      *reinterpret_cast<uint4*>(ws + WS_TB + sw) = make_uint4(wa[0], wa[1], wa[2], wa[3]);
+      *reinterpret_cast<uint4*>(sm + S1_TBG + sw) = make_uint4(wb[0], wb[1], wb[2], wb[3]);
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) {
+      // W = [T diag(beta gamma); 0] K  (rows 0-63 of the 128 x 128 result)
+      const uint32_t id = idesc_bf16(128, 128, false, true);
+      const uint64_t a = sdesc_sw128(sb + S1_TBG, 16, 1024);
+      const uint64_t b = sdesc_sw128(sb + S1_QK, 16384, 1024);
+      for (int ks = 0; ks < CT / 16; ++ks) mma_bf16(tbase + 64, a + ks * 2, b + ks * 128, id, ks > 0);
+      mma_commit(bar);
+    }
+    ok = mbar_wait(bar, 0, WAIT_LIMIT);
+    if (__syncthreads_and(ok ? 1 : 0)) {
+      tc_fence_after();
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float v[64];
+        tm_ld64(lane_base + 64 + half * 64, v);
+        if (tid < CT) st_row64_global(ws + WS_W + half * 8192, tid, v, -1.f);
       }
     } else if (tid == 0) {
       raise_error(p.err, kDevErrTimeout);
@@ -335,39 +400,38 @@ chunk_solve_kernel(const __grid_constant__ CUtensorMap tmk, ChunkArgs p) {
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tbase, 64);
+  if (warp == 0) tmem_dealloc(tbase, 256);
 }
 
 // ---------------------------------------------------------------------------
 // kernel 2: the scan over chunks, three warpgroups
 // ---------------------------------------------------------------------------
 constexpr int NT2 = 384;
-constexpr uint32_t K2_QK = 0;          // 3 stages x [Q box0 | K box0 | Q box1 | K box1] (32 KB)
-constexpr uint32_t K2_V = 98304;       // V box0 | V box1 (16 KB)
-constexpr uint32_t K2_TB = 114688;     // T diag(beta) | T diag(beta gamma) (16 KB)
-constexpr uint32_t K2_P = 131072;      // 2 x P [r][j] (8 KB)
-constexpr uint32_t K2_WMN = 147456;    // W as [dk rows][r] (16 KB)
-constexpr uint32_t K2_UK = 163840;     // U^T as [dv rows][j] (16 KB)
-constexpr uint32_t K2_SMN = 180224;    // S as [dk rows][dv], two 64-column blocks (32 KB)
-constexpr uint32_t K2_VEC = 212992;    // 3 stages x (G, gamma, dec) (768 B each)
+constexpr uint32_t K2_ST = 0;          // 2 stages x [-W dk0-63 | Q box0 | -W dk64-127 | Q box1 | K box0 | K box1]
+constexpr uint32_t STAGE_BYTES = 49152;
+constexpr uint32_t K2_P = 98304;       // 2 x P [r][j] (8 KB)
+constexpr uint32_t K2_VT = 114688;     // V box0 | V box1 | T diag(beta) | zeros (32 KB)
+constexpr uint32_t K2_UK = 147456;     // U^T as [dv rows][j] (16 KB)
+constexpr uint32_t K2_SMN = 163840;    // S as [dk rows][dv], two 64-column blocks (32 KB)
+constexpr uint32_t K2_VEC = 196608;    // 3 x (G, gamma, dec) (768 B each)
 constexpr uint32_t K2_BAR = K2_VEC + 3 * 768;
 constexpr uint32_t K2_SMEM = K2_BAR + 256 + 1024;
 static_assert(K2_SMEM <= 232448, "shared memory budget");
 
-// tensor memory columns
-constexpr uint32_t TM_D1 = 0, TM_WT = 64, TM_UT = 128, TM_OT = 256, TM_S = 384;
+// tensor memory: two accumulators of [U^T (64 columns) | O^T (64 columns)], then S
+constexpr uint32_t TM_ACC = 0, TM_S = 256;
 
 struct ScanBars {
-  uint64_t qk[3];   // q/k tiles of a stage landed
-  uint64_t vt;      // v and T tiles landed
-  uint64_t p;       // PREP products done
+  uint64_t stl[2];  // stage tiles of a chunk landed (q, k, -W, P)
+  uint64_t vt;      // v and T diag(beta) tiles landed
+  uint64_t p;       // PREP product done
   uint64_t pv;      // PREP gates of a chunk written (G, gamma, dec)
-  uint64_t sc;      // OUT scaled Q and K of a chunk in place and wrote W
-  uint64_t ready[2];// PREP of a chunk done
-  uint64_t fg;      // U^T - S^T W^T and S^T Q~^T done
-  uint64_t gh[2];   // U^T P^T and the state update done
+  uint64_t sc;      // OUT scaled Q and K of a chunk in place
+  uint64_t ready[2];// a chunk is ready for STATE
+  uint64_t fg;      // [U^T | O^T] += S^T [-W; Q~]^T done
+  uint64_t gh[2];   // O^T += U^T P^T and the state update done
   uint64_t st[2];   // U^T of a chunk read out of tensor memory
-  uint64_t of[2];   // output of a chunk stored
+  uint64_t of[2];   // O^T of a chunk stored
   uint32_t tslot;
   int abort;
 };
@@ -404,20 +468,22 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
   }
   const int n = (eos - bos + CT - 1) / CT;
   const int slot0 = slot_base(p, s);
+  const uint8_t* wsb = static_cast<const uint8_t*>(p.workspace);
+  auto ws_tile = [&](int c) { return wsb + ((size_t)(slot0 + c) * p.Nv + h) * TILE_T_BYTES; };
 
   if (tid == 0) {
-    for (int i = 0; i < 3; ++i) mbar_init(&B->qk[i], 1);
-    mbar_init(&B->vt, 1);
-    mbar_init(&B->p, 1);
-    mbar_init(&B->pv, 1);
-    mbar_init(&B->sc, 1);
-    mbar_init(&B->fg, 1);
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&B->stl[i], 1);
       mbar_init(&B->ready[i], 1);
       mbar_init(&B->gh[i], 1);
       mbar_init(&B->st[i], 1);
       mbar_init(&B->of[i], 1);
     }
+    mbar_init(&B->vt, 1);
+    mbar_init(&B->p, 1);
+    mbar_init(&B->pv, 1);
+    mbar_init(&B->sc, 1);
+    mbar_init(&B->fg, 1);
     B->abort = 0;
     fence_barrier_init();
     prefetch_tmap(&tmq);
@@ -425,6 +491,9 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
     prefetch_tmap(&tmv);
   }
   if (warp == 0) tmem_alloc(&B->tslot, 512);
+  for (int i = tid * 16; i < 8192; i += NT2 * 16)      // rows 64-127 of the [T diag(beta); 0] operand
+    *reinterpret_cast<uint4*>(sm + K2_VT + 24576 + i) = make_uint4(0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -432,47 +501,43 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
   const uint32_t lane_base = tbase + ((uint32_t)((warp & 3) * 32) << 16);
   const uint32_t sb = smem_u32(sm);
 
-  auto issue_qk = [&](int c) {
+  // stage loads of chunk c: q, k tiles (TMA), -W and P (bulk copies from the workspace)
+  auto issue_stage = [&](int c) {
     const int t = bos + c * CT;
-    const uint32_t base = K2_QK + (c % 3) * 32768;
-    uint64_t* bar = &B->qk[c % 3];
-    mbar_arrive_expect_tx(bar, 4 * 8192);
-    tma_load_2d(sm + base, &tmq, bar, hk * DK, t);
-    tma_load_2d(sm + base + 8192, &tmk, bar, hk * DK, t);
-    tma_load_2d(sm + base + 16384, &tmq, bar, hk * DK + 64, t);
-    tma_load_2d(sm + base + 24576, &tmk, bar, hk * DK + 64, t);
+    const uint32_t st = K2_ST + (c & 1) * STAGE_BYTES;
+    uint64_t* bar = &B->stl[c & 1];
+    mbar_arrive_expect_tx(bar, 4 * 8192 + 3 * 8192);
+    tma_load_2d(sm + st + 8192, &tmq, bar, hk * DK, t);
+    tma_load_2d(sm + st + 24576, &tmq, bar, hk * DK + 64, t);
+    tma_load_2d(sm + st + 32768, &tmk, bar, hk * DK, t);
+    tma_load_2d(sm + st + 40960, &tmk, bar, hk * DK + 64, t);
+    const uint8_t* src = ws_tile(c);
+    bulk_load(sm + st, src + WS_W, 8192, bar);
+    bulk_load(sm + st + 16384, src + WS_W + 8192, 8192, bar);
+    bulk_load(sm + K2_P + (c & 1) * 8192, src + WS_P, 8192, bar);
   };
   auto issue_vt = [&](int c) {
     const int t = bos + c * CT;
-    mbar_arrive_expect_tx(&B->vt, 2 * 8192 + TILE_T_BYTES);
-    tma_load_2d(sm + K2_V, &tmv, &B->vt, h * DV, t);
-    tma_load_2d(sm + K2_V + 8192, &tmv, &B->vt, h * DV + 64, t);
-    const uint8_t* src = static_cast<const uint8_t*>(p.workspace) + ((size_t)(slot0 + c) * p.Nv + h) * TILE_T_BYTES;
-    bulk_load(sm + K2_TB, src, TILE_T_BYTES, &B->vt);
+    mbar_arrive_expect_tx(&B->vt, 2 * 8192 + 8192);
+    tma_load_2d(sm + K2_VT, &tmv, &B->vt, h * DV, t);
+    tma_load_2d(sm + K2_VT + 8192, &tmv, &B->vt, h * DV + 64, t);
+    bulk_load(sm + K2_VT + 16384, ws_tile(c) + WS_TB, 8192, &B->vt);
   };
 
   if (wg == 0) {
     // ============================== PREP ==============================
-    int issued_qk = 0, issued_vt = 0;     // chunks whose loads were issued (thread 0)
-    if (wt == 0 && n > 0) {
-      issue_qk(0);
-      if (n > 1) issue_qk(1);
-      issue_vt(0);
-      issued_qk = n > 1 ? 2 : 1;
-      issued_vt = 1;
-    }
+    int issued_vt = 0;
+    if (wt == 0 && n > 0) { issue_vt(0); issued_vt = 1; }
     float g_next = 0.f;
     if (wt < CT && n > 0 && wt < eos - bos) g_next = p.g[(size_t)(bos + wt) * p.Nv + h];
     int c = 0;
     bool fail = false;
     for (; c < n; ++c) {
-      const int st3 = c % 3, b = c & 1;
-      const uint32_t qk = K2_QK + st3 * 32768;
-      float* Gs = reinterpret_cast<float*>(sm + K2_VEC + st3 * 768);
+      const int b = c & 1;
+      float* Gs = reinterpret_cast<float*>(sm + K2_VEC + (c % 3) * 768);
       float* Gam = Gs + CT;
       float* Dec = Gam + CT;
       const int c0 = bos + c * CT;
-      // gates of this chunk (prefetched one chunk ahead)
       if (wt < CT) {
         Gs[wt] = g_next;
         g_next = 0.f;
@@ -480,77 +545,32 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
       }
       named_sync(1, 128);
       if (warp == 0) chunk_cumsum(Gs, Gam, Dec, lane);
-      bool ok = wait_bar(&B->qk[st3], (c / 3) & 1, abort) && wait_bar(&B->vt, c & 1, abort);
-      if (ok && c >= 2) ok = wait_bar(&B->st[b], ((c >> 1) - 1) & 1, abort);   // U~^T buffer free
+      bool ok = wait_bar(&B->vt, c & 1, abort);
+      if (ok && c >= 2) ok = wait_bar(&B->st[b], ((c >> 1) - 1) & 1, abort) &&
+                              wait_bar(&B->of[b], ((c >> 1) - 1) & 1, abort);   // accumulator free
       if (named_sync_or(1, 128, !ok)) { fail = true; break; }
       tc_fence_after();
       if (wt == 0) {
-        mbar_arrive(&B->pv);                  // gates of chunk c are in shared memory
-        // D1 = [Q; K] K^T ; U~^T = V^T (T diag beta)^T ; W^T = K^T (T diag(beta gamma))^T
-        const uint32_t id1 = idesc_bf16(128, 64, false, false);
-        const uint64_t a1 = sdesc_sw128(sb + qk, 16, 1024), b1 = sdesc_sw128(sb + qk + 8192, 16, 1024);
-        for (int ks = 0; ks < DK / 16; ++ks) {
-          const uint32_t o = kstep_offset(true, ks, 16384) >> 4;
-          mma_bf16(tbase + TM_D1, a1 + o, b1 + o, id1, ks > 0);
-        }
-        const uint32_t id2 = idesc_bf16(128, 64, true, false);
-        const uint64_t av = sdesc_sw128(sb + K2_V, 8192, 1024), bt = sdesc_sw128(sb + K2_TB, 16, 1024);
-        const uint64_t ak = sdesc_sw128(sb + qk + 8192, 16384, 1024), bg = sdesc_sw128(sb + K2_TB + 8192, 16, 1024);
-        for (int ks = 0; ks < CT / 16; ++ks)
-          mma_bf16(tbase + TM_UT + b * 64, av + ks * (2048 >> 4), bt + ks * (32 >> 4), id2, ks > 0);
-        for (int ks = 0; ks < CT / 16; ++ks)
-          mma_bf16(tbase + TM_WT, ak + ks * (2048 >> 4), bg + ks * (32 >> 4), id2, ks > 0);
+        mbar_arrive(&B->pv);
+        // [U~^T | 0] = V^T [T diag(beta); 0]^T
+        const uint32_t id = idesc_bf16(128, 128, true, false);
+        const uint64_t av = sdesc_sw128(sb + K2_VT, 8192, 1024), bt = sdesc_sw128(sb + K2_VT + 16384, 16, 1024);
+        for (int ks = 0; ks < CT / 16; ++ks) mma_bf16(tbase + TM_ACC + b * 128, av + ks * 128, bt + ks * 2, id, ks > 0);
         mma_commit(&B->p);
       }
       ok = wait_bar(&B->p, c & 1, abort);
-      if (ok && c >= 2) ok = wait_bar(&B->gh[b], ((c >> 1) - 1) & 1, abort);   // P[b] free
+      if (ok && wt == 0 && c + 1 < n) { issue_vt(c + 1); issued_vt = c + 2; }
+      if (ok) ok = wait_bar(&B->sc, c & 1, abort);         // OUT scaled this chunk's Q and K
       if (named_sync_or(1, 128, !ok)) { fail = true; break; }
-      tc_fence_after();
-      if (wt == 0 && c + 1 < n) { issue_vt(c + 1); issued_vt = c + 2; }
-      {
-        float v[64];
-        tm_ld64(lane_base + TM_D1, v);          // warps 0, 1: rows r = wt of Q K^T
-        if (wt < CT) {
-          const int r = wt;
-          const float gr = Gs[r];
-#pragma unroll
-          for (int jb = 0; jb < 4; ++jb) {
-            if (jb * 16 <= r) {
-#pragma unroll
-              for (int j = jb * 16; j < jb * 16 + 16; ++j) v[j] = j <= r ? __expf(gr - Gs[j]) * v[j] : 0.f;
-            } else {
-#pragma unroll
-              for (int j = jb * 16; j < jb * 16 + 16; ++j) v[j] = 0.f;
-            }
-          }
-          st_row64(sm, K2_P + b * 8192, r, v);
-        }
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      ok = wait_bar(&B->sc, c & 1, abort);      // OUT scaled Q, K and wrote W
-      if (named_sync_or(1, 128, !ok)) { fail = true; break; }
-      if (wt == 0) {
-        mbar_arrive(&B->ready[b]);
-        // q/k tiles of chunk c + 2 go to the stage of chunk c - 1 once its last product ran
-        if (c + 2 < n) {
-          if (c < 1 || wait_bar(&B->gh[(c - 1) & 1], ((c - 1) >> 1) & 1, abort)) {
-            issue_qk(c + 2);
-            issued_qk = c + 3;
-          }
-        }
-      }
+      if (wt == 0) mbar_arrive(&B->ready[b]);
     }
     if (fail && wt == 0) {
-      // let the copies and products this warpgroup issued land before the exit
-      for (int k = max(c, 0); k < issued_qk; ++k) mbar_wait(&B->qk[k % 3], (k / 3) & 1, WAIT_LIMIT);
       for (int k = max(c, 0); k < issued_vt; ++k) mbar_wait(&B->vt, k & 1, WAIT_LIMIT);
       mbar_wait(&B->p, c & 1, WAIT_LIMIT);
     }
   } else if (wg == 1) {
     // ============================== STATE ==============================
     {
-      // initial state -> tensor memory (lane = dk, 128 columns = dv)
       const int dk = wt;
       const float* src = p.S0 ? p.S0 + (((size_t)s * p.Nv + h) * DK + dk) * DV : nullptr;
 #pragma unroll
@@ -568,9 +588,9 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
     bool fail = false;
     int c = 0;
     for (; c < n; ++c) {
-      const int st3 = c % 3, b = c & 1;
-      const uint32_t qk = K2_QK + st3 * 32768;
-      const float* Gam = reinterpret_cast<const float*>(sm + K2_VEC + st3 * 768) + CT;
+      const int b = c & 1;
+      const uint32_t st = K2_ST + b * STAGE_BYTES;
+      const float* Gam = reinterpret_cast<const float*>(sm + K2_VEC + (c % 3) * 768) + CT;
       bool ok = wait_bar(&B->ready[b], (c >> 1) & 1, abort);
       if (named_sync_or(2, 128, !ok)) { fail = true; break; }
       tc_fence_after();
@@ -590,20 +610,14 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
-      ok = c < 2 || wait_bar(&B->of[b], ((c >> 1) - 1) & 1, abort);    // O^T buffer free
-      if (named_sync_or(2, 128, !ok)) { fail = true; break; }
+      named_sync(2, 128);
       tc_fence_after();
       if (wt == 0) {
-        // U^T = U~^T - S^T W^T ;  O^T = S^T (diag(gamma) Q)^T
-        const uint32_t idf = idesc_bf16(128, 64, true, true, true);
-        const uint64_t as = sdesc_sw128(sb + K2_SMN, 16384, 1024), bw = sdesc_sw128(sb + K2_WMN, 16384, 1024);
+        // [U^T | O^T] += S^T [-W; diag(gamma) Q]^T
+        const uint32_t id = idesc_bf16(128, 128, true, false);
+        const uint64_t as = sdesc_sw128(sb + K2_SMN, 16384, 1024), bw = sdesc_sw128(sb + st, 16, 1024);
         for (int ks = 0; ks < DK / 16; ++ks)
-          mma_bf16(tbase + TM_UT + b * 64, as + ks * (2048 >> 4), bw + ks * (2048 >> 4), idf, 1u);
-        const uint32_t idq = idesc_bf16(128, 64, true, false);
-        const uint64_t bq = sdesc_sw128(sb + qk, 16, 1024);
-        for (int ks = 0; ks < DK / 16; ++ks)
-          mma_bf16(tbase + TM_OT + b * 64, as + ks * (2048 >> 4), bq + (kstep_offset(true, ks, 16384) >> 4), idq,
-                   ks > 0);
+          mma_bf16(tbase + TM_ACC + b * 128, as + ks * 128, bw + (kstep_offset(true, ks, 16384) >> 4), id, 1u);
         mma_commit(&B->fg);
       }
       ok = wait_bar(&B->fg, c & 1, abort);
@@ -611,7 +625,7 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
       tc_fence_after();
       {
         float v[64];
-        tm_ld64(lane_base + TM_UT + b * 64, v);   // lane dv holds U[0..63][dv]
+        tm_ld64(lane_base + TM_ACC + b * 128, v);   // lane dv holds U[0..63][dv]
         st_row64(sm, K2_UK, wt, v);
       }
       fence_proxy_async_smem();
@@ -624,11 +638,10 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
         const uint32_t idp = idesc_bf16(128, 64, false, false);
         const uint64_t au = sdesc_sw128(sb + K2_UK, 16, 1024), bp = sdesc_sw128(sb + K2_P + b * 8192, 16, 1024);
         for (int ks = 0; ks < CT / 16; ++ks)
-          mma_bf16(tbase + TM_OT + b * 64, au + ks * (32 >> 4), bp + ks * (32 >> 4), idp, 1u);
+          mma_bf16(tbase + TM_ACC + b * 128 + 64, au + ks * 2, bp + ks * 2, idp, 1u);
         const uint32_t ids = idesc_bf16(128, 128, true, false);
-        const uint64_t akt = sdesc_sw128(sb + qk + 8192, 16384, 1024);
-        for (int ks = 0; ks < CT / 16; ++ks)
-          mma_bf16(tbase + TM_S, akt + ks * (2048 >> 4), au + ks * (32 >> 4), ids, 1u);
+        const uint64_t ak = sdesc_sw128(sb + st + 32768, 8192, 1024);
+        for (int ks = 0; ks < CT / 16; ++ks) mma_bf16(tbase + TM_S, ak + ks * 128, au + ks * 2, ids, 1u);
         mma_commit(&B->gh[b]);
       }
       ok = wait_bar(&B->gh[b], (c >> 1) & 1, abort);
@@ -654,19 +667,25 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
     }
   } else {
     // ============================== OUT ==============================
-    // Per chunk: scale Q by gamma and K by exp(G_L - G) in place once PREP's
-    // products have read them raw, write W for STATE, then store the
-    // previous chunk's output rows.
+    // Per chunk: scale Q by gamma and K by exp(G_L - G) in place; then store
+    // the previous chunk's output rows and load the stage it freed.
     Tout* o = static_cast<Tout*>(p.o);
     const int dv = wt;
+    int issued = 0;
+    if (wt == 0 && n > 0) {
+      issue_stage(0);
+      if (n > 1) issue_stage(1);
+      issued = n > 1 ? 2 : 1;
+    }
     auto store_out = [&](int c) -> bool {
       const int b = c & 1;
       const int c0 = bos + c * CT, len = min(CT, eos - c0);
       const bool ok = wait_bar(&B->gh[b], (c >> 1) & 1, abort);
       if (named_sync_or(3, 128, !ok)) return false;
       tc_fence_after();
+      if (wt == 0 && c + 2 < n) { issue_stage(c + 2); issued = c + 3; }   // its stage is free now
       float v[64];
-      tm_ld64(lane_base + TM_OT + b * 64, v);   // lane dv holds O[0..63][dv]
+      tm_ld64(lane_base + TM_ACC + b * 128 + 64, v);   // lane dv holds O[0..63][dv]
       Tout* dst = o + ((size_t)c0 * p.Nv + h) * DV + dv;
 #pragma unroll
       for (int r = 0; r < CT; ++r)
@@ -677,31 +696,26 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
       return true;
     };
     bool alive = true;
-    for (int c = 0; c < n && alive; ++c) {
-      const int st3 = c % 3;
-      const uint32_t qk = K2_QK + st3 * 32768;
-      const float* Gam = reinterpret_cast<const float*>(sm + K2_VEC + st3 * 768) + CT;
+    int c = 0;
+    for (; c < n && alive; ++c) {
+      const int b = c & 1;
+      const uint32_t st = K2_ST + b * STAGE_BYTES;
+      const float* Gam = reinterpret_cast<const float*>(sm + K2_VEC + (c % 3) * 768) + CT;
       const float* Dec = Gam + CT;
-      bool ok = wait_bar(&B->pv, c & 1, abort) && wait_bar(&B->p, c & 1, abort);
-      if (ok && c >= 1) ok = wait_bar(&B->fg, (c - 1) & 1, abort);   // W buffer free
-      if (named_sync_or(3, 128, !ok)) break;
-      tc_fence_after();
-      scale_box(sm, qk, Gam, wt, 128);
-      scale_box(sm, qk + 16384, Gam, wt, 128);
-      scale_box(sm, qk + 8192, Dec, wt, 128);
-      scale_box(sm, qk + 24576, Dec, wt, 128);
-      {
-        float v[64];
-        tm_ld64(lane_base + TM_WT, v);          // lane dk holds W[0..63][dk]
-        st_row64(sm, K2_WMN, wt, v);
-      }
+      const bool ok = wait_bar(&B->stl[b], (c >> 1) & 1, abort) && wait_bar(&B->pv, c & 1, abort);
+      if (named_sync_or(3, 128, !ok)) { alive = false; break; }
+      scale_box(sm, st + 8192, Gam, wt, 128);
+      scale_box(sm, st + 24576, Gam, wt, 128);
+      scale_box(sm, st + 32768, Dec, wt, 128);
+      scale_box(sm, st + 40960, Dec, wt, 128);
       fence_proxy_async_smem();
-      tc_fence_before();
       named_sync(3, 128);
       if (wt == 0) mbar_arrive(&B->sc);
       if (c >= 1) alive = store_out(c - 1);
     }
-    if (alive && n > 0) store_out(n - 1);
+    if (alive && n > 0) alive = store_out(n - 1);
+    if (!alive && wt == 0)
+      for (int k = max(c, 0); k < issued; ++k) mbar_wait(&B->stl[k & 1], (k >> 1) & 1, WAIT_LIMIT);
   }
 
   if (*abort && tid == 0) raise_error(p.err, kDevErrTimeout);
@@ -757,7 +771,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs& p, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const int slots = p.total / CT + p.num_seqs;
   dim3 g1(slots, p.Nv);
-  chunk_solve_kernel<<<g1, 128, S1_SMEM, s>>>(mk, p);
+  chunk_solve_kernel<<<g1, 128, S1_SMEM, s>>>(mq, mk, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return p.out_bf16 ? launch_scan<bf16>(mq, mk, mv, p, s) : launch_scan<float>(mq, mk, mv, p, s);
