@@ -49,7 +49,12 @@ constexpr int DK = 128;
 constexpr int DV = 128;
 constexpr uint32_t WAIT_LIMIT = 1u << 22;
 constexpr int FS = 68;        // fp32 matrix row stride (16-byte aligned rows)
-constexpr uint32_t TILE_T_BYTES = 32768;   // workspace per (chunk, value head): 4 bf16 tiles
+// workspace per (chunk, value head), written by the solve kernel:
+//   [-W dk0-63 | Q~ dk0-63 | -W dk64-127 | Q~ dk64-127]  the N = 128 operand of the S products
+//   P, then dec = exp(G_L - G) (64 floats) and gamma_L, then T diag(beta)
+// (bf16 tiles in the 128-byte-swizzled layout a TMA load would give).
+constexpr uint32_t WS_QW = 0, WS_P = 32768, WS_VEC = 40960, WS_TB = 41472;
+constexpr uint32_t TILE_T_BYTES = 49664;
 
 // ---------------------------------------------------------------------------
 // shared helpers
@@ -225,11 +230,9 @@ constexpr uint32_t S1_QK = 0;                       // K box0 | Q box0 | K box1 
 constexpr uint32_t S1_TBG = 32768;                  // T diag(beta gamma) | zeros (16 KB)
 constexpr uint32_t S1_AF = 49152;                   // A fp32 [64][FS]
 constexpr uint32_t S1_TF = S1_AF + 64 * FS * 4;     // T fp32 [64][FS]
-constexpr uint32_t S1_VEC = S1_TF + 64 * FS * 4;    // G, beta, beta*gamma (3 x 64 floats)
-constexpr uint32_t S1_BAR = S1_VEC + 3 * 64 * 4;
+constexpr uint32_t S1_VEC = S1_TF + 64 * FS * 4;    // G, beta, beta*gamma, gamma, dec (5 x 64 floats)
+constexpr uint32_t S1_BAR = S1_VEC + 5 * 64 * 4;
 constexpr uint32_t S1_SMEM = S1_BAR + 64 + 1024;
-// workspace slot: [T diag(beta) | P | -W dk 0-63 | -W dk 64-127], 8 KB each
-constexpr uint32_t WS_TB = 0, WS_P = 8192, WS_W = 16384;
 
 // Write 64 bf16 values as swizzled row `row` of a 64-column block in global memory.
 __device__ __forceinline__ void st_row64_global(uint8_t* dst, uint32_t row, const float* v, float sc) {
@@ -256,6 +259,8 @@ chunk_solve_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
   float* Gs = reinterpret_cast<float*>(sm + S1_VEC);
   float* Bet = Gs + CT;
   float* BG = Bet + CT;
+  float* Gam = BG + CT;
+  float* Dec = Gam + CT;
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + S1_BAR);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S1_BAR + 16);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -298,8 +303,6 @@ chunk_solve_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
   const uint32_t lane_base = tbase + ((uint32_t)(warp * 32) << 16);
   const uint32_t sb = smem_u32(sm);
   if (warp == 0) {
-    float* Gam = TF;            // scratch for the cumsum helper (TF is rewritten later)
-    float* Dec = TF + 64;
     chunk_cumsum(Gs, Gam, Dec, lane);
     BG[lane] = Bet[lane] * Gam[lane];
     BG[lane + 32] = Bet[lane + 32] * Gam[lane + 32];
@@ -350,6 +353,23 @@ chunk_solve_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
         st_row64_global(ws + WS_P, r, v, 1.f);
       }
     }
+    // diag(gamma) Q -> rows 64-127 of the two [-W; Q~] blocks (same swizzled rows as
+    // the TMA tiles), then dec and gamma_L
+    for (int i = tid; i < 1024; i += 128) {
+      const uint32_t off = (uint32_t)(i >> 9) * 16384u + (uint32_t)(i & 511) * 16u;
+      const float f = Gam[(i & 511) >> 3];
+      uint4 u = *reinterpret_cast<const uint4*>(sm + S1_QK + 8192 + off);
+      uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 x = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w[j]));
+        __nv_bfloat162 y = __floats2bfloat162_rn(x.x * f, x.y * f);
+        w[j] = *reinterpret_cast<uint32_t*>(&y);
+      }
+      *reinterpret_cast<uint4*>(ws + WS_QW + 8192 + off) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    if (tid < CT) reinterpret_cast<float*>(ws + WS_VEC)[tid] = Dec[tid];
+    if (tid == 0) reinterpret_cast<float*>(ws + WS_VEC)[CT] = Gam[CT - 1];
     tc_fence_before();
     __syncthreads();
     invert_unit_lower(AF, TF, tid);
@@ -390,7 +410,7 @@ chunk_solve_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
       for (int half = 0; half < 2; ++half) {
         float v[64];
         tm_ld64(lane_base + 64 + half * 64, v);
-        if (tid < CT) st_row64_global(ws + WS_W + half * 8192, tid, v, -1.f);
+        if (tid < CT) st_row64_global(ws + WS_QW + half * 16384, tid, v, -1.f);
       }
     } else if (tid == 0) {
       raise_error(p.err, kDevErrTimeout);
@@ -404,39 +424,48 @@ chunk_solve_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
 }
 
 // ---------------------------------------------------------------------------
-// kernel 2: the scan over chunks, three warpgroups
+// kernel 2: the scan over chunks
+//   warp 0     PREP   loads v and T diag(beta), [U~^T | 0] = V^T [T diag(beta); 0]^T
+//   warps 1-4  STATE  the S-dependent products and their epilogues
+//   warps 5-8  OUT    loads each chunk's stage, stores the output rows
+// The state lives in tensor memory transposed (lane dv, column dk, fp32).
+// Per chunk, STATE writes S^T and U^T back into tensor memory as bf16 and
+// every S-dependent product reads its A operand from there:
+//   [U^T | O^T] += S^T [-W; Q~]^T          (N = 128, K = Dk)
+//   S^T = gamma_L S^T + (U^T diag(dec)) K  (N = 128, K = 64)
+//   O^T += U^T P^T                         (N = 64,  K = 64)
 // ---------------------------------------------------------------------------
-constexpr int NT2 = 384;
-constexpr uint32_t K2_ST = 0;          // 2 stages x [-W dk0-63 | Q box0 | -W dk64-127 | Q box1 | K box0 | K box1]
-constexpr uint32_t STAGE_BYTES = 49152;
-constexpr uint32_t K2_P = 98304;       // 2 x P [r][j] (8 KB)
-constexpr uint32_t K2_VT = 114688;     // V box0 | V box1 | T diag(beta) | zeros (32 KB)
-constexpr uint32_t K2_UK = 147456;     // U^T as [dv rows][j] (16 KB)
-constexpr uint32_t K2_SMN = 163840;    // S as [dk rows][dv], two 64-column blocks (32 KB)
-constexpr uint32_t K2_VEC = 196608;    // 3 x (G, gamma, dec) (768 B each)
-constexpr uint32_t K2_BAR = K2_VEC + 3 * 768;
+constexpr int NT2 = 288;
+constexpr uint32_t STAGE_BYTES = 58368;     // [-W | Q~] 32 KB | K box0 | K box1 | P | dec, gamma_L
+constexpr uint32_t SG_K = 32768, SG_P = 49152, SG_VEC = 57344;
+constexpr uint32_t K2_ST = 0;                          // 2 stages
+constexpr uint32_t K2_VT = 2 * STAGE_BYTES;            // 2 x [V box0 | V box1 | T diag(beta) | zeros]
+constexpr uint32_t K2_OS = K2_VT + 2 * 32768;          // 2 x output tile (two 64 x 64 boxes)
+constexpr uint32_t K2_BAR = K2_OS + 2 * 16384;
 constexpr uint32_t K2_SMEM = K2_BAR + 256 + 1024;
 static_assert(K2_SMEM <= 232448, "shared memory budget");
+static_assert(SG_VEC + 512 <= STAGE_BYTES && WS_VEC == WS_P + 8192 && SG_VEC == SG_P + 8192, "stage layout");
 
-// tensor memory: two accumulators of [U^T (64 columns) | O^T (64 columns)], then S
-constexpr uint32_t TM_ACC = 0, TM_S = 256;
+// tensor memory columns
+constexpr uint32_t TM_ACC = 0;     // 2 x [U^T (64) | O^T (64)], fp32
+constexpr uint32_t TM_S = 256;     // S^T, fp32 (128)
+constexpr uint32_t TM_SB = 384;    // S^T as bf16 pairs (64)
+constexpr uint32_t TM_UD = 448;    // U^T diag(dec) as bf16 pairs (32)
+constexpr uint32_t TM_UB = 480;    // U^T as bf16 pairs (32)
 
 struct ScanBars {
-  uint64_t stl[2];  // stage tiles of a chunk landed (q, k, -W, P)
-  uint64_t vt;      // v and T diag(beta) tiles landed
-  uint64_t p;       // PREP product done
-  uint64_t pv;      // PREP gates of a chunk written (G, gamma, dec)
-  uint64_t sc;      // OUT scaled Q and K of a chunk in place
-  uint64_t ready[2];// a chunk is ready for STATE
-  uint64_t fg;      // [U^T | O^T] += S^T [-W; Q~]^T done
-  uint64_t gh[2];   // O^T += U^T P^T and the state update done
-  uint64_t st[2];   // U^T of a chunk read out of tensor memory
-  uint64_t of[2];   // O^T of a chunk stored
+  uint64_t stl[2];   // stage of a chunk landed ([-W | Q~], K, P, dec)
+  uint64_t vt[2];    // v tiles and T diag(beta) of a chunk landed
+  uint64_t ready[2]; // [U~^T | 0] of a chunk in its accumulator (MMA commit)
+  uint64_t ob[2];    // O^T of a chunk complete (MMA commit)
+  uint64_t of[2];    // OUT finished reading a chunk's accumulator
+  uint64_t fg;       // [U^T | O^T] += S^T [-W; Q~]^T complete
+  uint64_t gh;       // state update complete
   uint32_t tslot;
   int abort;
 };
 
-// Bounded wait that also gives up when another warpgroup aborted.
+// Bounded wait that also gives up when another role aborted.
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort) {
   for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -446,10 +475,15 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
   return false;
 }
 
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 h2 = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h2);
+}
+
 template <typename Tout>
 __global__ void __launch_bounds__(NT2, 1)
-chunk_scan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                  const __grid_constant__ CUtensorMap tmv, ChunkArgs p) {
+chunk_scan_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                  const __grid_constant__ CUtensorMap tmo, ChunkArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   ScanBars* B = reinterpret_cast<ScanBars*>(sm + K2_BAR);
@@ -457,8 +491,7 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int wg = warp >> 2;                   // 0 PREP, 1 STATE, 2 OUT
-  const int wt = tid & 127;                   // thread index in the warpgroup = its tensor-memory lane
+  const int dv = (warp & 3) * 32 + lane;        // this thread's tensor-memory lane
   const int h = blockIdx.x, s = blockIdx.y;
   const int hk = h / (p.Nv / p.Nk);
   int bos, eos;
@@ -474,25 +507,24 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&B->stl[i], 1);
+      mbar_init(&B->vt[i], 1);
       mbar_init(&B->ready[i], 1);
-      mbar_init(&B->gh[i], 1);
-      mbar_init(&B->st[i], 1);
+      mbar_init(&B->ob[i], 1);
       mbar_init(&B->of[i], 1);
     }
-    mbar_init(&B->vt, 1);
-    mbar_init(&B->p, 1);
-    mbar_init(&B->pv, 1);
-    mbar_init(&B->sc, 1);
     mbar_init(&B->fg, 1);
+    mbar_init(&B->gh, 1);
     B->abort = 0;
     fence_barrier_init();
-    prefetch_tmap(&tmq);
     prefetch_tmap(&tmk);
     prefetch_tmap(&tmv);
+    prefetch_tmap(&tmo);
   }
   if (warp == 0) tmem_alloc(&B->tslot, 512);
-  for (int i = tid * 16; i < 8192; i += NT2 * 16)      // rows 64-127 of the [T diag(beta); 0] operand
-    *reinterpret_cast<uint4*>(sm + K2_VT + 24576 + i) = make_uint4(0u, 0u, 0u, 0u);
+  for (int i = tid * 16; i < 2 * 8192; i += NT2 * 16) {   // rows 64-127 of both [T diag(beta); 0] operands
+    const uint32_t off = K2_VT + (uint32_t)(i >> 13) * 32768u + 24576u + (uint32_t)(i & 8191);
+    *reinterpret_cast<uint4*>(sm + off) = make_uint4(0u, 0u, 0u, 0u);
+  }
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
@@ -501,221 +533,228 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant
   const uint32_t lane_base = tbase + ((uint32_t)((warp & 3) * 32) << 16);
   const uint32_t sb = smem_u32(sm);
 
-  // stage loads of chunk c: q, k tiles (TMA), -W and P (bulk copies from the workspace)
-  auto issue_stage = [&](int c) {
-    const int t = bos + c * CT;
-    const uint32_t st = K2_ST + (c & 1) * STAGE_BYTES;
-    uint64_t* bar = &B->stl[c & 1];
-    mbar_arrive_expect_tx(bar, 4 * 8192 + 3 * 8192);
-    tma_load_2d(sm + st + 8192, &tmq, bar, hk * DK, t);
-    tma_load_2d(sm + st + 24576, &tmq, bar, hk * DK + 64, t);
-    tma_load_2d(sm + st + 32768, &tmk, bar, hk * DK, t);
-    tma_load_2d(sm + st + 40960, &tmk, bar, hk * DK + 64, t);
-    const uint8_t* src = ws_tile(c);
-    bulk_load(sm + st, src + WS_W, 8192, bar);
-    bulk_load(sm + st + 16384, src + WS_W + 8192, 8192, bar);
-    bulk_load(sm + K2_P + (c & 1) * 8192, src + WS_P, 8192, bar);
-  };
-  auto issue_vt = [&](int c) {
-    const int t = bos + c * CT;
-    mbar_arrive_expect_tx(&B->vt, 2 * 8192 + 8192);
-    tma_load_2d(sm + K2_VT, &tmv, &B->vt, h * DV, t);
-    tma_load_2d(sm + K2_VT + 8192, &tmv, &B->vt, h * DV + 64, t);
-    bulk_load(sm + K2_VT + 16384, ws_tile(c) + WS_TB, 8192, &B->vt);
-  };
-
-  if (wg == 0) {
+  if (warp == 0) {
     // ============================== PREP ==============================
-    int issued_vt = 0;
-    if (wt == 0 && n > 0) { issue_vt(0); issued_vt = 1; }
-    float g_next = 0.f;
-    if (wt < CT && n > 0 && wt < eos - bos) g_next = p.g[(size_t)(bos + wt) * p.Nv + h];
-    int c = 0;
-    bool fail = false;
-    for (; c < n; ++c) {
-      const int b = c & 1;
-      float* Gs = reinterpret_cast<float*>(sm + K2_VEC + (c % 3) * 768);
-      float* Gam = Gs + CT;
-      float* Dec = Gam + CT;
-      const int c0 = bos + c * CT;
-      if (wt < CT) {
-        Gs[wt] = g_next;
-        g_next = 0.f;
-        if (c + 1 < n && c0 + CT + wt < eos) g_next = p.g[(size_t)(c0 + CT + wt) * p.Nv + h];
-      }
-      named_sync(1, 128);
-      if (warp == 0) chunk_cumsum(Gs, Gam, Dec, lane);
-      bool ok = wait_bar(&B->vt, c & 1, abort);
-      if (ok && c >= 2) ok = wait_bar(&B->st[b], ((c >> 1) - 1) & 1, abort) &&
-                              wait_bar(&B->of[b], ((c >> 1) - 1) & 1, abort);   // accumulator free
-      if (named_sync_or(1, 128, !ok)) { fail = true; break; }
-      tc_fence_after();
-      if (wt == 0) {
-        mbar_arrive(&B->pv);
-        // [U~^T | 0] = V^T [T diag(beta); 0]^T
+    if (lane == 0) {
+      auto issue_vt = [&](int c) {
+        const int t = bos + c * CT;
+        const uint32_t vt = K2_VT + (uint32_t)(c & 1) * 32768u;
+        uint64_t* bar = &B->vt[c & 1];
+        mbar_arrive_expect_tx(bar, 2 * 8192 + 8192);
+        tma_load_2d(sm + vt, &tmv, bar, h * DV, t);
+        tma_load_2d(sm + vt + 8192, &tmv, bar, h * DV + 64, t);
+        bulk_load(sm + vt + 16384, ws_tile(c) + WS_TB, 8192, bar);
+      };
+      int issued = 0, committed = 0, c = 0;
+      for (; issued < n && issued < 2; ++issued) issue_vt(issued);
+      bool ok = true;
+      for (; c < n; ++c) {
+        const int b = c & 1;
+        ok = wait_bar(&B->vt[b], (c >> 1) & 1, abort);
+        if (ok && c >= 2) ok = wait_bar(&B->of[b], ((c >> 1) - 1) & 1, abort);   // accumulator b free
+        if (!ok) break;
+        tc_fence_after();
+        // [U~^T | 0] = V^T [T diag(beta); 0]^T: A = V tiles read MN-major, B = [T diag(beta); 0]
+        const uint32_t vt = K2_VT + (uint32_t)b * 32768u;
         const uint32_t id = idesc_bf16(128, 128, true, false);
-        const uint64_t av = sdesc_sw128(sb + K2_VT, 8192, 1024), bt = sdesc_sw128(sb + K2_VT + 16384, 16, 1024);
-        for (int ks = 0; ks < CT / 16; ++ks) mma_bf16(tbase + TM_ACC + b * 128, av + ks * 128, bt + ks * 2, id, ks > 0);
-        mma_commit(&B->p);
-      }
-      ok = wait_bar(&B->p, c & 1, abort);
-      if (ok && wt == 0 && c + 1 < n) { issue_vt(c + 1); issued_vt = c + 2; }
-      if (ok) ok = wait_bar(&B->sc, c & 1, abort);         // OUT scaled this chunk's Q and K
-      if (named_sync_or(1, 128, !ok)) { fail = true; break; }
-      if (wt == 0) mbar_arrive(&B->ready[b]);
-    }
-    if (fail && wt == 0) {
-      for (int k = max(c, 0); k < issued_vt; ++k) mbar_wait(&B->vt, k & 1, WAIT_LIMIT);
-      mbar_wait(&B->p, c & 1, WAIT_LIMIT);
-    }
-  } else if (wg == 1) {
-    // ============================== STATE ==============================
-    {
-      const int dk = wt;
-      const float* src = p.S0 ? p.S0 + (((size_t)s * p.Nv + h) * DK + dk) * DV : nullptr;
+        const uint64_t av = sdesc_sw128(sb + vt, 8192, 1024), bt = sdesc_sw128(sb + vt + 16384, 16, 1024);
 #pragma unroll
-      for (int c0 = 0; c0 < DV; c0 += 32) {
+        for (int ks = 0; ks < CT / 16; ++ks)
+          mma_bf16(tbase + TM_ACC + b * 128, av + ks * 128, bt + ks * 2, id, ks > 0 ? 1u : 0u);
+        mma_commit(&B->ready[b]);
+        committed = c + 1;
+        if (c + 2 < n) {
+          ok = wait_bar(&B->ready[b], (c >> 1) & 1, abort);                    // tiles b consumed
+          if (!ok) break;
+          issue_vt(c + 2);
+          issued = c + 3;
+        }
+      }
+      if (!ok) {
+        for (int k = c; k < issued; ++k) mbar_wait(&B->vt[k & 1], (k >> 1) & 1, WAIT_LIMIT);
+        if (committed > 0) mbar_wait(&B->ready[(committed - 1) & 1], ((committed - 1) >> 1) & 1, WAIT_LIMIT);
+      }
+    }
+  } else if (warp <= 4) {
+    // ============================== STATE ==============================
+    const bool leader = tid == 32;
+    {
+      // S^T <- initial state (S0 is [dk][dv]: thread dv reads a column)
+      const float* src = p.S0 ? p.S0 + ((size_t)s * p.Nv + h) * DK * DV + dv : nullptr;
+#pragma unroll
+      for (int c0 = 0; c0 < DK; c0 += 32) {
         float v[32];
 #pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          float4 t4 = src ? *reinterpret_cast<const float4*>(src + c0 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-          v[i] = t4.x; v[i + 1] = t4.y; v[i + 2] = t4.z; v[i + 3] = t4.w;
-        }
+        for (int i = 0; i < 32; ++i) v[i] = src ? __ldg(src + (size_t)(c0 + i) * DV) : 0.f;
         tmem_st32(lane_base + TM_S + c0, v);
       }
       tmem_st_wait();
     }
+    int fg_issued = 0, gh_issued = 0;
     bool fail = false;
     int c = 0;
     for (; c < n; ++c) {
       const int b = c & 1;
-      const uint32_t st = K2_ST + b * STAGE_BYTES;
-      const float* Gam = reinterpret_cast<const float*>(sm + K2_VEC + (c % 3) * 768) + CT;
-      bool ok = wait_bar(&B->ready[b], (c >> 1) & 1, abort);
+      const uint32_t st = K2_ST + (uint32_t)b * STAGE_BYTES;
+      const float* vec = reinterpret_cast<const float*>(sm + st + SG_VEC);   // dec[0..63], gamma_L
+      bool ok = wait_bar(&B->stl[b], (c >> 1) & 1, abort) && wait_bar(&B->ready[b], (c >> 1) & 1, abort);
       if (named_sync_or(2, 128, !ok)) { fail = true; break; }
       tc_fence_after();
-      const float gamma_L = Gam[CT - 1];
-      // bf16 S -> shared memory (operand), gamma_L S -> tensor memory (accumulator)
+      // E_S: bf16 copy of S^T (the A operand), then S^T <- gamma_L S^T in place
+      const float gl = vec[CT];
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        float v[64];
-        tm_ld64(lane_base + TM_S + half * 64, v);
-        st_row64(sm, K2_SMN + half * 16384, wt, v);
-        float a[32], bb[32];
+        float x[32], y[32], pk[32];
+        tmem_ld32(lane_base + TM_S + half * 64, x);
+        tmem_ld32(lane_base + TM_S + half * 64 + 32, y);
+        tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) { a[i] = v[i] * gamma_L; bb[i] = v[32 + i] * gamma_L; }
-        tmem_st32(lane_base + TM_S + half * 64, a);
-        tmem_st32(lane_base + TM_S + half * 64 + 32, bb);
+        for (int i = 0; i < 16; ++i) {
+          pk[i] = __uint_as_float(pack_bf16(x[2 * i], x[2 * i + 1]));
+          pk[16 + i] = __uint_as_float(pack_bf16(y[2 * i], y[2 * i + 1]));
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) { x[i] *= gl; y[i] *= gl; }
+        tmem_st32(lane_base + TM_SB + half * 32, pk);
+        tmem_st32(lane_base + TM_S + half * 64, x);
+        tmem_st32(lane_base + TM_S + half * 64 + 32, y);
       }
       tmem_st_wait();
-      fence_proxy_async_smem();
       tc_fence_before();
       named_sync(2, 128);
-      tc_fence_after();
-      if (wt == 0) {
-        // [U^T | O^T] += S^T [-W; diag(gamma) Q]^T
-        const uint32_t id = idesc_bf16(128, 128, true, false);
-        const uint64_t as = sdesc_sw128(sb + K2_SMN, 16384, 1024), bw = sdesc_sw128(sb + st, 16, 1024);
+      if (leader) {
+        tc_fence_after();
+        // [U^T | O^T] += S^T [-W; Q~]^T
+        const uint32_t id = idesc_bf16(128, 128, false, false);
+        const uint64_t bq = sdesc_sw128(sb + st, 16, 1024);
+#pragma unroll
         for (int ks = 0; ks < DK / 16; ++ks)
-          mma_bf16(tbase + TM_ACC + b * 128, as + ks * 128, bw + (kstep_offset(true, ks, 16384) >> 4), id, 1u);
+          mma_bf16_ta(tbase + TM_ACC + b * 128, tbase + TM_SB + ks * 8, bq + (ks >> 2) * 1024 + (ks & 3) * 2, id, 1u);
         mma_commit(&B->fg);
+        fg_issued = c + 1;
       }
       ok = wait_bar(&B->fg, c & 1, abort);
       if (named_sync_or(2, 128, !ok)) { fail = true; break; }
       tc_fence_after();
+      // E_U: U^T and U^T diag(dec) as bf16 pairs
       {
-        float v[64];
-        tm_ld64(lane_base + TM_ACC + b * 128, v);   // lane dv holds U[0..63][dv]
-        st_row64(sm, K2_UK, wt, v);
+        float u[64], pu[32], pd[32];
+        tm_ld64(lane_base + TM_ACC + b * 128, u);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          pu[i] = __uint_as_float(pack_bf16(u[2 * i], u[2 * i + 1]));
+          pd[i] = __uint_as_float(pack_bf16(u[2 * i] * vec[2 * i], u[2 * i + 1] * vec[2 * i + 1]));
+        }
+        tmem_st32(lane_base + TM_UB, pu);
+        tmem_st32(lane_base + TM_UD, pd);
       }
-      fence_proxy_async_smem();
+      tmem_st_wait();
       tc_fence_before();
       named_sync(2, 128);
-      tc_fence_after();
-      if (wt == 0) {
-        mbar_arrive(&B->st[b]);
-        // O^T += U^T P^T ;  S += (diag(exp(G_L - G)) K)^T U
+      if (leader) {
+        tc_fence_after();
+        // S^T += (U^T diag(dec)) K: B = K tiles read MN-major
+        const uint32_t idh = idesc_bf16(128, 128, false, true);
+        const uint64_t bk = sdesc_sw128(sb + st + SG_K, 8192, 1024);
+#pragma unroll
+        for (int ks = 0; ks < CT / 16; ++ks) mma_bf16_ta(tbase + TM_S, tbase + TM_UD + ks * 8, bk + ks * 128, idh, 1u);
+        mma_commit(&B->gh);
+        // O^T += U^T P^T
         const uint32_t idp = idesc_bf16(128, 64, false, false);
-        const uint64_t au = sdesc_sw128(sb + K2_UK, 16, 1024), bp = sdesc_sw128(sb + K2_P + b * 8192, 16, 1024);
+        const uint64_t bp = sdesc_sw128(sb + st + SG_P, 16, 1024);
+#pragma unroll
         for (int ks = 0; ks < CT / 16; ++ks)
-          mma_bf16(tbase + TM_ACC + b * 128 + 64, au + ks * 2, bp + ks * 2, idp, 1u);
-        const uint32_t ids = idesc_bf16(128, 128, true, false);
-        const uint64_t ak = sdesc_sw128(sb + st + 32768, 8192, 1024);
-        for (int ks = 0; ks < CT / 16; ++ks) mma_bf16(tbase + TM_S, ak + ks * 128, au + ks * 2, ids, 1u);
-        mma_commit(&B->gh[b]);
+          mma_bf16_ta(tbase + TM_ACC + b * 128 + 64, tbase + TM_UB + ks * 8, bp + ks * 2, idp, 1u);
+        mma_commit(&B->ob[b]);
+        gh_issued = c + 1;
       }
-      ok = wait_bar(&B->gh[b], (c >> 1) & 1, abort);
+      ok = wait_bar(&B->gh, c & 1, abort);
       if (named_sync_or(2, 128, !ok)) { fail = true; break; }
       tc_fence_after();
     }
     if (fail) {
-      if (wt == 0) {
-        mbar_wait(&B->fg, c & 1, WAIT_LIMIT);
-        mbar_wait(&B->gh[c & 1], (c >> 1) & 1, WAIT_LIMIT);
+      if (leader) {
+        if (fg_issued > 0) mbar_wait(&B->fg, (fg_issued - 1) & 1, WAIT_LIMIT);
+        if (gh_issued > 0) {
+          const int k = gh_issued - 1;
+          mbar_wait(&B->gh, k & 1, WAIT_LIMIT);
+          mbar_wait(&B->ob[k & 1], (k >> 1) & 1, WAIT_LIMIT);
+        }
       }
     } else if (p.ST) {
-      const int dk = wt;
-      float* dst = p.ST + (((size_t)s * p.Nv + h) * DK + dk) * DV;
+      float* dst = p.ST + ((size_t)s * p.Nv + h) * DK * DV + dv;
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        float v[64];
-        tm_ld64(lane_base + TM_S + half * 64, v);
+      for (int c0 = 0; c0 < DK; c0 += 32) {
+        float v[32];
+        tmem_ld32(lane_base + TM_S + c0, v);
+        tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 64; i += 4)
-          *reinterpret_cast<float4*>(dst + half * 64 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+        for (int i = 0; i < 32; ++i) dst[(size_t)(c0 + i) * DV] = v[i];
       }
     }
   } else {
     // ============================== OUT ==============================
-    // Per chunk: scale Q by gamma and K by exp(G_L - G) in place; then store
-    // the previous chunk's output rows and load the stage it freed.
+    const bool leader = tid == 160;
     Tout* o = static_cast<Tout*>(p.o);
-    const int dv = wt;
+    constexpr bool kBf16Out = sizeof(Tout) == 2;
+    auto issue_stage = [&](int c) {
+      const int t = bos + c * CT;
+      const uint32_t st = K2_ST + (uint32_t)(c & 1) * STAGE_BYTES;
+      uint64_t* bar = &B->stl[c & 1];
+      const uint8_t* src = ws_tile(c);
+      mbar_arrive_expect_tx(bar, 32768 + 8192 + 512 + 2 * 8192);
+      bulk_load(sm + st, src + WS_QW, 32768, bar);
+      bulk_load(sm + st + SG_P, src + WS_P, 8192 + 512, bar);
+      tma_load_2d(sm + st + SG_K, &tmk, bar, hk * DK, t);
+      tma_load_2d(sm + st + SG_K + 8192, &tmk, bar, hk * DK + 64, t);
+    };
     int issued = 0;
-    if (wt == 0 && n > 0) {
-      issue_stage(0);
-      if (n > 1) issue_stage(1);
-      issued = n > 1 ? 2 : 1;
-    }
-    auto store_out = [&](int c) -> bool {
+    if (leader)
+      for (; issued < n && issued < 2; ++issued) issue_stage(issued);
+    bool fail = false;
+    int c = 0;
+    for (; c < n; ++c) {
       const int b = c & 1;
       const int c0 = bos + c * CT, len = min(CT, eos - c0);
-      const bool ok = wait_bar(&B->gh[b], (c >> 1) & 1, abort);
-      if (named_sync_or(3, 128, !ok)) return false;
+      const bool ok = wait_bar(&B->ob[b], (c >> 1) & 1, abort);
+      if (named_sync_or(3, 128, !ok)) { fail = true; break; }
       tc_fence_after();
-      if (wt == 0 && c + 2 < n) { issue_stage(c + 2); issued = c + 3; }   // its stage is free now
+      if (leader && c + 2 < n) { issue_stage(c + 2); issued = c + 3; }   // stage b is free now
       float v[64];
       tm_ld64(lane_base + TM_ACC + b * 128 + 64, v);   // lane dv holds O[0..63][dv]
-      Tout* dst = o + ((size_t)c0 * p.Nv + h) * DV + dv;
-#pragma unroll
-      for (int r = 0; r < CT; ++r)
-        if (r < len) dst[(size_t)r * p.Nv * DV] = from_f32<Tout>(p.scale * v[r]);
+      const bool use_tma = kBf16Out && len == CT;
+      if (use_tma && leader) bulk_wait_read<1>();     // the store of chunk c - 2 has left buffer b
       tc_fence_before();
       named_sync(3, 128);
-      if (wt == 0) mbar_arrive(&B->of[b]);
-      return true;
-    };
-    bool alive = true;
-    int c = 0;
-    for (; c < n && alive; ++c) {
-      const int b = c & 1;
-      const uint32_t st = K2_ST + b * STAGE_BYTES;
-      const float* Gam = reinterpret_cast<const float*>(sm + K2_VEC + (c % 3) * 768) + CT;
-      const float* Dec = Gam + CT;
-      const bool ok = wait_bar(&B->stl[b], (c >> 1) & 1, abort) && wait_bar(&B->pv, c & 1, abort);
-      if (named_sync_or(3, 128, !ok)) { alive = false; break; }
-      scale_box(sm, st + 8192, Gam, wt, 128);
-      scale_box(sm, st + 24576, Gam, wt, 128);
-      scale_box(sm, st + 32768, Dec, wt, 128);
-      scale_box(sm, st + 40960, Dec, wt, 128);
-      fence_proxy_async_smem();
-      named_sync(3, 128);
-      if (wt == 0) mbar_arrive(&B->sc);
-      if (c >= 1) alive = store_out(c - 1);
+      if (leader) mbar_arrive(&B->of[b]);
+      if (use_tma) {
+        uint8_t* os = sm + K2_OS + (uint32_t)b * 16384u;
+        uint8_t* box = os + (dv >> 6) * 8192;
+        const uint32_t e = (uint32_t)(dv & 63);
+#pragma unroll
+        for (int r = 0; r < CT; ++r) {
+          const uint32_t off = (uint32_t)r * 128u + ((((e >> 3) ^ (uint32_t)r) & 7u) << 4) + (e & 7u) * 2u;
+          *reinterpret_cast<bf16*>(box + off) = __float2bfloat16_rn(p.scale * v[r]);
+        }
+        fence_proxy_async_smem();
+        named_sync(3, 128);
+        if (leader) {
+          tma_store_2d(&tmo, os, h * DV, c0);
+          tma_store_2d(&tmo, os + 8192, h * DV + 64, c0);
+          bulk_commit_group();
+        }
+      } else {
+        Tout* dst = o + ((size_t)c0 * p.Nv + h) * DV + dv;
+#pragma unroll
+        for (int r = 0; r < CT; ++r)
+          if (r < len) dst[(size_t)r * p.Nv * DV] = from_f32<Tout>(p.scale * v[r]);
+      }
     }
-    if (alive && n > 0) alive = store_out(n - 1);
-    if (!alive && wt == 0)
-      for (int k = max(c, 0); k < issued; ++k) mbar_wait(&B->stl[k & 1], (k >> 1) & 1, WAIT_LIMIT);
+    if (leader) {
+      if (fail)
+        for (int k = c; k < issued; ++k) mbar_wait(&B->stl[k & 1], (k >> 1) & 1, WAIT_LIMIT);
+      bulk_wait_all();
+    }
   }
 
   if (*abort && tid == 0) raise_error(p.err, kDevErrTimeout);
@@ -732,13 +771,13 @@ bool make_map(CUtensorMap* map, const void* base, int rows, int cols) {
 }
 
 template <typename Tout>
-cudaError_t launch_scan(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const ChunkArgs& p,
+cudaError_t launch_scan(const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mo, const ChunkArgs& p,
                         cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(chunk_scan_kernel<Tout>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)K2_SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid(p.Nv, p.num_seqs);
-  chunk_scan_kernel<Tout><<<grid, NT2, K2_SMEM, s>>>(mq, mk, mv, p);
+  chunk_scan_kernel<Tout><<<grid, NT2, K2_SMEM, s>>>(mk, mv, mo, p);
   return cudaGetLastError();
 }
 
@@ -774,7 +813,10 @@ cudaError_t launch_chunk_tc(const ChunkArgs& p, cudaStream_t s) {
   chunk_solve_kernel<<<g1, 128, S1_SMEM, s>>>(mq, mk, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  return p.out_bf16 ? launch_scan<bf16>(mq, mk, mv, p, s) : launch_scan<float>(mq, mk, mv, p, s);
+  if (!p.out_bf16) return launch_scan<float>(mk, mv, mk, p, s);   // fp32 rows are stored directly
+  CUtensorMap mo;
+  if (!make_map(&mo, p.o, p.total, p.Nv * DV)) return cudaErrorInvalidValue;
+  return launch_scan<bf16>(mk, mv, mo, p, s);
 }
 
 // ---------------------------------------------------------------------------

@@ -188,8 +188,8 @@ int gdn_chunk_prefill_fp32(const gdn_dims* dims, const int32_t* cu_seqlens,
  *   - Supported inputs: bf16 q/k/v with Dk = Dv = 128 (else
  *     GDN_ERR_UNSUPPORTED).
  *   - Size limit: the workspace that gdn_chunk_prefill_workspace_size()
- *     reports for these dims must be at most 32 MiB (for 32 value heads,
- *     about 2,000 tokens); larger problems return
+ *     reports for these dims must be at most 32 MiB (for 32 value heads and
+ *     one sequence, about 1,280 tokens); larger problems return
  *     GDN_ERR_INVALID_ARG and should use gdn_chunk_prefill.
  *   - The first call on a device looks up the scratch array's device address
  *     (once per device, with that device current); make that first call before
