@@ -48,7 +48,6 @@ constexpr int CT = 64;        // chunk length
 constexpr int DK = 128;
 constexpr int DV = 128;
 constexpr uint32_t WAIT_LIMIT = 1u << 22;
-constexpr int FS = 68;        // fp32 matrix row stride (16-byte aligned rows)
 // workspace per (chunk, value head), written by the solve kernel:
 //   [-W dk0-63 | Q~ dk0-63 | -W dk64-127 | Q~ dk64-127]  the N = 128 operand of the S products
 //   P, then dec = exp(G_L - G) (64 floats) and gamma_L, then T diag(beta)
@@ -129,110 +128,21 @@ __device__ __forceinline__ int slot_base(const ChunkArgs& p, int s) {
   return seq_start(p.cu, p.num_seqs, p.total, s) / CT + s;
 }
 
-// C[i][j] (rows 2*ti + {0,1}, cols 4*tj + {0..3}) = sum_k X[xr + i][xc + k] * Y[yr + k][yc + j]
-// over k < K, a 32 x 32 output split over 128 threads (16 x 8 tiles of 2 x 4).
-__device__ __forceinline__ void gemm32_tile(const float* X, int xr, int xc, const float* Y, int yr, int yc,
-                                            int K, float (&acc)[2][4], int tid) {
-  const int ti = tid >> 3, tj = tid & 7;
-#pragma unroll
-  for (int a = 0; a < 2; ++a)
-#pragma unroll
-    for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
-#pragma unroll 8
-  for (int k = 0; k < K; ++k) {
-    const float x0 = X[(xr + 2 * ti) * FS + xc + k];
-    const float x1 = X[(xr + 2 * ti + 1) * FS + xc + k];
-    const float4 y = *reinterpret_cast<const float4*>(Y + (yr + k) * FS + yc + 4 * tj);
-    acc[0][0] = fmaf(x0, y.x, acc[0][0]); acc[0][1] = fmaf(x0, y.y, acc[0][1]);
-    acc[0][2] = fmaf(x0, y.z, acc[0][2]); acc[0][3] = fmaf(x0, y.w, acc[0][3]);
-    acc[1][0] = fmaf(x1, y.x, acc[1][0]); acc[1][1] = fmaf(x1, y.y, acc[1][1]);
-    acc[1][2] = fmaf(x1, y.z, acc[1][2]); acc[1][3] = fmaf(x1, y.w, acc[1][3]);
-  }
-}
-
-// T = (I + A)^-1 for a 64 x 64 strictly lower A (fp32, stride FS), by 128
-// threads; T is fully written (zeros above the diagonal).  16 x 16 diagonal
-// blocks by right-looking substitution, then the two 16 -> 32 merges and the
-// 32 -> 64 merge, each T21 = -T22 A21 T11.
-__device__ void invert_unit_lower(const float* AF, float* TF, int tid) {
-  for (int i = tid * 4; i < 64 * FS; i += 128 * 4)
-    *reinterpret_cast<float4*>(TF + i) = make_float4(0.f, 0.f, 0.f, 0.f);
-  __syncthreads();
-  if (tid < 64) {
-    const int b16 = (tid >> 4) * 16, cc = tid & 15;
-    float x[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) x[i] = (i == cc) ? 1.f : 0.f;
-#pragma unroll
-    for (int j = 0; j < 15; ++j) {
-#pragma unroll
-      for (int i = j + 1; i < 16; ++i) x[i] = fmaf(-AF[(b16 + i) * FS + b16 + j], x[j], x[i]);
-    }
-#pragma unroll
-    for (int i = 0; i < 16; ++i) TF[(b16 + i) * FS + b16 + cc] = x[i];
-  }
-  __syncthreads();
-  {   // 16 -> 32: pair p = tid / 64 handles block (2p+1, 2p); 2 x 2 outputs per thread
-    const int pr = tid >> 6, q = tid & 63, ti = q >> 3, tj = q & 7;
-    const int R = (2 * pr + 1) * 16, C = 2 * pr * 16;
-    float y[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      const float a0 = AF[(R + 2 * ti) * FS + C + k], a1 = AF[(R + 2 * ti + 1) * FS + C + k];
-      const float2 t = *reinterpret_cast<const float2*>(TF + (C + k) * FS + C + 2 * tj);
-      y[0][0] = fmaf(a0, t.x, y[0][0]); y[0][1] = fmaf(a0, t.y, y[0][1]);
-      y[1][0] = fmaf(a1, t.x, y[1][0]); y[1][1] = fmaf(a1, t.y, y[1][1]);
-    }
-#pragma unroll
-    for (int a = 0; a < 2; ++a)
-      *reinterpret_cast<float2*>(TF + (R + 2 * ti + a) * FS + C + 2 * tj) = make_float2(y[a][0], y[a][1]);
-    __syncthreads();
-    float x[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      const float t0 = TF[(R + 2 * ti) * FS + R + k], t1 = TF[(R + 2 * ti + 1) * FS + R + k];
-      const float2 yy = *reinterpret_cast<const float2*>(TF + (R + k) * FS + C + 2 * tj);
-      x[0][0] = fmaf(t0, yy.x, x[0][0]); x[0][1] = fmaf(t0, yy.y, x[0][1]);
-      x[1][0] = fmaf(t1, yy.x, x[1][0]); x[1][1] = fmaf(t1, yy.y, x[1][1]);
-    }
-    __syncthreads();
-#pragma unroll
-    for (int a = 0; a < 2; ++a)
-      *reinterpret_cast<float2*>(TF + (R + 2 * ti + a) * FS + C + 2 * tj) = make_float2(-x[a][0], -x[a][1]);
-    __syncthreads();
-  }
-  {   // 32 -> 64: T[32:64][0:32] = -T[32:64][32:64] (A[32:64][0:32] T[0:32][0:32])
-    const int ti = tid >> 3, tj = tid & 7;
-    float acc[2][4];
-    gemm32_tile(AF, 32, 0, TF, 0, 0, 32, acc, tid);
-#pragma unroll
-    for (int a = 0; a < 2; ++a)
-      *reinterpret_cast<float4*>(TF + (32 + 2 * ti + a) * FS + 4 * tj) =
-          make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
-    __syncthreads();
-    gemm32_tile(TF, 32, 32, TF, 32, 0, 32, acc, tid);
-    __syncthreads();
-#pragma unroll
-    for (int a = 0; a < 2; ++a)
-      *reinterpret_cast<float4*>(TF + (32 + 2 * ti + a) * FS + 4 * tj) =
-          make_float4(-acc[a][0], -acc[a][1], -acc[a][2], -acc[a][3]);
-    __syncthreads();
-  }
-}
-
 // ---------------------------------------------------------------------------
 // kernel 1: per (chunk slot, value head), in parallel over all of them
 //   D1 = [K; Q] K^T (rows 0-63 K K^T, rows 64-127 Q K^T), A and P from it,
-//   T = (I + A)^-1, then W = T diag(beta gamma) K.  Writes T diag(beta), P
-//   and -W as bf16 128-byte-swizzled tiles to the workspace slot.
+//   T = (I + A)^-1 in fp32 on CUDA cores, W = T diag(beta gamma) K.
+//   Writes every workspace tile of the head.
 // ---------------------------------------------------------------------------
+constexpr int FS = 68;                              // fp32 row stride: 16-byte rows, conflict-free columns
 constexpr uint32_t S1_QK = 0;                       // K box0 | Q box0 | K box1 | Q box1 (32 KB)
-constexpr uint32_t S1_TBG = 32768;                  // T diag(beta gamma) | zeros (16 KB)
-constexpr uint32_t S1_AF = 49152;                   // A fp32 [64][FS]
-constexpr uint32_t S1_TF = S1_AF + 64 * FS * 4;     // T fp32 [64][FS]
-constexpr uint32_t S1_VEC = S1_TF + 64 * FS * 4;    // G, beta, beta*gamma, gamma, dec (5 x 64 floats)
+constexpr uint32_t S1_AT = 32768;                   // A^T fp32 [k][i]; later [T diag(beta gamma); 0] bf16
+constexpr uint32_t S1_TR = S1_AT + 64 * FS * 4;     // T fp32 [i][j]
+constexpr uint32_t S1_XS = S1_TR + 64 * FS * 4;     // block-product scratch, fp32 32 x 36
+constexpr uint32_t S1_VEC = S1_XS + 32 * 36 * 4;    // G, beta, beta*gamma, gamma, dec (5 x 64 floats)
 constexpr uint32_t S1_BAR = S1_VEC + 5 * 64 * 4;
 constexpr uint32_t S1_SMEM = S1_BAR + 64 + 1024;
+static_assert(S1_TR % 1024 == 0 && S1_AT % 1024 == 0, "tile alignment");
 
 // Write 64 bf16 values as swizzled row `row` of a 64-column block in global memory.
 __device__ __forceinline__ void st_row64_global(uint8_t* dst, uint32_t row, const float* v, float sc) {
@@ -249,13 +159,108 @@ __device__ __forceinline__ void st_row64_global(uint8_t* dst, uint32_t row, cons
   }
 }
 
-__global__ void __launch_bounds__(128)
+// T = (I + A)^-1 for a 64 x 64 strictly lower A given transposed (AT[k][i] =
+// A[i][k], stride FS), by 128 threads into TR (row-major, stride FS; TR must
+// hold zeros above the diagonal blocks on entry).
+//   1. the four 16 x 16 diagonal blocks, one column per thread (64 threads);
+//   2. T[b+1][b] = -T[b+1][b+1] (A[b+1][b] T[b][b]) for the pairs (0,1), (2,3);
+//   3. T[32:64][0:32] = -T[32:64][32:64] (A[32:64][0:32] T[0:32][0:32]).
+// XS is fp32 scratch of 32 x 36.
+__device__ __forceinline__ void invert_unit_lower(const float* AT, float* TR, float* XS, int tid) {
+  if (tid < 64) {
+    const int b = (tid >> 4) * 16, c = tid & 15;
+    float x[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) x[i] = i == c ? 1.f : 0.f;
+#pragma unroll
+    for (int k = 0; k < 15; ++k) {
+      const float xk = x[k];
+#pragma unroll
+      for (int i4 = ((k + 1) >> 2) << 2; i4 < 16; i4 += 4) {
+        const float4 a = *reinterpret_cast<const float4*>(AT + (b + k) * FS + b + i4);
+        if (i4 + 0 > k) x[i4 + 0] = fmaf(-a.x, xk, x[i4 + 0]);
+        if (i4 + 1 > k) x[i4 + 1] = fmaf(-a.y, xk, x[i4 + 1]);
+        if (i4 + 2 > k) x[i4 + 2] = fmaf(-a.z, xk, x[i4 + 2]);
+        if (i4 + 3 > k) x[i4 + 3] = fmaf(-a.w, xk, x[i4 + 3]);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) TR[(b + i) * FS + b + c] = x[i];
+  }
+  __syncthreads();
+  {   // 16 -> 32: pair pr = tid / 64, block rows R = 16 (2 pr + 1), columns C = 32 pr
+    const int pr = tid >> 6, u = tid & 63;
+    const int r0 = 2 * (u >> 3), c0 = 2 * (u & 7);
+    const int R = 16 * (2 * pr + 1), C = 32 * pr;
+    float* X = XS + pr * 16 * 20;
+    float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
+#pragma unroll 4
+    for (int k = 0; k < 16; ++k) {
+      const float2 a = *reinterpret_cast<const float2*>(AT + (C + k) * FS + R + r0);
+      const float2 t = *reinterpret_cast<const float2*>(TR + (C + k) * FS + C + c0);
+      a00 = fmaf(a.x, t.x, a00); a01 = fmaf(a.x, t.y, a01);
+      a10 = fmaf(a.y, t.x, a10); a11 = fmaf(a.y, t.y, a11);
+    }
+    *reinterpret_cast<float2*>(X + r0 * 20 + c0) = make_float2(a00, a01);
+    *reinterpret_cast<float2*>(X + (r0 + 1) * 20 + c0) = make_float2(a10, a11);
+    __syncthreads();
+    a00 = a01 = a10 = a11 = 0.f;
+#pragma unroll 4
+    for (int k = 0; k < 16; ++k) {
+      const float t0 = TR[(R + r0) * FS + R + k], t1 = TR[(R + r0 + 1) * FS + R + k];
+      const float2 y = *reinterpret_cast<const float2*>(X + k * 20 + c0);
+      a00 = fmaf(t0, y.x, a00); a01 = fmaf(t0, y.y, a01);
+      a10 = fmaf(t1, y.x, a10); a11 = fmaf(t1, y.y, a11);
+    }
+    *reinterpret_cast<float2*>(TR + (R + r0) * FS + C + c0) = make_float2(-a00, -a01);
+    *reinterpret_cast<float2*>(TR + (R + r0 + 1) * FS + C + c0) = make_float2(-a10, -a11);
+  }
+  __syncthreads();
+  {   // 32 -> 64: 2 x 4 outputs per thread
+    const int r0 = 2 * (tid >> 3), c0 = 4 * (tid & 7);
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll 8
+    for (int k = 0; k < 32; ++k) {
+      const float2 a = *reinterpret_cast<const float2*>(AT + k * FS + 32 + r0);
+      const float4 t = *reinterpret_cast<const float4*>(TR + k * FS + c0);
+      acc[0][0] = fmaf(a.x, t.x, acc[0][0]); acc[0][1] = fmaf(a.x, t.y, acc[0][1]);
+      acc[0][2] = fmaf(a.x, t.z, acc[0][2]); acc[0][3] = fmaf(a.x, t.w, acc[0][3]);
+      acc[1][0] = fmaf(a.y, t.x, acc[1][0]); acc[1][1] = fmaf(a.y, t.y, acc[1][1]);
+      acc[1][2] = fmaf(a.y, t.z, acc[1][2]); acc[1][3] = fmaf(a.y, t.w, acc[1][3]);
+    }
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+      *reinterpret_cast<float4*>(XS + (r0 + a) * 36 + c0) = make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
+    __syncthreads();
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
+#pragma unroll 8
+    for (int k = 0; k < 32; ++k) {
+      const float t0 = TR[(32 + r0) * FS + 32 + k], t1 = TR[(32 + r0 + 1) * FS + 32 + k];
+      const float4 y = *reinterpret_cast<const float4*>(XS + k * 36 + c0);
+      acc[0][0] = fmaf(t0, y.x, acc[0][0]); acc[0][1] = fmaf(t0, y.y, acc[0][1]);
+      acc[0][2] = fmaf(t0, y.z, acc[0][2]); acc[0][3] = fmaf(t0, y.w, acc[0][3]);
+      acc[1][0] = fmaf(t1, y.x, acc[1][0]); acc[1][1] = fmaf(t1, y.y, acc[1][1]);
+      acc[1][2] = fmaf(t1, y.z, acc[1][2]); acc[1][3] = fmaf(t1, y.w, acc[1][3]);
+    }
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+      *reinterpret_cast<float4*>(TR + (32 + r0 + a) * FS + c0) =
+          make_float4(-acc[a][0], -acc[a][1], -acc[a][2], -acc[a][3]);
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(128, 3)
 chunk_solve_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                    ChunkArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* AF = reinterpret_cast<float*>(sm + S1_AF);
-  float* TF = reinterpret_cast<float*>(sm + S1_TF);
+  float* AT = reinterpret_cast<float*>(sm + S1_AT);
+  float* TR = reinterpret_cast<float*>(sm + S1_TR);
+  float* XS = reinterpret_cast<float*>(sm + S1_XS);
   float* Gs = reinterpret_cast<float*>(sm + S1_VEC);
   float* Bet = Gs + CT;
   float* BG = Bet + CT;
@@ -289,13 +294,13 @@ chunk_solve_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
     tma_load_2d(sm + S1_QK + 16384, &tmk, bar, hk * DK + 64, c0);
     tma_load_2d(sm + S1_QK + 24576, &tmq, bar, hk * DK + 64, c0);
   }
-  if (warp == 0) tmem_alloc(tslot, 256);
-  for (int i = tid * 16; i < 8192; i += 128 * 16)       // zero rows 64-127 of the W-product A operand
-    *reinterpret_cast<uint4*>(sm + S1_TBG + 8192 + i) = make_uint4(0u, 0u, 0u, 0u);
-  if (tid < CT) {
-    Gs[tid] = tid < len ? p.g[(size_t)(c0 + tid) * p.Nv + h] : 0.f;
-    Bet[tid] = tid < len ? p.beta[(size_t)(c0 + tid) * p.Nv + h] : 0.f;
+  {   // threads 0-63 read g, threads 64-127 read beta
+    const int r = tid & 63;
+    (tid < CT ? Gs : Bet)[r] = r < len ? (tid < CT ? p.g : p.beta)[(size_t)(c0 + r) * p.Nv + h] : 0.f;
   }
+  if (warp == 0) tmem_alloc(tslot, 128);
+  for (int i = tid * 4; i < 64 * FS; i += 128 * 4)       // T starts at zero above its diagonal blocks
+    *reinterpret_cast<float4*>(TR + i) = make_float4(0.f, 0.f, 0.f, 0.f);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -313,9 +318,10 @@ chunk_solve_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
     if (tid == 0) {
       const uint32_t id = idesc_bf16(128, 64, false, false);
       const uint64_t a = sdesc_sw128(sb + S1_QK, 16, 1024);
+#pragma unroll
       for (int ks = 0; ks < DK / 16; ++ks) {
-        const uint32_t o = kstep_offset(true, ks, 16384) >> 4;
-        mma_bf16(tbase, a + o, a + o, id, ks > 0);
+        const uint32_t o = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
+        mma_bf16(tbase, a + o, a + o, id, ks > 0 ? 1u : 0u);
       }
       mma_commit(bar);
     }
@@ -326,20 +332,13 @@ chunk_solve_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
     {
       float v[64];
       tm_ld64(lane_base, v);
-      if (tid < CT) {                       // K K^T row r -> lower triangle of A
-        const int r = tid;
-        const float gr = Gs[r], br = Bet[r];
+      const int r = tid & 63;
+      const float gr = Gs[r];
+      if (tid < CT) {                         // K K^T row r -> column r of A^T
+        const float br = Bet[r];
 #pragma unroll
-        for (int jb = 0; jb < 4; ++jb) {
-          if (jb * 16 < r) {
-#pragma unroll
-            for (int j = jb * 16; j < jb * 16 + 16; ++j)
-              if (j < r) AF[r * FS + j] = br * __expf(gr - Gs[j]) * v[j];
-          }
-        }
-      } else {                              // Q K^T row r -> P = M o Q K^T
-        const int r = tid - CT;
-        const float gr = Gs[r];
+        for (int j = 0; j < 64; ++j) AT[j * FS + r] = j < r ? br * __expf(gr - Gs[j]) * v[j] : 0.f;
+      } else {                                // Q K^T row r -> P = M o Q K^T
 #pragma unroll
         for (int jb = 0; jb < 4; ++jb) {
           if (jb * 16 <= r) {
@@ -355,6 +354,7 @@ chunk_solve_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
     }
     // diag(gamma) Q -> rows 64-127 of the two [-W; Q~] blocks (same swizzled rows as
     // the TMA tiles), then dec and gamma_L
+#pragma unroll 2
     for (int i = tid; i < 1024; i += 128) {
       const uint32_t off = (uint32_t)(i >> 9) * 16384u + (uint32_t)(i & 511) * 16u;
       const float f = Gam[(i & 511) >> 3];
@@ -372,11 +372,16 @@ chunk_solve_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
     if (tid == 0) reinterpret_cast<float*>(ws + WS_VEC)[CT] = Gam[CT - 1];
     tc_fence_before();
     __syncthreads();
-    invert_unit_lower(AF, TF, tid);
+    invert_unit_lower(AT, TR, XS, tid);
+    // A^T is dead: its space becomes the [T diag(beta gamma); 0] operand
+    uint8_t* tbg = sm + S1_AT;
+    for (int i = tid * 16; i < 8192; i += 128 * 16)
+      *reinterpret_cast<uint4*>(tbg + 8192 + i) = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll 2
     for (int idx = tid; idx < CT * 8; idx += 128) {
       const int r = idx >> 3, ch = idx & 7;
-      const float4 t0 = *reinterpret_cast<const float4*>(TF + r * FS + ch * 8);
-      const float4 t1 = *reinterpret_cast<const float4*>(TF + r * FS + ch * 8 + 4);
+      const float4 t0 = *reinterpret_cast<const float4*>(TR + r * FS + ch * 8);
+      const float4 t1 = *reinterpret_cast<const float4*>(TR + r * FS + ch * 8 + 4);
       const float t[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
       uint32_t wa[4], wb[4];
 #pragma unroll
@@ -389,7 +394,7 @@ chunk_solve_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
       }
       const uint32_t sw = r * 128u + ((((uint32_t)ch ^ (uint32_t)(r & 7)) & 7u) << 4);
       *reinterpret_cast<uint4*>(ws + WS_TB + sw) = make_uint4(wa[0], wa[1], wa[2], wa[3]);
-      *reinterpret_cast<uint4*>(sm + S1_TBG + sw) = make_uint4(wb[0], wb[1], wb[2], wb[3]);
+      *reinterpret_cast<uint4*>(tbg + sw) = make_uint4(wb[0], wb[1], wb[2], wb[3]);
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -398,19 +403,22 @@ chunk_solve_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
     if (tid == 0) {
       // W = [T diag(beta gamma); 0] K  (rows 0-63 of the 128 x 128 result)
       const uint32_t id = idesc_bf16(128, 128, false, true);
-      const uint64_t a = sdesc_sw128(sb + S1_TBG, 16, 1024);
+      const uint64_t a = sdesc_sw128(sb + S1_AT, 16, 1024);
       const uint64_t b = sdesc_sw128(sb + S1_QK, 16384, 1024);
-      for (int ks = 0; ks < CT / 16; ++ks) mma_bf16(tbase + 64, a + ks * 2, b + ks * 128, id, ks > 0);
+#pragma unroll
+      for (int ks = 0; ks < CT / 16; ++ks) mma_bf16(tbase, a + ks * 2, b + ks * 128, id, ks > 0 ? 1u : 0u);
       mma_commit(bar);
     }
     ok = mbar_wait(bar, 0, WAIT_LIMIT);
     if (__syncthreads_and(ok ? 1 : 0)) {
       tc_fence_after();
+      if (warp < 2) {
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        float v[64];
-        tm_ld64(lane_base + 64 + half * 64, v);
-        if (tid < CT) st_row64_global(ws + WS_QW + half * 16384, tid, v, -1.f);
+        for (int half = 0; half < 2; ++half) {
+          float v[64];
+          tm_ld64(lane_base + half * 64, v);
+          st_row64_global(ws + WS_QW + half * 16384, tid, v, -1.f);
+        }
       }
     } else if (tid == 0) {
       raise_error(p.err, kDevErrTimeout);
@@ -420,7 +428,7 @@ chunk_solve_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tbase, 256);
+  if (warp == 0) tmem_dealloc(tbase, 128);
 }
 
 // ---------------------------------------------------------------------------
