@@ -207,58 +207,109 @@ conv_gating_kernel(ConvGatingArgs p) {
   }
 }
 
-// Tiled variant for bf16 inputs with C a multiple of 1024: a CTA stages a
-// [3 + 32 tokens] x [1024 channels] tile of mixed_qkv in shared memory with
-// eight TMA box loads (the rows before the first token, including negative
-// token indices, arrive as zeros), then each warp walks its 128-channel strip
-// down the tile.  The data in flight lives in the copy engine, not in
-// registers, so many warps stay resident.  Tokens in the first 3 positions of
-// a sequence are recomputed with their conv state afterwards.
-constexpr int TT = 32;                       // tokens per tile
+// Tiled variant for bf16 inputs with C a multiple of 1024 and q/k regions of
+// whole 256-channel strips.  A persistent CTA walks tiles of [3 + 16 tokens] x
+// [1024 channels] of mixed_qkv, staged in shared memory by four TMA box loads
+// (the rows before the first token, including negative token indices, arrive
+// as zeros) with the next tile's loads in flight while the current one is
+// computed.  Warp w walks 256-channel strip w % 4 (8 channels per lane,
+// 16-byte reads) down tokens 8 (w / 4) .. + 7 of the tile with a four-row
+// register ring; the loop is unrolled so the ring never moves.  Tokens in
+// the first 3 positions of a sequence are recomputed with their conv state
+// afterwards.
+constexpr int TT = 16;                         // tokens per tile
 constexpr int TROWS = TT + 3;
-constexpr uint32_t STRIP_BYTES = TROWS * 256;  // 128 bf16 channels per row
-constexpr uint32_t TILE_BYTES = 8 * STRIP_BYTES;
-constexpr uint32_t TILE_SMEM = TILE_BYTES + 64 + 128;
+constexpr int RPW = TT / 2;                    // tokens per warp
+constexpr uint32_t STRIP_BYTES = TROWS * 512;  // 256 bf16 channels per row
+constexpr uint32_t TILE_BYTES = 4 * STRIP_BYTES;
+constexpr uint32_t TILE_SMEM = 2 * TILE_BYTES + 64 + 128;
+
+__device__ __forceinline__ float tanh_approx(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// SiLU for the tiled path: x sigmoid(x) = h + h tanh(h), h = x / 2, with the
+// hardware tanh when the result is rounded to bf16 anyway (its relative error,
+// about 2^-11, stays below half a bf16 ulp); the exact-division form for fp32.
+template <typename Tout> __device__ __forceinline__ float silu_out(float x);
+template <> __device__ __forceinline__ float silu_out<bf16>(float x) {
+  const float h = 0.5f * x;
+  return fmaf(h, tanh_approx(h), h);
+}
+template <> __device__ __forceinline__ float silu_out<float>(float x) { return silu_fast(x); }
+
+__device__ __forceinline__ void lds8(const uint8_t* p, float (&f)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+    f[2 * i] = v.x;
+    f[2 * i + 1] = v.y;
+  }
+}
 
 template <typename Tout>
-__global__ void __launch_bounds__(256, 3)
+__global__ void __launch_bounds__(256, 2)
 conv_gating_tile_kernel(const __grid_constant__ CUtensorMap tmx, ConvGatingArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + TILE_BYTES);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + 2 * TILE_BYTES);   // one per buffer
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int sid = warp & 3, half = warp >> 2;
   const int nct = p.C / 1024;
   const int ntiles = ((p.total + TT - 1) / TT) * nct;
   const int kd = p.Nk * p.Dk;
-  const int lanes_per_head = p.Dk / 4;
+  const int lanes_per_head = p.Dk / 8;
   const bf16* st_in = static_cast<const bf16*>(p.state_in);
   const bf16* xg = static_cast<const bf16*>(p.x);
+  auto issue = [&](int tile, int buf) {
+    const int t0 = (tile / nct) * TT, ct = tile % nct;
+    tc::mbar_arrive_expect_tx(&bar[buf], TILE_BYTES);
+    for (int i = 0; i < 4; ++i)
+      tc::tma_load_2d(sm + buf * TILE_BYTES + i * STRIP_BYTES, &tmx, &bar[buf], ct * 1024 + i * 256, t0 - 3);
+  };
   if (threadIdx.x == 0) {
-    tc::mbar_init(bar, 1);
+    tc::mbar_init(&bar[0], 1);
+    tc::mbar_init(&bar[1], 1);
     tc::fence_barrier_init();
+    if (blockIdx.x < ntiles) issue(blockIdx.x, 0);
   }
   __syncthreads();
-  uint32_t phase = 0;
-  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, phase ^= 1u) {
+  float wt[8][4], bias[8];
+  int wct = -1;                                      // channel block the weights belong to
+  int k = 0;
+  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k) {
+    const int buf = k & 1;
     const int tt = tile / nct, ct = tile % nct;
     const int t0 = tt * TT, t_end = min(t0 + TT, p.total);
-    if (threadIdx.x == 0) {
-      tc::mbar_arrive_expect_tx(bar, TILE_BYTES);
-      for (int i = 0; i < 8; ++i) tc::tma_load_2d(sm + i * STRIP_BYTES, &tmx, bar, ct * 1024 + i * 128, t0 - 3);
+    // the other buffer was released by the barrier that ended the previous tile
+    if (threadIdx.x == 0 && tile + (int)gridDim.x < ntiles) issue(tile + gridDim.x, buf ^ 1);
+    const int strip0 = ct * 1024 + sid * 256;         // first channel of the warp's strip
+    const int c0 = strip0 + lane * 8;
+    const int region = strip0 < kd ? 0 : (strip0 < 2 * kd ? 1 : 2);
+    if (ct != wct) {
+      wct = ct;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) load4(static_cast<const bf16*>(p.w) + (size_t)(c0 + c) * 4, wt[c]);
+      if (p.bias) {
+        load8(static_cast<const bf16*>(p.bias) + c0, bias);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) bias[c] = 0.f;
+      }
     }
-    const bool ok = tc::mbar_wait(bar, phase, 1u << 24);
+    const bool ok = tc::mbar_wait(&bar[buf], (uint32_t)(k >> 1) & 1u, 1u << 24);
     if (!__syncthreads_and(ok ? 1 : 0)) {
-      if (threadIdx.x == 0) raise_error(p.err, kDevErrTimeout);
+      if (threadIdx.x == 0) {
+        raise_error(p.err, kDevErrTimeout);
+        // let the copies in flight land before the CTA's shared memory goes away
+        tc::mbar_wait(&bar[buf], (uint32_t)(k >> 1) & 1u, 1u << 24);
+        if (tile + (int)gridDim.x < ntiles) tc::mbar_wait(&bar[buf ^ 1], (uint32_t)((k + 1) >> 1) & 1u, 1u << 24);
+      }
       return;
     }
-    const int strip = ct * 8 + warp;
-    const int c0 = strip * 128 + lane * 4;
-    const int region = c0 < kd ? 0 : (c0 < 2 * kd ? 1 : 2);
-    float wt[4][4];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) load4(static_cast<const bf16*>(p.w) + (size_t)(c0 + c) * 4, wt[c]);
-    float bias[4] = {0.f, 0.f, 0.f, 0.f};
-    if (p.bias) load4(static_cast<const bf16*>(p.bias) + c0, bias);
     Tout* dst;
     size_t row_stride;
     if (region < 2) {
@@ -268,83 +319,93 @@ conv_gating_tile_kernel(const __grid_constant__ CUtensorMap tmx, ConvGatingArgs 
       dst = static_cast<Tout*>(p.v) + (c0 - 2 * kd);
       row_stride = (size_t)p.Nv * p.Dv;
     }
+    Tout* const dst0 = dst;
     const float qs = region == 0 ? p.q_scale : 1.0f;
-    const uint8_t* rows = sm + warp * STRIP_BYTES + lane * 8;
-    float xm[3][4];
+    const int r0 = RPW * half;                        // first token of this warp within the tile
+    const uint8_t* rows = sm + buf * TILE_BYTES + sid * STRIP_BYTES + lane * 16 + r0 * 512;
+    dst += (size_t)(t0 + r0) * row_stride;
+    float ring[4][8];
 #pragma unroll
-    for (int j = 0; j < 3; ++j) load4(reinterpret_cast<const bf16*>(rows + j * 256), xm[j]);
-    for (int r = 0; r < TT; ++r) {
-      const int t = t0 + r;
-      if (t >= t_end) break;
-      float cur[4];
-      load4(reinterpret_cast<const bf16*>(rows + (r + 3) * 256), cur);
-      float y[4];
+    for (int j = 0; j < 3; ++j) lds8(rows + j * 512, ring[j]);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float acc = bias[c];
-        acc = fmaf(wt[c][0], xm[0][c], acc);
-        acc = fmaf(wt[c][1], xm[1][c], acc);
-        acc = fmaf(wt[c][2], xm[2][c], acc);
-        y[c] = silu_fast(fmaf(wt[c][3], cur[c], acc));
+    for (int r = 0; r < RPW; ++r) {
+      float(&cur)[8] = ring[(r + 3) & 3];
+      lds8(rows + (r + 3) * 512, cur);
+      if (t0 + r0 + r < t_end) {
+        const float(&x0)[8] = ring[r & 3];
+        const float(&x1)[8] = ring[(r + 1) & 3];
+        const float(&x2)[8] = ring[(r + 2) & 3];
+        float y[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          float acc = fmaf(wt[c][0], x0[c], bias[c]);
+          acc = fmaf(wt[c][1], x1[c], acc);
+          acc = fmaf(wt[c][2], x2[c], acc);
+          y[c] = silu_out<Tout>(fmaf(wt[c][3], cur[c], acc));
+        }
+        if (region < 2) {
+          float ss = 0.f;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) ss = fmaf(y[c], y[c], ss);
+          ss = group_sum(ss, lanes_per_head);
+          const float inv = rsqrtf(ss + p.l2_eps) * qs;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) y[c] *= inv;
+        }
+        store8(dst, y);
       }
-      if (region < 2) {
-        float ss = y[0] * y[0] + y[1] * y[1] + y[2] * y[2] + y[3] * y[3];
-        ss = group_sum(ss, lanes_per_head);
-        const float inv = rsqrtf(ss + p.l2_eps) * qs;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) y[c] *= inv;
-      }
-      store4(dst + (size_t)t * row_stride, y);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) { xm[0][c] = xm[1][c]; xm[1][c] = xm[2][c]; xm[2][c] = cur[c]; }
+      dst += row_stride;
     }
-    // tokens in the first 3 positions of a sequence: redo with the conv state
+    // tokens of this warp in the first 3 positions of a sequence: redo with the conv state
     {
-      const int seq0 = find_seq(p.cu, p.num_seqs, p.total, max(t0 - 3, 0));
+      const int ta = t0 + r0, tb = min(t0 + r0 + RPW, t_end);
+      const int seq0 = find_seq(p.cu, p.num_seqs, p.total, max(ta - 3, 0));
       for (int sq = seq0; sq < p.num_seqs; ++sq) {
         const int st = seq_start(p.cu, p.num_seqs, p.total, sq);
-        if (st >= t_end) break;
-        for (int t = max(st, t0); t < min(st + 3, t_end); ++t) {
+        if (st >= tb) break;
+        for (int t = max(st, ta); t < min(st + 3, tb); ++t) {
           const int seq = find_seq(p.cu, p.num_seqs, p.total, t);
           const int pos = t - seq_start(p.cu, p.num_seqs, p.total, seq);
-          float cur[4], y[4];
-          load4(xg + (size_t)t * p.C + c0, cur);
+          float cur[8], y[8];
+          load8(xg + (size_t)t * p.C + c0, cur);
 #pragma unroll
-          for (int c = 0; c < 4; ++c) y[c] = fmaf(wt[c][3], cur[c], bias[c]);
+          for (int c = 0; c < 8; ++c) y[c] = fmaf(wt[c][3], cur[c], bias[c]);
 #pragma unroll
           for (int j = 0; j < 3; ++j) {
             const int si = pos + j;
-            float xv[4];
+            float xv[8];
             if (si < 3) {
 #pragma unroll
-              for (int c = 0; c < 4; ++c)
+              for (int c = 0; c < 8; ++c)
                 xv[c] = (st_in != nullptr && si >= 0) ? __bfloat162float(st_in[((size_t)seq * p.C + c0 + c) * 3 + si]) : 0.f;
             } else {
-              load4(xg + (size_t)(t - 3 + j) * p.C + c0, xv);
+              load8(xg + (size_t)(t - 3 + j) * p.C + c0, xv);
             }
 #pragma unroll
-            for (int c = 0; c < 4; ++c) y[c] = fmaf(wt[c][j], xv[c], y[c]);
+            for (int c = 0; c < 8; ++c) y[c] = fmaf(wt[c][j], xv[c], y[c]);
           }
 #pragma unroll
-          for (int c = 0; c < 4; ++c) y[c] = silu_fast(y[c]);
+          for (int c = 0; c < 8; ++c) y[c] = silu_out<Tout>(y[c]);
           if (region < 2) {
-            float ss = y[0] * y[0] + y[1] * y[1] + y[2] * y[2] + y[3] * y[3];
+            float ss = 0.f;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) ss = fmaf(y[c], y[c], ss);
             ss = group_sum(ss, lanes_per_head);
             const float inv = rsqrtf(ss + p.l2_eps) * qs;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) y[c] *= inv;
+            for (int c = 0; c < 8; ++c) y[c] *= inv;
           }
-          store4(dst + (size_t)t * row_stride, y);
+          store8(dst0 + (size_t)t * row_stride, y);
         }
       }
     }
-    if (region == 2) {
-      const int hps = 128 / p.Dv;
-      const int h0 = (strip * 128 - 2 * kd) / p.Dv;
+    if (region == 2) {       // gates of the strip's value heads for this warp's tokens
+      const int hps = 256 / p.Dv;
+      const int h0 = (strip0 - 2 * kd) / p.Dv;
       const bf16* a = static_cast<const bf16*>(p.a);
       const bf16* b = static_cast<const bf16*>(p.b);
-      for (int idx = lane; idx < TT * hps; idx += 32) {
-        const int t = t0 + idx / hps;
+      for (int idx = lane; idx < RPW * hps; idx += 32) {
+        const int t = t0 + r0 + idx / hps;
         const int h = h0 + idx % hps;
         if (t < t_end) {
           const size_t o = (size_t)t * p.Nv + h;
@@ -391,15 +452,16 @@ __global__ void conv_state_kernel(ConvGatingArgs p) {
 template <typename Tin, typename Tout>
 cudaError_t launch_typed(const ConvGatingArgs& p, cudaStream_t s) {
   bool tiled = false;
-  if (std::is_same<Tin, bf16>::value && p.C % 1024 == 0 && p.total > 0) {
+  const int kd = p.Nk * p.Dk;
+  if (std::is_same<Tin, bf16>::value && p.C % 1024 == 0 && kd % 256 == 0 && p.total > 0) {
     CUtensorMap m;
-    if (make_tmap_2d(&m, p.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.total, p.C, 128, TROWS,
+    if (make_tmap_2d(&m, p.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.total, p.C, 256, TROWS,
                      CU_TENSOR_MAP_SWIZZLE_NONE)) {
       cudaError_t e = cudaFuncSetAttribute(conv_gating_tile_kernel<Tout>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TILE_SMEM);
       if (e != cudaSuccess) return e;
       const int ntiles = ((p.total + TT - 1) / TT) * (p.C / 1024);
-      const int blocks = std::min(ntiles, 152 * 3);
+      const int blocks = std::min(ntiles, 152 * 2);
       conv_gating_tile_kernel<Tout><<<blocks, 256, TILE_SMEM, s>>>(m, p);
       e = cudaGetLastError();
       if (e != cudaSuccess) return e;

@@ -14,11 +14,54 @@
 namespace gdn {
 namespace {
 
-constexpr int UNROLL = 2;
+// Eight consecutive elements held as loaded (packed bf16 or fp32) until used,
+// so UNROLL rows of x and z fit in flight with few registers.
+template <typename T> struct Raw8;
+template <> struct Raw8<bf16> {
+  uint4 u;
+  __device__ __forceinline__ void load(const bf16* p) { u = *reinterpret_cast<const uint4*>(p); }
+  __device__ __forceinline__ void zero() { u = make_uint4(0u, 0u, 0u, 0u); }
+  __device__ __forceinline__ void get(float (&f)[8]) const {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+      f[2 * i] = v.x;
+      f[2 * i + 1] = v.y;
+    }
+  }
+};
+template <> struct Raw8<float> {
+  float4 a, b;
+  __device__ __forceinline__ void load(const float* p) {
+    a = *reinterpret_cast<const float4*>(p);
+    b = *reinterpret_cast<const float4*>(p + 4);
+  }
+  __device__ __forceinline__ void zero() { a = b = make_float4(0.f, 0.f, 0.f, 0.f); }
+  __device__ __forceinline__ void get(float (&f)[8]) const {
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+  }
+};
+
+__device__ __forceinline__ float tanh_approx(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// silu(z) = h + h tanh(h), h = z / 2: the hardware tanh when y is rounded to
+// bf16 (relative error about 2^-11, below half a bf16 ulp), exact division for fp32.
+template <typename Ty> __device__ __forceinline__ float gate_silu(float z);
+template <> __device__ __forceinline__ float gate_silu<bf16>(float z) {
+  const float h = 0.5f * z;
+  return fmaf(h, tanh_approx(h), h);
+}
+template <> __device__ __forceinline__ float gate_silu<float>(float z) { return silu_fast(z); }
 
 template <typename Tx, typename Tz, typename Ty>
 __global__ void __launch_bounds__(256, 3)
 gated_rmsnorm_kernel(RmsNormArgs p) {
+  // rows in flight per warp step: 4 for bf16 x and z, fewer when wider types need the registers
+  constexpr int UNROLL = sizeof(Tx) + sizeof(Tz) == 4 ? 4 : 2;
   const int lanes_per_row = p.dim / 8;
   const int rows_per_step = 32 / lanes_per_row;          // rows per warp per unrolled step
   const int rows_per_iter = rows_per_step * UNROLL;
@@ -34,29 +77,33 @@ gated_rmsnorm_kernel(RmsNormArgs p) {
   const Tz* Z = static_cast<const Tz*>(p.z);
   Ty* Y = static_cast<Ty*>(p.y);
   for (int64_t r0 = warp_id * rows_per_iter; r0 < p.rows; r0 += warps_total * rows_per_iter) {
-    float x[UNROLL][8], z[UNROLL][8];
+    Raw8<Tx> xr[UNROLL];
+    Raw8<Tz> zr[UNROLL];
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
       const int64_t row = r0 + u * rows_per_step + sub;
       if (row < p.rows) {
-        load8(X + row * p.dim + col, x[u]);
-        load8(Z + row * p.dim + col, z[u]);
+        xr[u].load(X + row * p.dim + col);
+        zr[u].load(Z + row * p.dim + col);
       } else {
-#pragma unroll
-        for (int c = 0; c < 8; ++c) { x[u][c] = 0.f; z[u][c] = 0.f; }
+        xr[u].zero();
+        zr[u].zero();
       }
     }
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
       const int64_t row = r0 + u * rows_per_step + sub;
+      float x[8], z[8];
+      xr[u].get(x);
+      zr[u].get(z);
       float ss = 0.f;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) ss = fmaf(x[u][c], x[u][c], ss);
+      for (int c = 0; c < 8; ++c) ss = fmaf(x[c], x[c], ss);
       ss = group_sum(ss, lanes_per_row);
       const float inv = rsqrtf(ss * inv_dim + p.eps);
       float y[8];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) y[c] = x[u][c] * inv * w[c] * silu_fast(z[u][c]);
+      for (int c = 0; c < 8; ++c) y[c] = x[c] * inv * w[c] * gate_silu<Ty>(z[c]);
       if (row < p.rows) store8(Y + row * p.dim + col, y);
     }
   }
@@ -73,9 +120,9 @@ cudaError_t launch_y(const RmsNormArgs& p, cudaStream_t s, int blocks) {
 
 cudaError_t launch_gated_rmsnorm(const RmsNormArgs& p, cudaStream_t s) {
   if (p.rows == 0) return cudaSuccess;
-  const int rows_per_block = 8 * (32 / (p.dim / 8)) * UNROLL;
+  const int rows_per_block = 8 * (32 / (p.dim / 8)) * 4;
   const int64_t need = (p.rows + rows_per_block - 1) / rows_per_block;
-  const int blocks = (int)std::min<int64_t>(need, 152 * 8);
+  const int blocks = (int)std::min<int64_t>(need, 152 * 3);
   if (p.x_bf16) {
     return p.z_bf16 ? launch_y<bf16, bf16>(p, s, blocks) : launch_y<bf16, float>(p, s, blocks);
   }
