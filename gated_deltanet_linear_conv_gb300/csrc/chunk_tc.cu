@@ -165,8 +165,8 @@ __device__ __forceinline__ void st_row64_global(uint8_t* dst, uint32_t row, cons
 //   1. the four 16 x 16 diagonal blocks, one column per thread (64 threads);
 //   2. T[b+1][b] = -T[b+1][b+1] (A[b+1][b] T[b][b]) for the pairs (0,1), (2,3);
 //   3. T[32:64][0:32] = -T[32:64][32:64] (A[32:64][0:32] T[0:32][0:32]).
-// XS is fp32 scratch of 32 x 36.
-__device__ __forceinline__ void invert_unit_lower(const float* AT, float* TR, float* XS, int tid) {
+// XS is fp32 scratch of 32 x 36.  The 128 threads synchronise on named barrier barid.
+__device__ __forceinline__ void invert_unit_lower(const float* AT, float* TR, float* XS, int tid, uint32_t barid) {
   if (tid < 64) {
     const int b = (tid >> 4) * 16, c = tid & 15;
     float x[16];
@@ -187,7 +187,7 @@ __device__ __forceinline__ void invert_unit_lower(const float* AT, float* TR, fl
 #pragma unroll
     for (int i = 0; i < 16; ++i) TR[(b + i) * FS + b + c] = x[i];
   }
-  __syncthreads();
+  named_sync(barid, 128);
   {   // 16 -> 32: pair pr = tid / 64, block rows R = 16 (2 pr + 1), columns C = 32 pr
     const int pr = tid >> 6, u = tid & 63;
     const int r0 = 2 * (u >> 3), c0 = 2 * (u & 7);
@@ -203,7 +203,7 @@ __device__ __forceinline__ void invert_unit_lower(const float* AT, float* TR, fl
     }
     *reinterpret_cast<float2*>(X + r0 * 20 + c0) = make_float2(a00, a01);
     *reinterpret_cast<float2*>(X + (r0 + 1) * 20 + c0) = make_float2(a10, a11);
-    __syncthreads();
+    named_sync(barid, 128);
     a00 = a01 = a10 = a11 = 0.f;
 #pragma unroll 4
     for (int k = 0; k < 16; ++k) {
@@ -215,7 +215,7 @@ __device__ __forceinline__ void invert_unit_lower(const float* AT, float* TR, fl
     *reinterpret_cast<float2*>(TR + (R + r0) * FS + C + c0) = make_float2(-a00, -a01);
     *reinterpret_cast<float2*>(TR + (R + r0 + 1) * FS + C + c0) = make_float2(-a10, -a11);
   }
-  __syncthreads();
+  named_sync(barid, 128);
   {   // 32 -> 64: 2 x 4 outputs per thread
     const int r0 = 2 * (tid >> 3), c0 = 4 * (tid & 7);
     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -231,7 +231,7 @@ __device__ __forceinline__ void invert_unit_lower(const float* AT, float* TR, fl
 #pragma unroll
     for (int a = 0; a < 2; ++a)
       *reinterpret_cast<float4*>(XS + (r0 + a) * 36 + c0) = make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
-    __syncthreads();
+    named_sync(barid, 128);
 #pragma unroll
     for (int a = 0; a < 2; ++a)
 #pragma unroll
@@ -250,14 +250,16 @@ __device__ __forceinline__ void invert_unit_lower(const float* AT, float* TR, fl
       *reinterpret_cast<float4*>(TR + (32 + r0 + a) * FS + c0) =
           make_float4(-acc[a][0], -acc[a][1], -acc[a][2], -acc[a][3]);
   }
-  __syncthreads();
+  named_sync(barid, 128);
 }
 
-__global__ void __launch_bounds__(128, 3)
-chunk_solve_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                   ChunkArgs p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+// One (chunk slot, value head) by 128 threads (tid 0-127 of a group that
+// synchronises on named barrier barid).  sm is the group's 1024-aligned
+// shared memory (S1_BYTES), bar an initialised mbarrier whose next phase
+// parity is ph & 1 (ph advances by three), tbase 128 allocated tensor-memory
+// columns.  Returns false, with the device error flag raised, on a timeout.
+__device__ bool solve_item(uint8_t* sm, int tid, uint32_t barid, uint64_t* bar, uint32_t& ph, uint32_t tbase,
+                           const CUtensorMap* tmq, const CUtensorMap* tmk, const ChunkArgs& p, int slot, int h) {
   float* AT = reinterpret_cast<float*>(sm + S1_AT);
   float* TR = reinterpret_cast<float*>(sm + S1_TR);
   float* XS = reinterpret_cast<float*>(sm + S1_XS);
@@ -266,10 +268,7 @@ chunk_solve_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
   float* BG = Bet + CT;
   float* Gam = BG + CT;
   float* Dec = Gam + CT;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + S1_BAR);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S1_BAR + 16);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int slot = blockIdx.x, h = blockIdx.y;
+  const int warp = tid >> 5, lane = tid & 31;
   const int hk = h / (p.Nv / p.Nk);
 
   // slot -> (sequence, chunk)
@@ -280,40 +279,35 @@ chunk_solve_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
   }
   const int s = lo, c = slot - slot_base(p, s);
   int bos, eos;
-  if (!seq_bounds(p.cu, p.num_seqs, p.total, s, bos, eos)) return;   // reported by the scan kernel
-  if (c < 0 || c * CT >= eos - bos) return;                           // slot not used
+  if (!seq_bounds(p.cu, p.num_seqs, p.total, s, bos, eos)) return true;   // reported by the scan
+  if (c < 0 || c * CT >= eos - bos) return true;                           // slot not used
   const int c0 = bos + c * CT, len = min(CT, eos - c0);
   uint8_t* ws = static_cast<uint8_t*>(p.workspace) + ((size_t)slot * p.Nv + h) * TILE_T_BYTES;
+  const uint32_t lane_base = tbase + ((uint32_t)(warp * 32) << 16);
+  const uint32_t sb = smem_u32(sm);
 
   if (tid == 0) {
-    mbar_init(bar, 1);
-    fence_barrier_init();
     mbar_arrive_expect_tx(bar, 32768);
-    tma_load_2d(sm + S1_QK, &tmk, bar, hk * DK, c0);
-    tma_load_2d(sm + S1_QK + 8192, &tmq, bar, hk * DK, c0);
-    tma_load_2d(sm + S1_QK + 16384, &tmk, bar, hk * DK + 64, c0);
-    tma_load_2d(sm + S1_QK + 24576, &tmq, bar, hk * DK + 64, c0);
+    tma_load_2d(sm + S1_QK, tmk, bar, hk * DK, c0);
+    tma_load_2d(sm + S1_QK + 8192, tmq, bar, hk * DK, c0);
+    tma_load_2d(sm + S1_QK + 16384, tmk, bar, hk * DK + 64, c0);
+    tma_load_2d(sm + S1_QK + 24576, tmq, bar, hk * DK + 64, c0);
   }
   {   // threads 0-63 read g, threads 64-127 read beta
     const int r = tid & 63;
     (tid < CT ? Gs : Bet)[r] = r < len ? (tid < CT ? p.g : p.beta)[(size_t)(c0 + r) * p.Nv + h] : 0.f;
   }
-  if (warp == 0) tmem_alloc(tslot, 128);
   for (int i = tid * 4; i < 64 * FS; i += 128 * 4)       // T starts at zero above its diagonal blocks
     *reinterpret_cast<float4*>(TR + i) = make_float4(0.f, 0.f, 0.f, 0.f);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tbase = *tslot;
-  const uint32_t lane_base = tbase + ((uint32_t)(warp * 32) << 16);
-  const uint32_t sb = smem_u32(sm);
+  named_sync(barid, 128);
   if (warp == 0) {
     chunk_cumsum(Gs, Gam, Dec, lane);
     BG[lane] = Bet[lane] * Gam[lane];
     BG[lane + 32] = Bet[lane + 32] * Gam[lane + 32];
   }
-  bool ok = mbar_wait(bar, 0, WAIT_LIMIT);
-  if (__syncthreads_and(ok ? 1 : 0)) {
+  bool ok = mbar_wait(bar, ph & 1u, WAIT_LIMIT);
+  ph += 1;
+  if (!named_sync_or(barid, 128, !ok)) {
     tc_fence_after();
     if (tid == 0) {
       const uint32_t id = idesc_bf16(128, 64, false, false);
@@ -325,9 +319,11 @@ chunk_solve_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
       }
       mma_commit(bar);
     }
-    ok = mbar_wait(bar, 1, WAIT_LIMIT);
+    ok = mbar_wait(bar, ph & 1u, WAIT_LIMIT);
   }
-  if (__syncthreads_and(ok ? 1 : 0)) {
+  ph += 1;
+  bool done = false;
+  if (!named_sync_or(barid, 128, !ok)) {
     tc_fence_after();
     {
       float v[64];
@@ -371,8 +367,8 @@ chunk_solve_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
     if (tid < CT) reinterpret_cast<float*>(ws + WS_VEC)[tid] = Dec[tid];
     if (tid == 0) reinterpret_cast<float*>(ws + WS_VEC)[CT] = Gam[CT - 1];
     tc_fence_before();
-    __syncthreads();
-    invert_unit_lower(AT, TR, XS, tid);
+    named_sync(barid, 128);
+    invert_unit_lower(AT, TR, XS, tid, barid);
     // A^T is dead: its space becomes the [T diag(beta gamma); 0] operand
     uint8_t* tbg = sm + S1_AT;
     for (int i = tid * 16; i < 8192; i += 128 * 16)
@@ -398,7 +394,7 @@ chunk_solve_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
     }
     fence_proxy_async_smem();
     tc_fence_before();
-    __syncthreads();
+    named_sync(barid, 128);
     tc_fence_after();
     if (tid == 0) {
       // W = [T diag(beta gamma); 0] K  (rows 0-63 of the 128 x 128 result)
@@ -409,8 +405,8 @@ chunk_solve_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
       for (int ks = 0; ks < CT / 16; ++ks) mma_bf16(tbase, a + ks * 2, b + ks * 128, id, ks > 0 ? 1u : 0u);
       mma_commit(bar);
     }
-    ok = mbar_wait(bar, 0, WAIT_LIMIT);
-    if (__syncthreads_and(ok ? 1 : 0)) {
+    ok = mbar_wait(bar, ph & 1u, WAIT_LIMIT);
+    if (!named_sync_or(barid, 128, !ok)) {
       tc_fence_after();
       if (warp < 2) {
 #pragma unroll
@@ -420,15 +416,37 @@ chunk_solve_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
           st_row64_global(ws + WS_QW + half * 16384, tid, v, -1.f);
         }
       }
-    } else if (tid == 0) {
-      raise_error(p.err, kDevErrTimeout);
+      done = true;
     }
-  } else if (tid == 0) {
-    raise_error(p.err, kDevErrTimeout);
   }
+  ph += 1;
+  if (!done && tid == 0) raise_error(p.err, kDevErrTimeout);
+  // the next item may reuse this shared and tensor memory
+  tc_fence_before();
+  named_sync(barid, 128);
+  tc_fence_after();
+  return done;
+}
+
+__global__ void __launch_bounds__(128, 3)
+chunk_solve_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                   ChunkArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + S1_BAR);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S1_BAR + 16);
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    fence_barrier_init();
+  }
+  if ((tid >> 5) == 0) tmem_alloc(tslot, 128);
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tbase, 128);
+  tc_fence_after();
+  uint32_t ph = 0;
+  solve_item(sm, tid, 1, bar, ph, *tslot, &tmq, &tmk, p, blockIdx.x, blockIdx.y);
+  if ((tid >> 5) == 0) tmem_dealloc(*tslot, 128);
 }
 
 // ---------------------------------------------------------------------------
@@ -488,19 +506,37 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h2);
 }
 
+// Bounded wait until the solve of one (chunk slot, value head) published
+// its workspace tiles (1), or reported a failure (-1).
+constexpr uint32_t FLAG_WAIT_LIMIT = 1u << 21;
+__device__ __forceinline__ bool wait_flag(const int* f, volatile int* abort) {
+  for (uint32_t i = 0; i < FLAG_WAIT_LIMIT; ++i) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+    if (v > 0) {
+      asm volatile("fence.proxy.async.global;" ::: "memory");   // the tiles are read by the copy engine
+      return true;
+    }
+    if (v < 0 || *abort) break;
+    __nanosleep(100);
+  }
+  *abort = 1;
+  return false;
+}
+
+// The scan of one (sequence s, value head h) by the CTA's warps 0-8 (more
+// warps may be present; they only join the final barrier).  sm is 1024-aligned
+// shared memory of K2 bytes.  With `flags`, every chunk's workspace tiles are
+// awaited before they are loaded (the solve runs concurrently in other CTAs).
 template <typename Tout>
-__global__ void __launch_bounds__(NT2, 1)
-chunk_scan_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
-                  const __grid_constant__ CUtensorMap tmo, ChunkArgs p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+__device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap* tmv, const CUtensorMap* tmo,
+                          const ChunkArgs& p, int h, int s, const int* flags) {
   ScanBars* B = reinterpret_cast<ScanBars*>(sm + K2_BAR);
   volatile int* abort = &B->abort;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int dv = (warp & 3) * 32 + lane;        // this thread's tensor-memory lane
-  const int h = blockIdx.x, s = blockIdx.y;
   const int hk = h / (p.Nv / p.Nk);
   int bos, eos;
   if (!seq_bounds(p.cu, p.num_seqs, p.total, s, bos, eos)) {
@@ -524,12 +560,12 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     mbar_init(&B->gh, 1);
     B->abort = 0;
     fence_barrier_init();
-    prefetch_tmap(&tmk);
-    prefetch_tmap(&tmv);
-    prefetch_tmap(&tmo);
+    prefetch_tmap(tmk);
+    prefetch_tmap(tmv);
+    prefetch_tmap(tmo);
   }
   if (warp == 0) tmem_alloc(&B->tslot, 512);
-  for (int i = tid * 16; i < 2 * 8192; i += NT2 * 16) {   // rows 64-127 of both [T diag(beta); 0] operands
+  for (int i = tid * 16; i < 2 * 8192; i += (int)blockDim.x * 16) {   // rows 64-127 of both [T diag(beta); 0] operands
     const uint32_t off = K2_VT + (uint32_t)(i >> 13) * 32768u + 24576u + (uint32_t)(i & 8191);
     *reinterpret_cast<uint4*>(sm + off) = make_uint4(0u, 0u, 0u, 0u);
   }
@@ -544,17 +580,19 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
   if (warp == 0) {
     // ============================== PREP ==============================
     if (lane == 0) {
-      auto issue_vt = [&](int c) {
+      auto issue_vt = [&](int c) -> bool {
+        if (flags != nullptr && !wait_flag(flags + (size_t)(slot0 + c) * p.Nv + h, abort)) return false;
         const int t = bos + c * CT;
         const uint32_t vt = K2_VT + (uint32_t)(c & 1) * 32768u;
         uint64_t* bar = &B->vt[c & 1];
         mbar_arrive_expect_tx(bar, 2 * 8192 + 8192);
-        tma_load_2d(sm + vt, &tmv, bar, h * DV, t);
-        tma_load_2d(sm + vt + 8192, &tmv, bar, h * DV + 64, t);
+        tma_load_2d(sm + vt, tmv, bar, h * DV, t);
+        tma_load_2d(sm + vt + 8192, tmv, bar, h * DV + 64, t);
         bulk_load(sm + vt + 16384, ws_tile(c) + WS_TB, 8192, bar);
+        return true;
       };
       int issued = 0, committed = 0, c = 0;
-      for (; issued < n && issued < 2; ++issued) issue_vt(issued);
+      while (issued < n && issued < 2 && issue_vt(issued)) ++issued;
       bool ok = true;
       for (; c < n; ++c) {
         const int b = c & 1;
@@ -572,9 +610,8 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         mma_commit(&B->ready[b]);
         committed = c + 1;
         if (c + 2 < n) {
-          ok = wait_bar(&B->ready[b], (c >> 1) & 1, abort);                    // tiles b consumed
+          ok = wait_bar(&B->ready[b], (c >> 1) & 1, abort) && issue_vt(c + 2);   // tiles b consumed
           if (!ok) break;
-          issue_vt(c + 2);
           issued = c + 3;
         }
       }
@@ -700,12 +737,13 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         for (int i = 0; i < 32; ++i) dst[(size_t)(c0 + i) * DV] = v[i];
       }
     }
-  } else {
+  } else if (warp <= 8) {
     // ============================== OUT ==============================
     const bool leader = tid == 160;
     Tout* o = static_cast<Tout*>(p.o);
     constexpr bool kBf16Out = sizeof(Tout) == 2;
-    auto issue_stage = [&](int c) {
+    auto issue_stage = [&](int c) -> bool {
+      if (flags != nullptr && !wait_flag(flags + (size_t)(slot0 + c) * p.Nv + h, abort)) return false;
       const int t = bos + c * CT;
       const uint32_t st = K2_ST + (uint32_t)(c & 1) * STAGE_BYTES;
       uint64_t* bar = &B->stl[c & 1];
@@ -713,12 +751,13 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
       mbar_arrive_expect_tx(bar, 32768 + 8192 + 512 + 2 * 8192);
       bulk_load(sm + st, src + WS_QW, 32768, bar);
       bulk_load(sm + st + SG_P, src + WS_P, 8192 + 512, bar);
-      tma_load_2d(sm + st + SG_K, &tmk, bar, hk * DK, t);
-      tma_load_2d(sm + st + SG_K + 8192, &tmk, bar, hk * DK + 64, t);
+      tma_load_2d(sm + st + SG_K, tmk, bar, hk * DK, t);
+      tma_load_2d(sm + st + SG_K + 8192, tmk, bar, hk * DK + 64, t);
+      return true;
     };
     int issued = 0;
     if (leader)
-      for (; issued < n && issued < 2; ++issued) issue_stage(issued);
+      while (issued < n && issued < 2 && issue_stage(issued)) ++issued;
     bool fail = false;
     int c = 0;
     for (; c < n; ++c) {
@@ -727,7 +766,7 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
       const bool ok = wait_bar(&B->ob[b], (c >> 1) & 1, abort);
       if (named_sync_or(3, 128, !ok)) { fail = true; break; }
       tc_fence_after();
-      if (leader && c + 2 < n) { issue_stage(c + 2); issued = c + 3; }   // stage b is free now
+      if (leader && c + 2 < n && issue_stage(c + 2)) issued = c + 3;   // stage b is free now
       float v[64];
       tm_ld64(lane_base + TM_ACC + b * 128 + 64, v);   // lane dv holds O[0..63][dv]
       const bool use_tma = kBf16Out && len == CT;
@@ -747,8 +786,8 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         fence_proxy_async_smem();
         named_sync(3, 128);
         if (leader) {
-          tma_store_2d(&tmo, os, h * DV, c0);
-          tma_store_2d(&tmo, os + 8192, h * DV + 64, c0);
+          tma_store_2d(tmo, os, h * DV, c0);
+          tma_store_2d(tmo, os + 8192, h * DV + 64, c0);
           bulk_commit_group();
         }
       } else {
@@ -769,6 +808,79 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tbase, 512);
+}
+
+template <typename Tout>
+__global__ void __launch_bounds__(NT2, 1)
+chunk_scan_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                  const __grid_constant__ CUtensorMap tmo, ChunkArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  scan_body<Tout>(sm, &tmk, &tmv, &tmo, p, blockIdx.x, blockIdx.y, nullptr);
+}
+
+// ---------------------------------------------------------------------------
+// Solve and scan in one cooperative launch, for a single sequence: the first
+// `nscan` CTAs run the scan of one value head each; every other CTA runs three
+// independent 128-thread solve groups (own shared memory slice, 128 tensor-
+// memory columns, named barrier) that claim (chunk slot, value head) items in
+// chunk order and publish a ready flag per item.  A scan CTA awaits a chunk's
+// flag before loading its tiles, so the solve of later chunks overlaps the
+// scan of earlier ones.  All CTAs are resident at once (cooperative launch
+// with one CTA per SM), so these waits always end; each is bounded anyway.
+// ---------------------------------------------------------------------------
+constexpr int NT3 = 384;
+constexpr uint32_t S1_GROUP = (S1_BAR + 64 + 1023) & ~1023u;     // one solve group's shared memory
+constexpr uint32_t K3_SMEM = (3 * S1_GROUP + 1024) > K2_SMEM ? (3 * S1_GROUP + 1024) : K2_SMEM;
+static_assert(K3_SMEM <= 232448, "shared memory budget");
+
+__device__ __forceinline__ void st_release(int* f, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
+}
+
+template <typename Tout>
+__global__ void __launch_bounds__(NT3, 1)
+chunk_fused_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                   const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo, ChunkArgs p,
+                   int nscan, int nitems, int* flags) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  if ((int)blockIdx.x < nscan) {
+    scan_body<Tout>(sm, &tmk, &tmv, &tmo, p, blockIdx.x % p.Nv, blockIdx.x / p.Nv, flags);
+    return;
+  }
+  const int g = threadIdx.x >> 7, tid = threadIdx.x & 127, warp = tid >> 5;
+  uint8_t* gsm = sm + g * S1_GROUP;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(gsm + S1_BAR);
+  volatile int* item_slot = reinterpret_cast<volatile int*>(gsm + S1_BAR + 32);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S1_BAR + 16);        // in group 0's slice
+  const uint32_t barid = 1 + g;
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    fence_barrier_init();
+  }
+  if (threadIdx.x < 32) tmem_alloc(tslot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tslot + 128u * (uint32_t)g;
+  int* counter = flags + nitems;
+  uint32_t ph = 0;
+  for (;;) {
+    if (tid == 0) *item_slot = atomicAdd(counter, 1);
+    named_sync(barid, 128);
+    const int item = *item_slot;
+    named_sync(barid, 128);
+    if (item >= nitems) break;
+    const bool ok = solve_item(gsm, tid, barid, bar, ph, tbase, &tmq, &tmk, p, item / p.Nv, item % p.Nv);
+    __threadfence();                       // this thread's tile stores are visible device-wide
+    named_sync(barid, 128);
+    if (tid == 0) st_release(flags + item, ok ? 1 : -1);
+    if (!ok) break;
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x < 32) tmem_dealloc(*tslot, 512);
 }
 
 // ---- host: tensor maps and launch
@@ -795,9 +907,49 @@ bool chunk_tc_supported(const ChunkArgs& p) {
   return p.Dk == DK && p.Dv == DV && p.in_bf16 && tmap_encoder() != nullptr;
 }
 
+// Workspace: the tiles of every (chunk slot, value head), then one ready flag
+// per tile and the solve groups' item counter (used by the fused launch).
 size_t chunk_tc_workspace_bytes(int num_seqs, int total, int Nv) {
-  return ((size_t)(total / CT) + (size_t)num_seqs) * (size_t)Nv * TILE_T_BYTES;
+  const size_t tiles = ((size_t)(total / CT) + (size_t)num_seqs) * (size_t)Nv;
+  return tiles * TILE_T_BYTES + ((tiles + 1) * sizeof(int) + 255) / 256 * 256;
 }
+
+namespace {
+// Per device: can one fused CTA stay resident on every SM (cooperative launch)?
+struct FusedDevice {
+  bool init = false;
+  bool ok = false;
+  int sms = 0;
+};
+std::mutex g_fused_mu;
+FusedDevice g_fused[64];
+
+bool fused_device(int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  std::lock_guard<std::mutex> lock(g_fused_mu);
+  FusedDevice& f = g_fused[dev];
+  if (!f.init) {
+    f.init = true;
+    int coop = 0, n = 0, nb0 = 0, nb1 = 0;
+    if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) == cudaSuccess && coop &&
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+        cudaFuncSetAttribute(chunk_fused_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)K3_SMEM) == cudaSuccess &&
+        cudaFuncSetAttribute(chunk_fused_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)K3_SMEM) == cudaSuccess &&
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb0, chunk_fused_kernel<bf16>, NT3, K3_SMEM) == cudaSuccess &&
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb1, chunk_fused_kernel<float>, NT3, K3_SMEM) == cudaSuccess &&
+        nb0 >= 1 && nb1 >= 1) {
+      f.ok = true;
+      f.sms = n;
+    }
+    cudaGetLastError();   // a refused query leaves no sticky error behind
+  }
+  *sms = f.sms;
+  return f.ok;
+}
+}  // namespace
 
 cudaError_t launch_chunk_tc(const ChunkArgs& p, cudaStream_t s) {
   if (p.total == 0) {
@@ -813,10 +965,25 @@ cudaError_t launch_chunk_tc(const ChunkArgs& p, cudaStream_t s) {
   if (!make_map(&mq, p.q, p.total, p.Nk * DK) || !make_map(&mk, p.k, p.total, p.Nk * DK) ||
       !make_map(&mv, p.v, p.total, p.Nv * DV))
     return cudaErrorInvalidValue;
+  const int slots = p.total / CT + p.num_seqs;
+  int sms = 0;
+  if (p.num_seqs == 1 && fused_device(&sms) && sms > p.Nv) {
+    // one sequence: solve and scan overlap in one cooperative launch
+    int nscan = p.Nv, nitems = slots * p.Nv;
+    int* flags = reinterpret_cast<int*>(static_cast<uint8_t*>(p.workspace) + (size_t)nitems * TILE_T_BYTES);
+    cudaError_t e = cudaMemsetAsync(flags, 0, (size_t)(nitems + 1) * sizeof(int), s);
+    if (e != cudaSuccess) return e;
+    CUtensorMap mo = mk;                               // fp32 rows are stored directly
+    if (p.out_bf16 && !make_map(&mo, p.o, p.total, p.Nv * DV)) return cudaErrorInvalidValue;
+    ChunkArgs pc = p;
+    void* args[] = {&mq, &mk, &mv, &mo, &pc, &nscan, &nitems, &flags};
+    const void* fn = p.out_bf16 ? reinterpret_cast<const void*>(chunk_fused_kernel<bf16>)
+                                : reinterpret_cast<const void*>(chunk_fused_kernel<float>);
+    return cudaLaunchCooperativeKernel(fn, dim3(sms), dim3(NT3), args, K3_SMEM, s);
+  }
   cudaError_t e = cudaFuncSetAttribute(chunk_solve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)S1_SMEM);
   if (e != cudaSuccess) return e;
-  const int slots = p.total / CT + p.num_seqs;
   dim3 g1(slots, p.Nv);
   chunk_solve_kernel<<<g1, 128, S1_SMEM, s>>>(mq, mk, p);
   e = cudaGetLastError();
