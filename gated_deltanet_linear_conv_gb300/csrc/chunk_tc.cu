@@ -15,17 +15,21 @@
 //   S   <- gamma_L S + (diag(exp(G_L - G)) K)^T U
 // Padding rows beyond L get beta = g = 0, which makes them exact identities.
 //
-// Two launches:
-//  * chunk_solve_kernel, parallel over every (chunk, value head): K K^T on
-//    the tensor core, A, and T = (I + A)^-1 in fp32 on CUDA cores; writes
-//    T diag(beta) and T diag(beta gamma) as bf16 128-byte-swizzled tiles to
-//    the workspace (16 KB per chunk and head).
-//  * chunk_scan_kernel, one CTA per (sequence, value head), walks the chunks
-//    with the state resident in tensor memory.  Three warpgroups run as a
-//    pipeline: PREP (TMA, Q K^T and the T products, P, the scaled Q and K
-//    tiles, W) works one chunk ahead of STATE (the S-dependent products and
-//    their epilogues), and OUT stores each chunk's output rows.  Every product
-//    is an M = 128 tcgen05.mma with Dv or Dk on the tensor-memory lanes.
+// Two parts:
+//  * the solve, independent per (chunk, value head): K K^T and Q K^T on the
+//    tensor core, A and P, T = (I + A)^-1 in fp32 on CUDA cores, and
+//    W = T diag(beta gamma) K; it writes one workspace tile per (chunk, head):
+//    [-W | diag(gamma) Q], P, the decays, and T diag(beta), as bf16 tiles in
+//    the 128-byte-swizzled layout of a TMA load;
+//  * the scan, one CTA per (sequence, value head), carries S through the
+//    chunks with S^T resident in tensor memory.  PREP (warp 0) forms
+//    [U~^T | 0]; STATE (warps 1-4) runs the S-dependent products, whose A
+//    operands (bf16 S^T and U^T) it writes back into tensor memory; OUT
+//    (warps 5-8) loads each chunk's tiles and stores the output rows.  Every
+//    product is an M = 128 tcgen05.mma with Dv on the tensor-memory lanes.
+// A single sequence runs both parts in one cooperative launch: the scan CTAs
+// take the chunks' tiles as soon as solve groups on the other SMs publish
+// them.  Packed batches run the solve kernel, then the scan kernel.
 // Every mbarrier wait is bounded; on a timeout the CTA raises the device
 // error flag, lets its outstanding copies and products land, releases its
 // tensor memory and exits.

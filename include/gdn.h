@@ -142,8 +142,16 @@ int gdn_gating(int64_t rows, int32_t num_v_heads, const void* a, const void* b, 
  * every sequence, chunk by chunk (chunks restart at each sequence start):
  *   S <- exp(g_t) S;  u = beta_t (v_t - S^T k_t);  S <- S + k_t u^T;
  *   o_t = S^T (scale * q_t),     S in [Dk, Dv] layout, fp32.
- * q, k, v are rounded to bf16 for the tensor-core products (in_dtype F32 is
- * accepted and rounded on load); accumulation and the state are fp32.
+ * bf16 q, k, v with Dk = Dv = 128 run on the tensor cores (bf16 products,
+ * fp32 accumulation and state); fp32 inputs and 64-wide heads run the fp32
+ * CUDA-core kernel of gdn_chunk_prefill_fp32.
+ *
+ * Launches: on the tensor-core path, a memset of the workspace's ready flags
+ * and then, for one sequence, a single cooperative launch (one CTA per SM;
+ * the scan of each head overlaps the solve of later chunks), or, for packed
+ * batches, a solve kernel and a scan kernel.  The workspace holds the
+ * per-(chunk, head) solve tiles and those flags; one workspace must not be
+ * shared by calls that can run at the same time.
  *
  *   q, k           [tokens, Nk, Dk]     in_dtype
  *   v              [tokens, Nv, Dv]     in_dtype
