@@ -380,10 +380,15 @@ def run_ours(args):
     kb = chunk_bytes(T, sh.Nk, sh.Nv, sh.Dk, sh.Dv)
     dbytes = decode_bytes(B, sh.Nk, sh.Nv, sh.Dk, sh.Dv)
     dec_gbs = dbytes / (ms_dec * 1e-3) / 1e9
-    traffic = None
+    traffic = None      # DRAM bytes per launch from an ncu capture of the same kernel source, else null
     tp = os.path.join(ROOT, 'profiles', 'traffic.json')
     if os.path.exists(tp):
-        traffic = json.load(open(tp)).get('chunk_prefill_t4096')
+        rec = json.load(open(tp)).get('chunk_prefill_t4096')
+        if rec:
+            import hashlib
+            with open(os.path.join(ROOT, rec['source']), 'rb') as f:
+                if hashlib.sha1(f.read()).hexdigest() == rec['source_sha1']:
+                    traffic = rec['bytes_per_launch']
     line = {
         'metric': METRIC,
         'value': ws * T / (ms_step * 1e-3),
