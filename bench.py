@@ -4,6 +4,8 @@
 A step is one pass of the whole prefill path on the prefill workload
 (B=1, T=4096, Nk=16 -> Nv=32, Dk=Dv=128, C=8192, bf16, fp32 gates/state):
 gdn_conv_gating (+ conv-state output) -> gdn_chunk_prefill -> gdn_gated_rmsnorm.
+The single call gdn_chunk_prefill_gated_norm (chunk prefill with the norm in its
+epilogue) is timed beside it.
 The fused decode step (B=256, one token each, fp32 state in place) is timed in
 the same run and reported under "decode".
 
@@ -49,15 +51,15 @@ def chunk_bytes(tokens, Nk, Nv, Dk, Dv, act=2, out=2):
     return tokens * (2 * Nk * Dk * act + Nv * Dv * act + 2 * Nv * 4 + Nv * Dv * out)
 
 
+def rmsnorm_bytes(rows, dim, act=2, out=2):
+    return rows * dim * (act + act + out) + dim * 4
+
+
 def conv_gating_bytes(tokens, num_seqs, C, Nk, Nv, Dk, Dv, act=2):
     return (tokens * (C * act + 2 * Nv * act)            # mixed_qkv, a, b
             + tokens * (2 * Nk * Dk + Nv * Dv) * act      # q, k, v out
             + tokens * Nv * 2 * 4                         # g, beta out
             + C * 4 * act + num_seqs * C * 3 * act)       # weights, conv state out
-
-
-def rmsnorm_bytes(rows, dim, act=2, out=2):
-    return rows * dim * (act + act + out) + dim * 4
 
 
 def decode_bytes(B, Nk, Nv, Dk, Dv, act=2, out=2):
@@ -260,6 +262,10 @@ def run_ours(args):
     def norm_call():
         gdn.gated_rmsnorm(bufs['o'], z, nw, 1e-6, bf, bufs['y'])
 
+    def fused_call():          # chunk prefill with the gated RMSNorm in its epilogue (reported beside)
+        gdn.chunk_prefill_gated_norm(bufs['q'], bufs['k'], bufs['v'], bufs['g'], bufs['beta'], z, nw, 1.0,
+                                     None, final_state, None, 1, 1e-6, bf, bufs['y'], bufs.get('workspace'))
+
     def prefill_step():
         conv_call()
         chunk_call()
@@ -274,7 +280,7 @@ def run_ours(args):
     # buffers, without the host's per-call marshalling in between); the L2
     # flush runs before every timed replay.
     timing = 'cuda-graph replay'
-    run = {'step': prefill_step, 'conv': conv_call, 'chunk': chunk_call, 'norm': norm_call}
+    run = {'step': prefill_step, 'conv': conv_call, 'chunk': chunk_call, 'norm': norm_call, 'fused': fused_call}
     try:
         graphs = {}
         for name, fn in run.items():
@@ -307,9 +313,12 @@ def run_ours(args):
     t_conv = timed(run['conv'])
     t_chunk = timed(run['chunk'])
     t_norm = timed(run['norm'])
+    t_fused = timed(run['fused'])
     ms_step = max_over_ranks(statistics.mean(t_step))
     # conv tile + conv state, chunk prefill (one sequence: one cooperative solve + scan launch), rmsnorm
-    launches_prefill = 4 * args.steps * 2     # the step replays, then one replay of each call
+    # conv tile + conv state, chunk prefill (one sequence: one cooperative launch), gated norm;
+    # timed: the step replays, then the replays of each call and of the fused chunk + norm call
+    launches_prefill = 4 * args.steps * 2 + args.steps
 
     # ---------------- decode workload (fused step, state in place; 512 MiB state > L2)
     del flush
@@ -374,9 +383,10 @@ def run_ours(args):
     us_chunk = statistics.mean(t_chunk) * 1e3
     us_conv = statistics.mean(t_conv) * 1e3
     us_norm = statistics.mean(t_norm) * 1e3
+    us_fused = statistics.mean(t_fused) * 1e3
+    nb = rmsnorm_bytes(T * sh.Nv, sh.Dv)
     tflops = flops / (us_chunk * 1e-6) / 1e12
     cb = conv_gating_bytes(T, 1, sh.C, sh.Nk, sh.Nv, sh.Dk, sh.Dv)
-    nb = rmsnorm_bytes(T * sh.Nv, sh.Dv)
     kb = chunk_bytes(T, sh.Nk, sh.Nv, sh.Dk, sh.Dv)
     dbytes = decode_bytes(B, sh.Nk, sh.Nv, sh.Dk, sh.Dv)
     dec_gbs = dbytes / (ms_dec * 1e-3) / 1e9
@@ -411,7 +421,8 @@ def run_ours(args):
                             'frac_hbm': cb / (us_conv * 1e-6) / 1e9 / hbm_peak, 'bytes': cb},
             'chunk_prefill': {'us': us_chunk, 'TFLOP/s': tflops, 'frac_tc': tflops / tc_peak},
             'gated_rmsnorm': {'us': us_norm, 'GB/s': nb / (us_norm * 1e-6) / 1e9,
-                              'frac_hbm': nb / (us_norm * 1e-6) / 1e9 / hbm_peak, 'bytes': nb}},
+                              'frac_hbm': nb / (us_norm * 1e-6) / 1e9 / hbm_peak, 'bytes': nb},
+            'chunk_prefill_gated_norm': {'us': us_fused, 'note': 'one call: chunk prefill with the norm in its epilogue'}},
         'decode': {'workload': 'decode_b256', 'kernel': 'gdn_decode_fused', 'steps': dsteps,
                    'us_per_step': ms_dec * 1e3, 'tokens_per_s': ws * B / (ms_dec * 1e-3),
                    'roofline': {'bound': 'hbm', 'achieved': dec_gbs, 'peak': hbm_peak, 'unit': 'GB/s',

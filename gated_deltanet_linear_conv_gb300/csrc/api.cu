@@ -253,6 +253,40 @@ int gdn_chunk_prefill(const gdn_dims* dims, const int32_t* cu_seqlens, const voi
   return GDN_OK;
 }
 
+int gdn_chunk_prefill_gated_norm(const gdn_dims* dims, const int32_t* cu_seqlens, const void* q,
+                                 const void* k, const void* v, int in_dtype, const float* g,
+                                 const float* beta, float scale, const float* initial_state,
+                                 float* final_state, const void* z, int z_dtype, const float* norm_w,
+                                 float norm_eps, void* y, int out_dtype, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  const char* fn = "gdn_chunk_prefill_gated_norm";
+  gdn::ChunkArgs p;
+  int st = chunk_common(fn, dims, cu_seqlens, q, k, v, in_dtype, g, beta, initial_state,
+                        final_state, y, out_dtype, &p);
+  if (st != GDN_OK) return st;
+  if (!valid_dtype(z_dtype)) return fail(GDN_ERR_INVALID_ARG, "%s: bad dtype", fn);
+  if (!gdn::chunk_tc_supported(p))
+    return fail(GDN_ERR_UNSUPPORTED, "%s: needs bf16 q/k/v and 128-wide heads", fn);
+  if (z_dtype != GDN_BF16) return fail(GDN_ERR_UNSUPPORTED, "%s: z must be bf16", fn);
+  REQUIRE_PTR(norm_w);
+  if (dims->total_tokens > 0) {
+    REQUIRE_PTR(z);
+    const size_t need = gdn::chunk_tc_workspace_bytes(dims->num_seqs, dims->total_tokens, dims->num_v_heads);
+    if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))
+      return fail(GDN_ERR_INVALID_ARG, "%s: workspace of %zu bytes (16-byte aligned) required, got %zu", fn,
+                  need, workspace_bytes);
+  }
+  p.scale = scale;
+  p.workspace = workspace;
+  p.workspace_bytes = workspace_bytes;
+  p.z = z;
+  p.norm_w = norm_w;
+  p.norm_eps = norm_eps;
+  cudaError_t e = gdn::launch_chunk_tc(p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  return GDN_OK;
+}
+
 int gdn_chunk_prefill_fp32(const gdn_dims* dims, const int32_t* cu_seqlens, const void* q,
                            const void* k, const void* v, int in_dtype, const float* g,
                            const float* beta, float scale, const float* initial_state,

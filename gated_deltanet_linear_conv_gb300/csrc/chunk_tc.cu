@@ -471,7 +471,8 @@ constexpr uint32_t SG_K = 32768, SG_P = 49152, SG_VEC = 57344;
 constexpr uint32_t K2_ST = 0;                          // 2 stages
 constexpr uint32_t K2_VT = 2 * STAGE_BYTES;            // 2 x [V box0 | V box1 | T diag(beta) | zeros]
 constexpr uint32_t K2_OS = K2_VT + 2 * 32768;          // 2 x output tile (two 64 x 64 boxes)
-constexpr uint32_t K2_BAR = K2_OS + 2 * 16384;
+constexpr uint32_t K2_RED = K2_OS + 2 * 16384;        // gated norm: weight (Dv floats, Dv bf16), row sums
+constexpr uint32_t K2_BAR = K2_RED + 2048;
 constexpr uint32_t K2_SMEM = K2_BAR + 256 + 1024;
 static_assert(K2_SMEM <= 232448, "shared memory budget");
 static_assert(SG_VEC + 512 <= STAGE_BYTES && WS_VEC == WS_P + 8192 && SG_VEC == SG_P + 8192, "stage layout");
@@ -491,6 +492,7 @@ struct ScanBars {
   uint64_t of[2];    // OUT finished reading a chunk's accumulator
   uint64_t fg;       // [U^T | O^T] += S^T [-W; Q~]^T complete
   uint64_t gh;       // state update complete
+  uint64_t zb[2];    // z tile of a chunk landed in its output buffer (gated norm)
   uint32_t tslot;
   int abort;
 };
@@ -503,6 +505,31 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
   }
   *abort = 1;
   return false;
+}
+
+// silu(z) = h + h tanh(h), h = z / 2, with the hardware tanh when the result is
+// rounded to bf16 (relative error about 2^-11, below half a bf16 ulp); exact division for fp32.
+__device__ __forceinline__ float tanh_hw(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+template <typename Tout> __device__ __forceinline__ float silu_out(float z);
+template <> __device__ __forceinline__ float silu_out<bf16>(float z) {
+  const float hz = 0.5f * z;
+  return fmaf(hz, tanh_hw(hz), hz);
+}
+template <> __device__ __forceinline__ float silu_out<float>(float z) { return silu_fast(z); }
+
+// w silu(z) for two bf16 z values at once, in bf16x2 arithmetic (h + h tanh(h), h = z / 2,
+// then times w): the gate of a bf16 output, whose own rounding is coarser than these steps.
+__device__ __forceinline__ uint32_t gate_bf16x2(uint32_t z2, uint32_t w2) {
+  uint32_t hz, t, s, g;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(hz) : "r"(z2), "r"(0x3F003F00u));     // z / 2
+  asm("tanh.approx.bf16x2 %0, %1;" : "=r"(t) : "r"(hz));
+  asm("fma.rn.bf16x2 %0, %1, %2, %1;" : "=r"(s) : "r"(hz), "r"(t));
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(g) : "r"(s), "r"(w2));
+  return g;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -534,7 +561,7 @@ __device__ __forceinline__ bool wait_flag(const int* f, volatile int* abort) {
 // awaited before they are loaded (the solve runs concurrently in other CTAs).
 template <typename Tout>
 __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap* tmv, const CUtensorMap* tmo,
-                          const ChunkArgs& p, int h, int s, const int* flags) {
+                          const CUtensorMap* tmz, const ChunkArgs& p, int h, int s, const int* flags) {
   ScanBars* B = reinterpret_cast<ScanBars*>(sm + K2_BAR);
   volatile int* abort = &B->abort;
 
@@ -562,6 +589,8 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
     }
     mbar_init(&B->fg, 1);
     mbar_init(&B->gh, 1);
+    mbar_init(&B->zb[0], 1);
+    mbar_init(&B->zb[1], 1);
     B->abort = 0;
     fence_barrier_init();
     prefetch_tmap(tmk);
@@ -581,22 +610,61 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
   const uint32_t lane_base = tbase + ((uint32_t)((warp & 3) * 32) << 16);
   const uint32_t sb = smem_u32(sm);
 
-  if (warp == 0) {
+  // loads of a chunk: v tiles and T diag(beta) (for [U~^T | 0]), and the stage
+  auto issue_vt = [&](int c) {
+    const int t = bos + c * CT;
+    const uint32_t vt = K2_VT + (uint32_t)(c & 1) * 32768u;
+    uint64_t* bar = &B->vt[c & 1];
+    mbar_arrive_expect_tx(bar, 2 * 8192 + 8192);
+    tma_load_2d(sm + vt, tmv, bar, h * DV, t);
+    tma_load_2d(sm + vt + 8192, tmv, bar, h * DV + 64, t);
+    bulk_load(sm + vt + 16384, ws_tile(c) + WS_TB, 8192, bar);
+    return true;
+  };
+  auto issue_stage = [&](int c) {
+    const int t = bos + c * CT;
+    const uint32_t st = K2_ST + (uint32_t)(c & 1) * STAGE_BYTES;
+    uint64_t* bar = &B->stl[c & 1];
+    const uint8_t* src = ws_tile(c);
+    mbar_arrive_expect_tx(bar, 32768 + 8192 + 512 + 2 * 8192);
+    bulk_load(sm + st, src + WS_QW, 32768, bar);
+    bulk_load(sm + st + SG_P, src + WS_P, 8192 + 512, bar);
+    tma_load_2d(sm + st + SG_K, tmk, bar, hk * DK, t);
+    tma_load_2d(sm + st + SG_K + 8192, tmk, bar, hk * DK + 64, t);
+    return true;
+  };
+  // With `flags` (the fused launch) one LOADER thread (warp 9) awaits each chunk's
+  // tiles and issues all of these loads, so no flag latency sits on PREP or OUT;
+  // otherwise PREP issues the v loads and OUT the stage loads.
+  const bool self_load = flags == nullptr;
+
+  if (warp == 9 && !self_load) {
+    // ============================== LOADER ==============================
+    if (lane == 0) {
+      int st_issued = 0, vt_issued = 0;
+      bool ok = true;
+      for (int c = 0; c < n && ok; ++c) {
+        ok = wait_flag(flags + (size_t)(slot0 + c) * p.Nv + h, abort);
+        if (ok && c >= 2) ok = wait_bar(&B->ob[c & 1], ((c - 2) >> 1) & 1, abort);      // stage free
+        if (!ok) break;
+        issue_stage(c);
+        st_issued = c + 1;
+        if (c >= 2) ok = wait_bar(&B->ready[c & 1], ((c - 2) >> 1) & 1, abort);        // v tiles free
+        if (!ok) break;
+        issue_vt(c);
+        vt_issued = c + 1;
+      }
+      if (!ok) {     // let the copies in flight land (the waits are bounded)
+        for (int k = max(st_issued - 2, 0); k < st_issued; ++k) mbar_wait(&B->stl[k & 1], (k >> 1) & 1, WAIT_LIMIT);
+        for (int k = max(vt_issued - 2, 0); k < vt_issued; ++k) mbar_wait(&B->vt[k & 1], (k >> 1) & 1, WAIT_LIMIT);
+      }
+    }
+  } else if (warp == 0) {
     // ============================== PREP ==============================
     if (lane == 0) {
-      auto issue_vt = [&](int c) -> bool {
-        if (flags != nullptr && !wait_flag(flags + (size_t)(slot0 + c) * p.Nv + h, abort)) return false;
-        const int t = bos + c * CT;
-        const uint32_t vt = K2_VT + (uint32_t)(c & 1) * 32768u;
-        uint64_t* bar = &B->vt[c & 1];
-        mbar_arrive_expect_tx(bar, 2 * 8192 + 8192);
-        tma_load_2d(sm + vt, tmv, bar, h * DV, t);
-        tma_load_2d(sm + vt + 8192, tmv, bar, h * DV + 64, t);
-        bulk_load(sm + vt + 16384, ws_tile(c) + WS_TB, 8192, bar);
-        return true;
-      };
       int issued = 0, committed = 0, c = 0;
-      while (issued < n && issued < 2 && issue_vt(issued)) ++issued;
+      if (self_load)
+        while (issued < n && issued < 2 && issue_vt(issued)) ++issued;
       bool ok = true;
       for (; c < n; ++c) {
         const int b = c & 1;
@@ -613,7 +681,7 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
           mma_bf16(tbase + TM_ACC + b * 128, av + ks * 128, bt + ks * 2, id, ks > 0 ? 1u : 0u);
         mma_commit(&B->ready[b]);
         committed = c + 1;
-        if (c + 2 < n) {
+        if (self_load && c + 2 < n) {
           ok = wait_bar(&B->ready[b], (c >> 1) & 1, abort) && issue_vt(c + 2);   // tiles b consumed
           if (!ok) break;
           issued = c + 3;
@@ -746,40 +814,132 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
     const bool leader = tid == 160;
     Tout* o = static_cast<Tout*>(p.o);
     constexpr bool kBf16Out = sizeof(Tout) == 2;
-    auto issue_stage = [&](int c) -> bool {
-      if (flags != nullptr && !wait_flag(flags + (size_t)(slot0 + c) * p.Nv + h, abort)) return false;
-      const int t = bos + c * CT;
-      const uint32_t st = K2_ST + (uint32_t)(c & 1) * STAGE_BYTES;
-      uint64_t* bar = &B->stl[c & 1];
-      const uint8_t* src = ws_tile(c);
-      mbar_arrive_expect_tx(bar, 32768 + 8192 + 512 + 2 * 8192);
-      bulk_load(sm + st, src + WS_QW, 32768, bar);
-      bulk_load(sm + st + SG_P, src + WS_P, 8192 + 512, bar);
-      tma_load_2d(sm + st + SG_K, tmk, bar, hk * DK, t);
-      tma_load_2d(sm + st + SG_K + 8192, tmk, bar, hk * DK + 64, t);
-      return true;
-    };
     int issued = 0;
-    if (leader)
+    if (leader && self_load)
       while (issued < n && issued < 2 && issue_stage(issued)) ++issued;
+    // Gated RMSNorm in the epilogue (when z is given): y = o / sqrt(mean_dv o^2 + eps) * w * silu(z);
+    // the mean over a row is a sum over this warpgroup's 128 lanes.  The z tile of a chunk
+    // arrives by TMA in the output buffer its y tile is later written over, one chunk ahead.
+    const bool norm = p.z != nullptr;
+    int zissued = 0;
+    auto issue_z = [&](int c) {
+      uint8_t* os = sm + K2_OS + (uint32_t)(c & 1) * 16384u;
+      mbar_arrive_expect_tx(&B->zb[c & 1], 16384);
+      tma_load_2d(os, tmz, &B->zb[c & 1], h * DV, bos + c * CT);
+      tma_load_2d(os + 8192, tmz, &B->zb[c & 1], h * DV + 64, bos + c * CT);
+    };
+    if (norm && leader && n > 0) {
+      issue_z(0);
+      zissued = 1;
+    }
     bool fail = false;
     int c = 0;
+    if (norm) {     // the weight as fp32 and as bf16 pairs, read by the row phase
+      reinterpret_cast<float*>(sm + K2_RED)[dv] = p.norm_w[dv];
+      reinterpret_cast<bf16*>(sm + K2_RED + 512)[dv] = __float2bfloat16_rn(p.norm_w[dv]);
+      named_sync(3, 128);
+    }
+    const int ot = tid - 160;                     // thread within OUT
     for (; c < n; ++c) {
       const int b = c & 1;
       const int c0 = bos + c * CT, len = min(CT, eos - c0);
+      const uint32_t st = K2_ST + (uint32_t)b * STAGE_BYTES;
       const bool ok = wait_bar(&B->ob[b], (c >> 1) & 1, abort);
       if (named_sync_or(3, 128, !ok)) { fail = true; break; }
       tc_fence_after();
-      if (leader && c + 2 < n && issue_stage(c + 2)) issued = c + 3;   // stage b is free now
+      if (self_load && leader && c + 2 < n && issue_stage(c + 2)) issued = c + 3;   // stage b is free now
       float v[64];
       tm_ld64(lane_base + TM_ACC + b * 128 + 64, v);   // lane dv holds O[0..63][dv]
       const bool use_tma = kBf16Out && len == CT;
-      if (use_tma && leader) bulk_wait_read<1>();     // the store of chunk c - 2 has left buffer b
+      if (leader) {
+        // the stores that read the buffers have left them (with the norm, the other
+        // buffer holds this chunk's o rows next)
+        if (!norm && use_tma) bulk_wait_read<1>();
+      }
       tc_fence_before();
       named_sync(3, 128);
       if (leader) mbar_arrive(&B->of[b]);
-      if (use_tma) {
-        uint8_t* os = sm + K2_OS + (uint32_t)b * 16384u;
+      uint8_t* os = sm + K2_OS + (uint32_t)b * 16384u;
+      if (norm) {
+        // o rows (bf16, the precision of a stored o) into the other output buffer, [r][dv] swizzled
+        uint8_t* oscr = sm + K2_OS + (uint32_t)(b ^ 1) * 16384u;
+        {
+          uint8_t* box = oscr + (dv >> 6) * 8192;
+          const uint32_t e = (uint32_t)(dv & 63);
+#pragma unroll
+          for (int r = 0; r < CT; ++r) {
+            const uint32_t off = (uint32_t)r * 128u + ((((e >> 3) ^ (uint32_t)r) & 7u) << 4) + (e & 7u) * 2u;
+            *reinterpret_cast<bf16*>(box + off) = __float2bfloat16_rn(p.scale * v[r]);
+          }
+        }
+        const bool zok = wait_bar(&B->zb[b], (c >> 1) & 1, abort);   // z of this chunk in buffer b
+        if (named_sync_or(3, 128, !zok)) { fail = true; break; }     // (also: the o rows are written)
+        // row phase: thread (r, bx) = (ot % 64, ot / 64) owns the 64 Dv columns of row r in
+        // box bx (a quarter-warp spans 8 rows of one box: conflict-free 16-byte accesses);
+        // every load is issued before the arithmetic
+        const int r = ot & 63, bx = ot >> 6;
+        const uint32_t rowoff = (uint32_t)bx * 8192u + (uint32_t)r * 128u;
+        const float* wsm = reinterpret_cast<const float*>(sm + K2_RED) + bx * 64;
+        const uint8_t* wsm2 = sm + K2_RED + 512 + bx * 128;              // bf16 pairs
+        uint4 xu[8], zu[8];
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          const uint32_t off = rowoff + ((((uint32_t)ch ^ (uint32_t)r) & 7u) << 4);
+          xu[ch] = *reinterpret_cast<const uint4*>(oscr + off);
+          zu[ch] = *reinterpret_cast<const uint4*>(os + off);
+        }
+        float ssp[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          const uint32_t w4[4] = {xu[ch].x, xu[ch].y, xu[ch].z, xu[ch].w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[i]));
+            ssp[i] = fmaf(f.x, f.x, ssp[i]);
+            ssp[i] = fmaf(f.y, f.y, ssp[i]);
+          }
+        }
+        float* part = reinterpret_cast<float*>(sm + K2_RED + 768);     // the two halves' sums
+        part[bx * 64 + r] = (ssp[0] + ssp[1]) + (ssp[2] + ssp[3]);
+        named_sync(3, 128);
+        const float inv = rsqrtf((part[r] + part[64 + r]) * (1.0f / DV) + p.norm_eps);
+        Tout* yrow = o + ((size_t)(c0 + r) * p.Nv + h) * DV + bx * 64;
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          const uint32_t off = rowoff + ((((uint32_t)ch ^ (uint32_t)r) & 7u) << 4);
+          const uint32_t xw[4] = {xu[ch].x, xu[ch].y, xu[ch].z, xu[ch].w};
+          const uint32_t zw[4] = {zu[ch].x, zu[ch].y, zu[ch].z, zu[ch].w};
+          float y[8];
+          if (kBf16Out) {
+            const uint4 wu = *reinterpret_cast<const uint4*>(wsm2 + ch * 16);
+            const uint32_t wp[4] = {wu.x, wu.y, wu.z, wu.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const uint32_t g2 = gate_bf16x2(zw[i], wp[i]);
+              const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&g2));
+              const float2 xf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xw[i]));
+              y[2 * i] = xf.x * inv * gf.x;
+              y[2 * i + 1] = xf.y * inv * gf.y;
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float2 zf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&zw[i]));
+              const float2 xf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xw[i]));
+              const int j = ch * 8 + 2 * i;
+              y[2 * i] = xf.x * inv * wsm[j] * silu_out<Tout>(zf.x);
+              y[2 * i + 1] = xf.y * inv * wsm[j + 1] * silu_out<Tout>(zf.y);
+            }
+          }
+          if (r < len) store8(yrow + ch * 8, y);   // 128 contiguous bytes per thread and row
+        }
+        fence_proxy_async_smem();      // the z tile and the o scratch are next written by the copy engine
+        named_sync(3, 128);
+        if (leader && c + 1 < n) {      // the next chunk's z goes into the scratch buffer
+          issue_z(c + 1);
+          zissued = c + 2;
+        }
+      } else if (use_tma) {
         uint8_t* box = os + (dv >> 6) * 8192;
         const uint32_t e = (uint32_t)(dv & 63);
 #pragma unroll
@@ -802,8 +962,10 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
       }
     }
     if (leader) {
-      if (fail)
+      if (fail) {
         for (int k = c; k < issued; ++k) mbar_wait(&B->stl[k & 1], (k >> 1) & 1, WAIT_LIMIT);
+        for (int k = c; k < zissued; ++k) mbar_wait(&B->zb[k & 1], (k >> 1) & 1, WAIT_LIMIT);
+      }
       bulk_wait_all();
     }
   }
@@ -817,10 +979,10 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
 template <typename Tout>
 __global__ void __launch_bounds__(NT2, 1)
 chunk_scan_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
-                  const __grid_constant__ CUtensorMap tmo, ChunkArgs p) {
+                  const __grid_constant__ CUtensorMap tmo, const __grid_constant__ CUtensorMap tmz, ChunkArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  scan_body<Tout>(sm, &tmk, &tmv, &tmo, p, blockIdx.x, blockIdx.y, nullptr);
+  scan_body<Tout>(sm, &tmk, &tmv, &tmo, &tmz, p, blockIdx.x, blockIdx.y, nullptr);
 }
 
 // ---------------------------------------------------------------------------
@@ -845,12 +1007,12 @@ __device__ __forceinline__ void st_release(int* f, int v) {
 template <typename Tout>
 __global__ void __launch_bounds__(NT3, 1)
 chunk_fused_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                   const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo, ChunkArgs p,
-                   int nscan, int nitems, int* flags) {
+                   const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo,
+                   const __grid_constant__ CUtensorMap tmz, ChunkArgs p, int nscan, int nitems, int* flags) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   if ((int)blockIdx.x < nscan) {
-    scan_body<Tout>(sm, &tmk, &tmv, &tmo, p, blockIdx.x % p.Nv, blockIdx.x / p.Nv, flags);
+    scan_body<Tout>(sm, &tmk, &tmv, &tmo, &tmz, p, blockIdx.x % p.Nv, blockIdx.x / p.Nv, flags);
     return;
   }
   const int g = threadIdx.x >> 7, tid = threadIdx.x & 127, warp = tid >> 5;
@@ -895,13 +1057,13 @@ bool make_map(CUtensorMap* map, const void* base, int rows, int cols) {
 }
 
 template <typename Tout>
-cudaError_t launch_scan(const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mo, const ChunkArgs& p,
-                        cudaStream_t s) {
+cudaError_t launch_scan(const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mo, const CUtensorMap& mz,
+                        const ChunkArgs& p, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(chunk_scan_kernel<Tout>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)K2_SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid(p.Nv, p.num_seqs);
-  chunk_scan_kernel<Tout><<<grid, NT2, K2_SMEM, s>>>(mk, mv, mo, p);
+  chunk_scan_kernel<Tout><<<grid, NT2, K2_SMEM, s>>>(mk, mv, mo, mz, p);
   return cudaGetLastError();
 }
 
@@ -969,6 +1131,8 @@ cudaError_t launch_chunk_tc(const ChunkArgs& p, cudaStream_t s) {
   if (!make_map(&mq, p.q, p.total, p.Nk * DK) || !make_map(&mk, p.k, p.total, p.Nk * DK) ||
       !make_map(&mv, p.v, p.total, p.Nv * DV))
     return cudaErrorInvalidValue;
+  CUtensorMap mz = mk;                                 // z tiles of the fused gated norm
+  if (p.z != nullptr && !make_map(&mz, p.z, p.total, p.Nv * DV)) return cudaErrorInvalidValue;
   const int slots = p.total / CT + p.num_seqs;
   int sms = 0;
   if (p.num_seqs == 1 && fused_device(&sms) && sms > p.Nv) {
@@ -980,7 +1144,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs& p, cudaStream_t s) {
     CUtensorMap mo = mk;                               // fp32 rows are stored directly
     if (p.out_bf16 && !make_map(&mo, p.o, p.total, p.Nv * DV)) return cudaErrorInvalidValue;
     ChunkArgs pc = p;
-    void* args[] = {&mq, &mk, &mv, &mo, &pc, &nscan, &nitems, &flags};
+    void* args[] = {&mq, &mk, &mv, &mo, &mz, &pc, &nscan, &nitems, &flags};
     const void* fn = p.out_bf16 ? reinterpret_cast<const void*>(chunk_fused_kernel<bf16>)
                                 : reinterpret_cast<const void*>(chunk_fused_kernel<float>);
     return cudaLaunchCooperativeKernel(fn, dim3(sms), dim3(NT3), args, K3_SMEM, s);
@@ -992,10 +1156,10 @@ cudaError_t launch_chunk_tc(const ChunkArgs& p, cudaStream_t s) {
   chunk_solve_kernel<<<g1, 128, S1_SMEM, s>>>(mq, mk, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (!p.out_bf16) return launch_scan<float>(mk, mv, mk, p, s);   // fp32 rows are stored directly
+  if (!p.out_bf16) return launch_scan<float>(mk, mv, mk, mz, p, s);   // fp32 rows are stored directly
   CUtensorMap mo;
   if (!make_map(&mo, p.o, p.total, p.Nv * DV)) return cudaErrorInvalidValue;
-  return launch_scan<bf16>(mk, mv, mo, p, s);
+  return launch_scan<bf16>(mk, mv, mo, mz, p, s);
 }
 
 // ---------------------------------------------------------------------------

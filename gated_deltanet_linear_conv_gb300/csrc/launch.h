@@ -78,6 +78,10 @@ struct ChunkArgs {
   int in_bf16, out_bf16;
   void* workspace; size_t workspace_bytes;
   int* err;
+  // gated RMSNorm fused into the output (tensor-core path): o holds y then
+  const void* z;                                 // [T, Nv, Dv] bf16, or null (plain o)
+  const float* norm_w;                           // [Dv]
+  float norm_eps;
 };
 // Portable fp32 CUDA-core implementation of the chunk form.
 cudaError_t launch_chunk_simt(const ChunkArgs& p, cudaStream_t s);

@@ -21,7 +21,8 @@ GDN_BF16, GDN_F32 = 0, 1
 
 EXPORTS = ('gdn_version', 'gdn_last_error_string', 'gdn_check_device_error', 'gdn_conv_gating',
            'gdn_gating', 'gdn_chunk_prefill_workspace_size', 'gdn_chunk_prefill',
-           'gdn_chunk_prefill_fp32', 'gdn_chunk_prefill_static', 'gdn_recurrent_decode',
+           'gdn_chunk_prefill_fp32', 'gdn_chunk_prefill_static', 'gdn_chunk_prefill_gated_norm',
+           'gdn_recurrent_decode',
            'gdn_gated_rmsnorm', 'gdn_decode_fused')
 
 
@@ -50,6 +51,8 @@ _SIGS = {
     'gdn_chunk_prefill': ([_DIMS, _P, _P, _P, _P, _I, _P, _P, _F, _P, _P, _P, _I, _P, _SZ, _P], _I),
     'gdn_chunk_prefill_fp32': ([_DIMS, _P, _P, _P, _P, _I, _P, _P, _F, _P, _P, _P, _I, _P], _I),
     'gdn_chunk_prefill_static': ([_DIMS, _P, _P, _P, _P, _I, _P, _P, _F, _P, _P, _P, _I, _P], _I),
+    'gdn_chunk_prefill_gated_norm': ([_DIMS, _P, _P, _P, _P, _I, _P, _P, _F, _P, _P, _P, _I, _P, _F, _P, _I,
+                                      _P, _SZ, _P], _I),
     'gdn_recurrent_decode': ([_DIMS, _P, _P, _P, _P, _I, _P, _P, _F, _P, _P, _I, _P], _I),
     'gdn_gated_rmsnorm': ([_I64, ctypes.c_int32, _P, _I, _P, _I, _P, _F, _P, _I, _P], _I),
     'gdn_decode_fused': ([_DIMS, _P, _I, _P, _P, _P, _P, _P, _P, _P, _F, _F, _P, _P, _P, _F,
@@ -205,6 +208,34 @@ def chunk_prefill(q, k, v, g, beta, scale=1.0, initial_state=None, final_state=N
     return o, final_state
 
 
+def chunk_prefill_gated_norm(q, k, v, g, beta, z, norm_w, scale=1.0, initial_state=None,
+                             final_state=None, cu_seqlens=None, num_seqs=1, norm_eps=1e-6,
+                             out_dtype=torch.bfloat16, y=None, workspace=None, want_final_state=True):
+    """gdn_chunk_prefill_gated_norm: chunk prefill with the gated RMSNorm fused into its
+    output.  Returns (y, final_state)."""
+    T, Nk, Dk = q.shape
+    Nv, Dv = v.shape[1], v.shape[2]
+    if cu_seqlens is not None:
+        num_seqs = cu_seqlens.numel() - 1
+    if y is None:
+        y = torch.empty(T, Nv, Dv, dtype=out_dtype, device=q.device)
+    if final_state is None and want_final_state:
+        final_state = torch.empty(num_seqs, Nv, Dk, Dv, dtype=torch.float32, device=q.device)
+    if q.dtype != k.dtype or q.dtype != v.dtype:
+        raise ValueError('q, k, v must share a dtype')
+    d = _dims(num_seqs, T, Nk, Nv, Dk, Dv)
+    ws_bytes = chunk_prefill_workspace_size(num_seqs, T, Nk, Nv, Dk, Dv)
+    if workspace is None and ws_bytes > 0:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    st = lib().gdn_chunk_prefill_gated_norm(
+        ctypes.byref(d), _ptr(cu_seqlens), _ptr(q), _ptr(k), _ptr(v), _dt(q), _ptr(_f32(g)),
+        _ptr(_f32(beta)), float(scale), _ptr(_f32(initial_state)), _ptr(_f32(final_state)), _ptr(z),
+        _dt(z), _ptr(_f32(norm_w)), float(norm_eps), _ptr(y), _dt(y), _ptr(workspace),
+        ws_bytes if workspace is not None else 0, _stream())
+    _check(st, 'gdn_chunk_prefill_gated_norm')
+    return y, final_state
+
+
 def recurrent_decode(q, k, v, g, beta, state, scale=1.0, cu_seqlens=None, num_seqs=None,
                      out_dtype=torch.bfloat16, o=None):
     """gdn_recurrent_decode: state [N, Nv, Dk, Dv] fp32 is updated in place.  Returns o."""
@@ -259,8 +290,10 @@ def mixer_prefill(mixed_qkv, conv_w, a, b, A_log, dt_bias, z, norm_w, Nk, Nv, Dk
                   cu_seqlens=None, num_seqs=1, conv_bias=None, conv_state_in=None,
                   conv_state_out=None, initial_state=None, final_state=None, q_scale=None,
                   l2_eps=1e-6, norm_eps=1e-6, act_dtype=torch.bfloat16, out_dtype=torch.bfloat16,
-                  bufs=None):
-    """The prefill path: conv_gating -> chunk_prefill -> gated_rmsnorm.
+                  bufs=None, fuse_norm=True):
+    """The prefill path: conv_gating -> chunk_prefill -> gated_rmsnorm, with the norm
+    fused into the chunk prefill's output (gdn_chunk_prefill_gated_norm) when
+    ``fuse_norm`` and the shapes run on the tensor cores (bf16, 128-wide heads).
 
     ``bufs`` (optional dict) supplies preallocated q, k, v, g, beta, o, y."""
     bufs = bufs or {}
@@ -270,6 +303,10 @@ def mixer_prefill(mixed_qkv, conv_w, a, b, A_log, dt_bias, z, norm_w, Nk, Nv, Dk
     q, k, v, g, beta = conv_gating(mixed_qkv, conv_w, a, b, A_log, dt_bias, Nk, Nv, Dk, Dv,
                                    cu_seqlens, num_seqs, conv_bias, conv_state_in, conv_state_out,
                                    q_scale, l2_eps, act_dtype, out)
+    if fuse_norm and act_dtype == torch.bfloat16 and z.dtype == torch.bfloat16 and Dk == 128 and Dv == 128:
+        return chunk_prefill_gated_norm(q, k, v, g, beta, z, norm_w, 1.0, initial_state, final_state,
+                                        cu_seqlens, num_seqs, norm_eps, out_dtype, bufs.get('y'),
+                                        bufs.get('workspace'))
     o, S = chunk_prefill(q, k, v, g, beta, 1.0, initial_state, final_state, cu_seqlens, num_seqs,
                          act_dtype, bufs.get('o'), bufs.get('workspace'))
     y = gated_rmsnorm(o, z, norm_w, norm_eps, out_dtype, bufs.get('y'))

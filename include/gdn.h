@@ -173,6 +173,30 @@ int gdn_chunk_prefill(const gdn_dims* dims, const int32_t* cu_seqlens,
                       void* o, int out_dtype,
                       void* workspace, size_t workspace_bytes, void* stream);
 
+/* ------------------------------------------------------------------------
+ * gdn_chunk_prefill_gated_norm -- steps a4 + a6 in one pass: the chunked
+ * gated delta rule of gdn_chunk_prefill followed by the gated RMSNorm of
+ * gdn_gated_rmsnorm on each (token, value head) row of its output
+ * ([RFC] 2.2 ops 4 and 6; [QDA] forward listing: core output, then
+ * self.norm(core_output, z)).  The core output o is never stored; it is
+ * rounded to bf16 (as a stored bf16 o would be) and normalised:
+ *   y[t, h] = o[t, h] / sqrt(mean(o[t, h]^2) + norm_eps) * norm_w * silu(z[t, h])
+ * Arguments as gdn_chunk_prefill, with o replaced by
+ *   z              [tokens, Nv, Dv]     bf16 (else GDN_ERR_UNSUPPORTED)
+ *   norm_w         [Dv]                 float32
+ *   norm_eps       the RMSNorm epsilon
+ *   y              [tokens, Nv, Dv]     out_dtype
+ * Tensor-core shapes only (bf16 q/k/v, Dk = Dv = 128; else
+ * GDN_ERR_UNSUPPORTED); same workspace as gdn_chunk_prefill.
+ * ------------------------------------------------------------------------ */
+int gdn_chunk_prefill_gated_norm(const gdn_dims* dims, const int32_t* cu_seqlens,
+                                 const void* q, const void* k, const void* v, int in_dtype,
+                                 const float* g, const float* beta, float scale,
+                                 const float* initial_state, float* final_state,
+                                 const void* z, int z_dtype, const float* norm_w, float norm_eps,
+                                 void* y, int out_dtype,
+                                 void* workspace, size_t workspace_bytes, void* stream);
+
 /* gdn_chunk_prefill_fp32 -- the same computation as gdn_chunk_prefill, on
  * CUDA cores in fp32 throughout (q, k, v are not rounded to bf16).  Slower;
  * for callers that want fp32 accuracy of the chunk form.  Same arguments,

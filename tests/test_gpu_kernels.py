@@ -228,7 +228,7 @@ def test_chunk_prefill_zero_state_bf16_io(fp32):
     ro, rS = O.recurrent_gated_delta_rule(np64(c.q), np64(c.k), np64(c.v), np64(gt), np64(bt),
                                           1 / math.sqrt(128))
     assert rel_l2(np64(o), ro) <= TOL_BF16
-    assert rel_l2(np64(ST), rS) <= TOL_BF16 if not fp32 else TOL_F32
+    assert rel_l2(np64(ST), rS) <= (TOL_F32 if fp32 else TOL_BF16)
 
 
 def test_chunk_in_place_state():
@@ -266,7 +266,8 @@ def test_tiny_workload_chunked_vs_recurrent():
 
 # ------------------------------------------------------------------ whole prefill path
 
-def test_mixer_prefill_small_end_to_end():
+@pytest.mark.parametrize('fuse_norm', [True, False], ids=['fused_norm', 'separate_norm'])
+def test_mixer_prefill_small_end_to_end(fuse_norm):
     shape = SHAPES[0]
     inp = I.make_mixer_inputs(51, [90, 1, 200], shape, conv_state_std=1.0, S0_std=0.05)
     sh = inp.shape
@@ -276,7 +277,7 @@ def test_mixer_prefill_small_end_to_end():
                              cuda(inp.A_log), cuda(inp.dt_bias), cuda(inp.z), cuda(inp.norm_w),
                              sh.Nk, sh.Nv, sh.Dk, sh.Dv, cu_seqlens=cuda(cu),
                              conv_state_in=cuda(inp.conv_state), conv_state_out=cs_out,
-                             initial_state=cuda(inp.S0), out_dtype=torch.float32)
+                             initial_state=cuda(inp.S0), out_dtype=torch.float32, fuse_norm=fuse_norm)
     ref = O.mixer_prefill(np64(inp.mixed_qkv), np64(inp.conv_w), np64(inp.a), np64(inp.b),
                           np64(inp.A_log), np64(inp.dt_bias), np64(inp.z), np64(inp.norm_w),
                           sh.Nk, sh.Nv, sh.Dk, sh.Dv, cu_seqlens=cu.numpy(),
@@ -284,6 +285,38 @@ def test_mixer_prefill_small_end_to_end():
     assert rel_l2(np64(y), ref['y']) <= TOL_BF16
     assert rel_l2(np64(S), ref['state']) <= TOL_BF16
     np.testing.assert_array_equal(np64(cs_out), ref['conv_state'])
+
+
+@pytest.mark.parametrize('odt', [torch.float32, torch.bfloat16], ids=['f32', 'bf16'])
+@pytest.mark.parametrize('lengths', [[300], [130, 0, 64, 7]], ids=['one_seq', 'packed'])
+def test_chunk_prefill_gated_norm(lengths, odt):
+    """Chunk prefill with the gated RMSNorm in its epilogue: against the oracle
+    (recurrence, then the norm) and against the two separate calls.  One
+    sequence runs the cooperative launch, the packed batch the two launches."""
+    shape = SHAPES[0]
+    c = I.make_core_inputs(61, lengths, shape, dtype=torch.bfloat16, S0_std=0.1)
+    gt, bt = _core_gates(c)
+    cu = c.cu_seqlens()
+    T = sum(lengths)
+    z = I.draw_normal(62, (T, shape.Nv, shape.Dv), dtype=torch.bfloat16)
+    w = I.draw_normal(63, (shape.Dv,), mean=1.0, std=0.1)
+    packed = len(lengths) > 1
+    args = (cuda(c.q), cuda(c.k), cuda(c.v), cuda(gt), cuda(bt))
+    y, ST = gdn.chunk_prefill_gated_norm(*args, cuda(z), cuda(w), 0.2, initial_state=cuda(c.S0),
+                                         cu_seqlens=cuda(cu) if packed else None, num_seqs=len(lengths),
+                                         out_dtype=odt)
+    torch.cuda.synchronize()
+    ro, rS = O.recurrent_gated_delta_rule(np64(c.q), np64(c.k), np64(c.v), np64(gt), np64(bt), 0.2,
+                                          np64(c.S0), cu.numpy())
+    ry = O.gated_rmsnorm(ro, np64(z), np64(w), 1e-6)
+    assert rel_l2(np64(y), ry) <= TOL_BF16
+    assert rel_l2(np64(ST), rS) <= TOL_BF16
+    # the fused call normalises o as a bf16 o would be stored
+    o2, _ = gdn.chunk_prefill(*args, 0.2, initial_state=cuda(c.S0), cu_seqlens=cuda(cu) if packed else None,
+                              num_seqs=len(lengths), out_dtype=torch.bfloat16)
+    y2 = gdn.gated_rmsnorm(o2, cuda(z), cuda(w), 1e-6, out_dtype=odt)
+    assert rel_l2(np64(y), np64(y2)) <= (1e-5 if odt == torch.float32 else 1e-2)
+    gdn.check_device_error()
 
 
 def test_device_error_flag_on_bad_cu_seqlens():
