@@ -329,16 +329,16 @@ int gdn_chunk_prefill_static(const gdn_dims* dims, const int32_t* cu_seqlens, co
   return GDN_OK;
 }
 
-int gdn_recurrent_decode(const gdn_dims* dims, const int32_t* cu_seqlens, const void* q,
-                         const void* k, const void* v, int in_dtype, const float* g,
-                         const float* beta, float scale, float* state, void* o, int out_dtype,
-                         void* stream) {
-  const char* fn = "gdn_recurrent_decode";
+static int recurrent_decode(const char* fn, const gdn_dims* dims, const int32_t* cu_seqlens, const void* q,
+                            const void* k, const void* v, int in_dtype, const float* g,
+                            const float* beta, float scale, float* state, float* step_states, void* o,
+                            int out_dtype, void* stream) {
   int st = check_dims(fn, dims, cu_seqlens);
   if (st != GDN_OK) return st;
   if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype))
     return fail(GDN_ERR_INVALID_ARG, "%s: bad dtype", fn);
   REQUIRE_PTR(state);
+  OPTIONAL_PTR(step_states);
   if (dims->total_tokens > 0) {
     REQUIRE_PTR(q);
     REQUIRE_PTR(k);
@@ -352,6 +352,7 @@ int gdn_recurrent_decode(const gdn_dims* dims, const int32_t* cu_seqlens, const 
   if (st != GDN_OK) return st;
   gdn::DecodeArgs p{};
   p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.state = state; p.o = o;
+  p.step_states = step_states;
   p.cu = cu_seqlens; p.num_seqs = dims->num_seqs; p.total = dims->total_tokens;
   p.Nk = dims->num_k_heads; p.Nv = dims->num_v_heads;
   p.Dk = dims->head_k_dim; p.Dv = dims->head_v_dim;
@@ -360,6 +361,24 @@ int gdn_recurrent_decode(const gdn_dims* dims, const int32_t* cu_seqlens, const 
   cudaError_t e = gdn::launch_recurrent_decode(p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, fn);
   return GDN_OK;
+}
+
+int gdn_recurrent_decode(const gdn_dims* dims, const int32_t* cu_seqlens, const void* q,
+                         const void* k, const void* v, int in_dtype, const float* g,
+                         const float* beta, float scale, float* state, void* o, int out_dtype,
+                         void* stream) {
+  return recurrent_decode("gdn_recurrent_decode", dims, cu_seqlens, q, k, v, in_dtype, g, beta, scale, state,
+                          nullptr, o, out_dtype, stream);
+}
+
+int gdn_recurrent_decode_steps(const gdn_dims* dims, const int32_t* cu_seqlens, const void* q,
+                               const void* k, const void* v, int in_dtype, const float* g,
+                               const float* beta, float scale, float* state, float* step_states, void* o,
+                               int out_dtype, void* stream) {
+  if (step_states == nullptr)
+    return fail(GDN_ERR_INVALID_ARG, "gdn_recurrent_decode_steps: step_states is NULL");
+  return recurrent_decode("gdn_recurrent_decode_steps", dims, cu_seqlens, q, k, v, in_dtype, g, beta, scale,
+                          state, step_states, o, out_dtype, stream);
 }
 
 int gdn_gated_rmsnorm(int64_t rows, int32_t dim, const void* x, int x_dtype, const void* z,

@@ -158,6 +158,8 @@ recurrent_decode_kernel(DecodeArgs p) {
     recurrent_step<DK, DV>(sm, st);
     if (threadIdx.x < DV)
       static_cast<Tout*>(p.o)[((size_t)t * p.Nv + h) * DV + threadIdx.x] = from_f32<Tout>(sm.o[threadIdx.x]);
+    if (p.step_states != nullptr)      // the state after token t (speculative-decode rollback points)
+      store_state<DK, DV>(p.step_states + ((size_t)t * p.Nv + h) * DK * DV, st);
   }
   store_state<DK, DV>(S, st);
 }

@@ -53,6 +53,7 @@ struct DecodeArgs {
   float scale;
   int in_bf16, out_bf16;
   int* err;
+  float* step_states;                            // [T, Nv, Dk, Dv] state after each token, or null
 };
 cudaError_t launch_recurrent_decode(const DecodeArgs& p, cudaStream_t s);
 

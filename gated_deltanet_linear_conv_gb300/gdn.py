@@ -22,7 +22,7 @@ GDN_BF16, GDN_F32 = 0, 1
 EXPORTS = ('gdn_version', 'gdn_last_error_string', 'gdn_check_device_error', 'gdn_conv_gating',
            'gdn_gating', 'gdn_chunk_prefill_workspace_size', 'gdn_chunk_prefill',
            'gdn_chunk_prefill_fp32', 'gdn_chunk_prefill_static', 'gdn_chunk_prefill_gated_norm',
-           'gdn_recurrent_decode',
+           'gdn_recurrent_decode', 'gdn_recurrent_decode_steps',
            'gdn_gated_rmsnorm', 'gdn_decode_fused')
 
 
@@ -54,6 +54,7 @@ _SIGS = {
     'gdn_chunk_prefill_gated_norm': ([_DIMS, _P, _P, _P, _P, _I, _P, _P, _F, _P, _P, _P, _I, _P, _F, _P, _I,
                                       _P, _SZ, _P], _I),
     'gdn_recurrent_decode': ([_DIMS, _P, _P, _P, _P, _I, _P, _P, _F, _P, _P, _I, _P], _I),
+    'gdn_recurrent_decode_steps': ([_DIMS, _P, _P, _P, _P, _I, _P, _P, _F, _P, _P, _P, _I, _P], _I),
     'gdn_gated_rmsnorm': ([_I64, ctypes.c_int32, _P, _I, _P, _I, _P, _F, _P, _I, _P], _I),
     'gdn_decode_fused': ([_DIMS, _P, _I, _P, _P, _P, _P, _P, _P, _P, _F, _F, _P, _P, _P, _F,
                           _P, _I, _P], _I),
@@ -237,8 +238,10 @@ def chunk_prefill_gated_norm(q, k, v, g, beta, z, norm_w, scale=1.0, initial_sta
 
 
 def recurrent_decode(q, k, v, g, beta, state, scale=1.0, cu_seqlens=None, num_seqs=None,
-                     out_dtype=torch.bfloat16, o=None):
-    """gdn_recurrent_decode: state [N, Nv, Dk, Dv] fp32 is updated in place.  Returns o."""
+                     out_dtype=torch.bfloat16, o=None, step_states=None):
+    """gdn_recurrent_decode: state [N, Nv, Dk, Dv] fp32 is updated in place.  Returns o.
+    With ``step_states`` ([tokens, Nv, Dk, Dv] fp32) it calls gdn_recurrent_decode_steps,
+    which also writes the state after every token."""
     T, Nk, Dk = q.shape
     Nv, Dv = v.shape[1], v.shape[2]
     if cu_seqlens is not None:
@@ -248,10 +251,14 @@ def recurrent_decode(q, k, v, g, beta, state, scale=1.0, cu_seqlens=None, num_se
     if o is None:
         o = torch.empty(T, Nv, Dv, dtype=out_dtype, device=q.device)
     d = _dims(num_seqs, T, Nk, Nv, Dk, Dv)
-    st = lib().gdn_recurrent_decode(ctypes.byref(d), _ptr(cu_seqlens), _ptr(q), _ptr(k), _ptr(v),
-                                    _dt(q), _ptr(_f32(g)), _ptr(_f32(beta)), float(scale),
-                                    _ptr(_f32(state)), _ptr(o), _dt(o), _stream())
-    _check(st, 'gdn_recurrent_decode')
+    args = (ctypes.byref(d), _ptr(cu_seqlens), _ptr(q), _ptr(k), _ptr(v), _dt(q), _ptr(_f32(g)),
+            _ptr(_f32(beta)), float(scale), _ptr(_f32(state)))
+    if step_states is None:
+        st = lib().gdn_recurrent_decode(*args, _ptr(o), _dt(o), _stream())
+        _check(st, 'gdn_recurrent_decode')
+    else:
+        st = lib().gdn_recurrent_decode_steps(*args, _ptr(_f32(step_states)), _ptr(o), _dt(o), _stream())
+        _check(st, 'gdn_recurrent_decode_steps')
     return o
 
 

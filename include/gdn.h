@@ -255,6 +255,24 @@ int gdn_recurrent_decode(const gdn_dims* dims, const int32_t* cu_seqlens,
                          float* state, void* o, int out_dtype, void* stream);
 
 /* ------------------------------------------------------------------------
+ * gdn_recurrent_decode_steps -- gdn_recurrent_decode that also writes the
+ * state after every token: the rollback points of a multi-token (draft +
+ * verify) decode step, where a caller keeps the state after the last
+ * accepted token by copying step_states[bos + j] into state.  No counterpart
+ * on the source pages beyond the multi-token decode itself ([QDA]
+ * recurrent_gated_delta_rule over several tokens).
+ *   step_states    [tokens, Nv, Dk, Dv] float32, written: the state after
+ *                  token t of its sequence (same [Dk, Dv] layout as state);
+ *                  NULL returns GDN_ERR_INVALID_ARG
+ * Other arguments and the in-place final state as gdn_recurrent_decode.
+ * ------------------------------------------------------------------------ */
+int gdn_recurrent_decode_steps(const gdn_dims* dims, const int32_t* cu_seqlens,
+                               const void* q, const void* k, const void* v, int in_dtype,
+                               const float* g, const float* beta, float scale,
+                               float* state, float* step_states, void* o, int out_dtype,
+                               void* stream);
+
+/* ------------------------------------------------------------------------
  * gdn_gated_rmsnorm -- step a6 ([RFC] 2.2 op 6, [QDA] self.norm(core, z)):
  *   y[r, :] = x[r, :] / sqrt(mean(x[r, :]^2) + eps) * w * silu(z[r, :])
  *   x [rows, dim] x_dtype; z [rows, dim] z_dtype; w [dim] float32;

@@ -144,6 +144,44 @@ def test_recurrent_decode_multi_token(shape):
     assert rel_l2(np64(state), rS) <= TOL_F32
 
 
+@pytest.mark.parametrize('shape', SHAPES, ids=['d128', 'd64'])
+def test_recurrent_decode_step_states(shape):
+    """Draft + verify decode (1 + 3 tokens per sequence): the state after every
+    token equals the recurrence over that prefix, and restarting from one of
+    them (a rollback to the last accepted token) reproduces the rest."""
+    lengths = [4, 4, 4]
+    c = I.make_core_inputs(57, lengths, shape, dtype=torch.float32, S0_std=0.1)
+    gt, bt = _core_gates(c)
+    cu = c.cu_seqlens()
+    S = cuda(c.S0.clone())
+    steps = torch.empty(sum(lengths), shape.Nv, shape.Dk, shape.Dv, device='cuda')
+    o = gdn.recurrent_decode(cuda(c.q), cuda(c.k), cuda(c.v), cuda(gt), cuda(bt), S, 0.3,
+                             cu_seqlens=cuda(cu), out_dtype=torch.float32, step_states=steps)
+    torch.cuda.synchronize()
+    cu_l = cu.tolist()
+    for s in range(len(lengths)):
+        b0, b1 = cu_l[s], cu_l[s + 1]
+        for j in range(b1 - b0):
+            sub = slice(b0, b0 + j + 1)
+            _, Sj = O.recurrent_gated_delta_rule(np64(c.q[sub]), np64(c.k[sub]), np64(c.v[sub]), np64(gt[sub]),
+                                                 np64(bt[sub]), 0.3, np64(c.S0[s:s + 1]))
+            assert rel_l2(np64(steps[b0 + j]), Sj[0]) <= TOL_F32, (s, j)
+    ro, rS = O.recurrent_gated_delta_rule(np64(c.q), np64(c.k), np64(c.v), np64(gt), np64(bt), 0.3,
+                                          np64(c.S0), cu.numpy())
+    assert rel_l2(np64(o), ro) <= TOL_F32
+    assert rel_l2(np64(S), rS) <= TOL_F32
+    for s in range(len(lengths)):
+        assert torch.equal(steps[cu_l[s + 1] - 1], S[s])        # the last step is the final state
+    # roll sequence 1 back to its second token and replay its last two tokens
+    b0 = cu_l[1]
+    S1 = steps[b0 + 1:b0 + 2].clone()
+    tail = slice(b0 + 2, b0 + 4)
+    o_tail = gdn.recurrent_decode(cuda(c.q[tail]), cuda(c.k[tail]), cuda(c.v[tail]), cuda(gt[tail]),
+                                  cuda(bt[tail]), S1, 0.3, num_seqs=1, out_dtype=torch.float32)
+    torch.testing.assert_close(o_tail, o[tail], rtol=1e-5, atol=1e-6)
+    torch.testing.assert_close(S1[0], S[1], rtol=1e-5, atol=1e-6)
+
+
 def test_gpu_gating_feeds_decode():
     """gdn_gating + gdn_recurrent_decode on the tiny workload vs the oracle."""
     c = I.workload('tiny_core_t256')

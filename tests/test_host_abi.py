@@ -77,6 +77,11 @@ def test_invalid_arguments_rejected_on_host(lib):
     st = lib.gdn_chunk_prefill_gated_norm(ctypes.byref(d), None, None, None, None, 0, None, None, 1.0, None,
                                           None, None, 0, None, 1e-6, None, 0, None, 0, None)
     assert st == E.GDN_ERR_INVALID_ARG and b'multiple' in lib.gdn_last_error_string()
+    # per-step decode states are required by the steps variant
+    d = _dims(1, 4, 2, 4, 128, 128)
+    st = lib.gdn_recurrent_decode_steps(ctypes.byref(d), None, 0x1000, 0x1000, 0x1000, 0, 0x1000, 0x1000, 1.0,
+                                        0x1000, None, 0x1000, 0, None)
+    assert st == E.GDN_ERR_INVALID_ARG and b'step_states' in lib.gdn_last_error_string()
     n = ctypes.c_size_t(99)
     assert lib.gdn_chunk_prefill_workspace_size(ctypes.byref(_dims(1, 64, 2, 4, 128, 128)),
                                                 ctypes.byref(n)) == 0
