@@ -499,6 +499,7 @@ struct ScanBars {
 
 // Bounded wait that also gives up when another role aborted.
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  if (mbar_test_wait(bar, parity)) return true;      // already complete: no suspension
   for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 1023u) == 1023u && *abort) return false;
@@ -644,15 +645,17 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
       int st_issued = 0, vt_issued = 0;
       bool ok = true;
       for (int c = 0; c < n && ok; ++c) {
+        // the v tiles first: their buffer frees (the [U~^T | 0] product of chunk c - 2) a
+        // period before the stage buffer does
         ok = wait_flag(flags + (size_t)(slot0 + c) * p.Nv + h, abort);
-        if (ok && c >= 2) ok = wait_bar(&B->ob[c & 1], ((c - 2) >> 1) & 1, abort);      // stage free
-        if (!ok) break;
-        issue_stage(c);
-        st_issued = c + 1;
-        if (c >= 2) ok = wait_bar(&B->ready[c & 1], ((c - 2) >> 1) & 1, abort);        // v tiles free
+        if (ok && c >= 2) ok = wait_bar(&B->ready[c & 1], ((c - 2) >> 1) & 1, abort);   // v tiles free
         if (!ok) break;
         issue_vt(c);
         vt_issued = c + 1;
+        if (c >= 2) ok = wait_bar(&B->ob[c & 1], ((c - 2) >> 1) & 1, abort);           // stage free
+        if (!ok) break;
+        issue_stage(c);
+        st_issued = c + 1;
       }
       if (!ok) {     // let the copies in flight land (the waits are bounded)
         for (int k = max(st_issued - 2, 0); k < st_issued; ++k) mbar_wait(&B->stl[k & 1], (k >> 1) & 1, WAIT_LIMIT);
