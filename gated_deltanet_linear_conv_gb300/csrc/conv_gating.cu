@@ -214,9 +214,12 @@ conv_gating_kernel(ConvGatingArgs p) {
 // as zeros) with the next tile's loads in flight while the current one is
 // computed.  Warp w walks 256-channel strip w % 4 (8 channels per lane,
 // 16-byte reads) down tokens 8 (w / 4) .. + 7 of the tile with a four-row
-// register ring; the loop is unrolled so the ring never moves.  Tokens in
+// register ring; the loop is unrolled so the ring never moves.  Channel pairs
+// go through the packed fp32x2 FMA (each lane holds an even/odd channel pair
+// as one float2), which rounds each half as the scalar FMA does.  Tokens in
 // the first 3 positions of a sequence are recomputed with their conv state
-// afterwards.
+// afterwards.  The gates, which depend on the token and head only, are a
+// grid-stride prologue whose loads overlap the first tile's copy.
 constexpr int TT = 16;                         // tokens per tile
 constexpr int TROWS = TT + 3;
 constexpr int RPW = TT / 2;                    // tokens per warp
@@ -238,16 +241,39 @@ template <> __device__ __forceinline__ float silu_out<bf16>(float x) {
   return fmaf(h, tanh_approx(h), h);
 }
 template <> __device__ __forceinline__ float silu_out<float>(float x) { return silu_fast(x); }
+template <typename Tout> __device__ __forceinline__ float2 silu_out2(float2 x);
+template <> __device__ __forceinline__ float2 silu_out2<bf16>(float2 x) {
+  const float2 h = __fmul2_rn(x, make_float2(0.5f, 0.5f));
+  return __ffma2_rn(h, make_float2(tanh_approx(h.x), tanh_approx(h.y)), h);
+}
+template <> __device__ __forceinline__ float2 silu_out2<float>(float2 x) {
+  return make_float2(silu_fast(x.x), silu_fast(x.y));
+}
 
-__device__ __forceinline__ void lds8(const uint8_t* p, float (&f)[8]) {
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t w) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
+}
+// 8 consecutive bf16 channels from shared memory as 4 (even, odd) pairs
+__device__ __forceinline__ void lds8x2(const uint8_t* p, float2 (&f)[4]) {
   const uint4 u = *reinterpret_cast<const uint4*>(p);
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+  f[0] = bf2_to_f2(u.x);
+  f[1] = bf2_to_f2(u.y);
+  f[2] = bf2_to_f2(u.z);
+  f[3] = bf2_to_f2(u.w);
+}
+template <typename T> __device__ __forceinline__ void store8x2(T* p, const float2 (&y)[4]) {
+  const float f[8] = {y[0].x, y[0].y, y[1].x, y[1].y, y[2].x, y[2].y, y[3].x, y[3].y};
+  store8(p, f);
+}
+// L2-normalise (times qs) a head split over `lanes_per_head` lanes of 8 channels
+__device__ __forceinline__ void l2norm8x2(float2 (&y)[4], int lanes_per_head, float eps, float qs) {
+  float2 ss2 = __fmul2_rn(y[0], y[0]);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
-    f[2 * i] = v.x;
-    f[2 * i + 1] = v.y;
-  }
+  for (int i = 1; i < 4; ++i) ss2 = __ffma2_rn(y[i], y[i], ss2);
+  const float ss = group_sum(ss2.x + ss2.y, lanes_per_head);
+  const float inv = rsqrtf(ss + eps) * qs;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) y[i] = __fmul2_rn(y[i], make_float2(inv, inv));
 }
 
 template <typename Tout>
@@ -276,8 +302,30 @@ conv_gating_tile_kernel(const __grid_constant__ CUtensorMap tmx, ConvGatingArgs 
     tc::fence_barrier_init();
     if (blockIdx.x < ntiles) issue(blockIdx.x, 0);
   }
+  // gates (token, head) in a grid-stride loop, two items per thread with both loads issued first
+  {
+    const bf16* a = static_cast<const bf16*>(p.a);
+    const bf16* b = static_cast<const bf16*>(p.b);
+    const int64_t n = (int64_t)p.total * p.Nv;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i0 < n; i0 += 2 * stride) {
+      const int64_t i1 = i0 + stride;
+      const bool has1 = i1 < n;
+      const float a0 = __bfloat162float(a[i0]), b0 = __bfloat162float(b[i0]);
+      const float a1 = has1 ? __bfloat162float(a[i1]) : 0.f, b1 = has1 ? __bfloat162float(b[i1]) : 0.f;
+      const int h0 = (int)(i0 % p.Nv);
+      p.beta[i0] = sigmoidf_(b0);
+      p.g[i0] = -expf(p.A_log[h0]) * softplusf_(a0 + p.dt_bias[h0]);
+      if (has1) {
+        const int h1 = (int)(i1 % p.Nv);
+        p.beta[i1] = sigmoidf_(b1);
+        p.g[i1] = -expf(p.A_log[h1]) * softplusf_(a1 + p.dt_bias[h1]);
+      }
+    }
+  }
   __syncthreads();
-  float wt[8][4], bias[8];
+  float2 wt[4][4], bias[4];                          // [channel pair][tap]
+  auto W = [&](int c, int j) { return (c & 1) ? wt[c >> 1][j].y : wt[c >> 1][j].x; };
   int wct = -1;                                      // channel block the weights belong to
   int k = 0;
   for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k) {
@@ -291,13 +339,20 @@ conv_gating_tile_kernel(const __grid_constant__ CUtensorMap tmx, ConvGatingArgs 
     const int region = strip0 < kd ? 0 : (strip0 < 2 * kd ? 1 : 2);
     if (ct != wct) {
       wct = ct;
+      float w8[8][4], b8[8];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) load4(static_cast<const bf16*>(p.w) + (size_t)(c0 + c) * 4, wt[c]);
+      for (int c = 0; c < 8; ++c) load4(static_cast<const bf16*>(p.w) + (size_t)(c0 + c) * 4, w8[c]);
       if (p.bias) {
-        load8(static_cast<const bf16*>(p.bias) + c0, bias);
+        load8(static_cast<const bf16*>(p.bias) + c0, b8);
       } else {
 #pragma unroll
-        for (int c = 0; c < 8; ++c) bias[c] = 0.f;
+        for (int c = 0; c < 8; ++c) b8[c] = 0.f;
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        bias[q] = make_float2(b8[2 * q], b8[2 * q + 1]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) wt[q][j] = make_float2(w8[2 * q][j], w8[2 * q + 1][j]);
       }
     }
     const bool ok = tc::mbar_wait(&bar[buf], (uint32_t)(k >> 1) & 1u, 1u << 24);
@@ -324,41 +379,34 @@ conv_gating_tile_kernel(const __grid_constant__ CUtensorMap tmx, ConvGatingArgs 
     const int r0 = RPW * half;                        // first token of this warp within the tile
     const uint8_t* rows = sm + buf * TILE_BYTES + sid * STRIP_BYTES + lane * 16 + r0 * 512;
     dst += (size_t)(t0 + r0) * row_stride;
-    float ring[4][8];
+    float2 ring[4][4];
 #pragma unroll
-    for (int j = 0; j < 3; ++j) lds8(rows + j * 512, ring[j]);
+    for (int j = 0; j < 3; ++j) lds8x2(rows + j * 512, ring[j]);
 #pragma unroll
     for (int r = 0; r < RPW; ++r) {
-      float(&cur)[8] = ring[(r + 3) & 3];
-      lds8(rows + (r + 3) * 512, cur);
+      float2(&cur)[4] = ring[(r + 3) & 3];
+      lds8x2(rows + (r + 3) * 512, cur);
       if (t0 + r0 + r < t_end) {
-        const float(&x0)[8] = ring[r & 3];
-        const float(&x1)[8] = ring[(r + 1) & 3];
-        const float(&x2)[8] = ring[(r + 2) & 3];
-        float y[8];
+        const float2(&x0)[4] = ring[r & 3];
+        const float2(&x1)[4] = ring[(r + 1) & 3];
+        const float2(&x2)[4] = ring[(r + 2) & 3];
+        float2 y[4];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          float acc = fmaf(wt[c][0], x0[c], bias[c]);
-          acc = fmaf(wt[c][1], x1[c], acc);
-          acc = fmaf(wt[c][2], x2[c], acc);
-          y[c] = silu_out<Tout>(fmaf(wt[c][3], cur[c], acc));
+        for (int q = 0; q < 4; ++q) {
+          float2 acc = __ffma2_rn(wt[q][0], x0[q], bias[q]);
+          acc = __ffma2_rn(wt[q][1], x1[q], acc);
+          acc = __ffma2_rn(wt[q][2], x2[q], acc);
+          y[q] = silu_out2<Tout>(__ffma2_rn(wt[q][3], cur[q], acc));
         }
-        if (region < 2) {
-          float ss = 0.f;
-#pragma unroll
-          for (int c = 0; c < 8; ++c) ss = fmaf(y[c], y[c], ss);
-          ss = group_sum(ss, lanes_per_head);
-          const float inv = rsqrtf(ss + p.l2_eps) * qs;
-#pragma unroll
-          for (int c = 0; c < 8; ++c) y[c] *= inv;
-        }
-        store8(dst, y);
+        if (region < 2) l2norm8x2(y, lanes_per_head, p.l2_eps, qs);
+        store8x2(dst, y);
       }
       dst += row_stride;
     }
     // tokens of this warp in the first 3 positions of a sequence: redo with the conv state
-    {
-      const int ta = t0 + r0, tb = min(t0 + r0 + RPW, t_end);
+    // (a single sequence starts at token 0 only)
+    const int ta = t0 + r0, tb = min(t0 + r0 + RPW, t_end);
+    if (p.num_seqs > 1 || ta < 3) {
       const int seq0 = find_seq(p.cu, p.num_seqs, p.total, max(ta - 3, 0));
       for (int sq = seq0; sq < p.num_seqs; ++sq) {
         const int st = seq_start(p.cu, p.num_seqs, p.total, sq);
@@ -366,10 +414,10 @@ conv_gating_tile_kernel(const __grid_constant__ CUtensorMap tmx, ConvGatingArgs 
         for (int t = max(st, ta); t < min(st + 3, tb); ++t) {
           const int seq = find_seq(p.cu, p.num_seqs, p.total, t);
           const int pos = t - seq_start(p.cu, p.num_seqs, p.total, seq);
-          float cur[8], y[8];
+          float cur[8], y8[8];
           load8(xg + (size_t)t * p.C + c0, cur);
 #pragma unroll
-          for (int c = 0; c < 8; ++c) y[c] = fmaf(wt[c][3], cur[c], bias[c]);
+          for (int c = 0; c < 8; ++c) y8[c] = fmaf(W(c, 3), cur[c], (c & 1) ? bias[c >> 1].y : bias[c >> 1].x);
 #pragma unroll
           for (int j = 0; j < 3; ++j) {
             const int si = pos + j;
@@ -382,35 +430,13 @@ conv_gating_tile_kernel(const __grid_constant__ CUtensorMap tmx, ConvGatingArgs 
               load8(xg + (size_t)(t - 3 + j) * p.C + c0, xv);
             }
 #pragma unroll
-            for (int c = 0; c < 8; ++c) y[c] = fmaf(wt[c][j], xv[c], y[c]);
+            for (int c = 0; c < 8; ++c) y8[c] = fmaf(W(c, j), xv[c], y8[c]);
           }
+          float2 y[4];
 #pragma unroll
-          for (int c = 0; c < 8; ++c) y[c] = silu_out<Tout>(y[c]);
-          if (region < 2) {
-            float ss = 0.f;
-#pragma unroll
-            for (int c = 0; c < 8; ++c) ss = fmaf(y[c], y[c], ss);
-            ss = group_sum(ss, lanes_per_head);
-            const float inv = rsqrtf(ss + p.l2_eps) * qs;
-#pragma unroll
-            for (int c = 0; c < 8; ++c) y[c] *= inv;
-          }
-          store8(dst0 + (size_t)t * row_stride, y);
-        }
-      }
-    }
-    if (region == 2) {       // gates of the strip's value heads for this warp's tokens
-      const int hps = 256 / p.Dv;
-      const int h0 = (strip0 - 2 * kd) / p.Dv;
-      const bf16* a = static_cast<const bf16*>(p.a);
-      const bf16* b = static_cast<const bf16*>(p.b);
-      for (int idx = lane; idx < RPW * hps; idx += 32) {
-        const int t = t0 + r0 + idx / hps;
-        const int h = h0 + idx % hps;
-        if (t < t_end) {
-          const size_t o = (size_t)t * p.Nv + h;
-          p.beta[o] = sigmoidf_(__bfloat162float(b[o]));
-          p.g[o] = -expf(p.A_log[h]) * softplusf_(__bfloat162float(a[o]) + p.dt_bias[h]);
+          for (int q = 0; q < 4; ++q) y[q] = make_float2(silu_out<Tout>(y8[2 * q]), silu_out<Tout>(y8[2 * q + 1]));
+          if (region < 2) l2norm8x2(y, lanes_per_head, p.l2_eps, qs);
+          store8x2(dst0 + (size_t)t * row_stride, y);
         }
       }
     }
