@@ -508,6 +508,13 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
   return false;
 }
 
+// Both phases at once: the two completed-phase tests are issued back to back.
+__device__ __forceinline__ bool wait_bar2(uint64_t* b1, uint32_t p1, uint64_t* b2, uint32_t p2, volatile int* abort) {
+  const bool t1 = mbar_test_wait(b1, p1), t2 = mbar_test_wait(b2, p2);
+  if (t1 && t2) return true;
+  return (t1 || wait_bar(b1, p1, abort)) && (t2 || wait_bar(b2, p2, abort));
+}
+
 // silu(z) = h + h tanh(h), h = z / 2, with the hardware tanh when the result is
 // rounded to bf16 (relative error about 2^-11, below half a bf16 ulp); exact division for fp32.
 __device__ __forceinline__ float tanh_hw(float x) {
@@ -710,18 +717,18 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
       }
       tmem_st_wait();
     }
-    int fg_issued = 0, gh_issued = 0;
+    int fg_issued = 0, gh_issued = 0, ob_issued = 0;
     bool fail = false;
     int c = 0;
+    // ok carries each thread's waits of the chunk before (its S^T update, and this chunk's
+    // stage and [U~^T | 0] product) into the barrier that precedes this chunk's first product
+    bool ok = n == 0 || wait_bar2(&B->stl[0], 0, &B->ready[0], 0, abort);
     for (; c < n; ++c) {
       const int b = c & 1;
       const uint32_t st = K2_ST + (uint32_t)b * STAGE_BYTES;
       const float* vec = reinterpret_cast<const float*>(sm + st + SG_VEC);   // dec[0..63], gamma_L
-      bool ok = wait_bar(&B->stl[b], (c >> 1) & 1, abort) && wait_bar(&B->ready[b], (c >> 1) & 1, abort);
-      if (named_sync_or(2, 128, !ok)) { fail = true; break; }
       tc_fence_after();
-      // E_S: bf16 copy of S^T (the A operand), then S^T <- gamma_L S^T in place
-      const float gl = vec[CT];
+      // E_S: bf16 copy of S^T (the A operand); only this sits before the product
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         float x[32], y[32], pk[32];
@@ -733,15 +740,11 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
           pk[i] = __uint_as_float(pack_bf16(x[2 * i], x[2 * i + 1]));
           pk[16 + i] = __uint_as_float(pack_bf16(y[2 * i], y[2 * i + 1]));
         }
-#pragma unroll
-        for (int i = 0; i < 32; ++i) { x[i] *= gl; y[i] *= gl; }
         tmem_st32(lane_base + TM_SB + half * 32, pk);
-        tmem_st32(lane_base + TM_S + half * 64, x);
-        tmem_st32(lane_base + TM_S + half * 64 + 32, y);
       }
       tmem_st_wait();
       tc_fence_before();
-      named_sync(2, 128);
+      if (named_sync_or(2, 128, !ok)) { fail = true; break; }
       if (leader) {
         tc_fence_after();
         // [U^T | O^T] += S^T [-W; Q~]^T
@@ -753,8 +756,24 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
         mma_commit(&B->fg);
         fg_issued = c + 1;
       }
+      // S^T <- gamma_L S^T in place while the product runs (it reads the bf16 copy; the
+      // S^T update below reads this)
+      {
+        const float gl = vec[CT];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          float x[32], y[32];
+          tmem_ld32(lane_base + TM_S + half * 64, x);
+          tmem_ld32(lane_base + TM_S + half * 64 + 32, y);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) { x[i] *= gl; y[i] *= gl; }
+          tmem_st32(lane_base + TM_S + half * 64, x);
+          tmem_st32(lane_base + TM_S + half * 64 + 32, y);
+        }
+      }
+      // each thread awaits the product itself; a failed wait is carried by the barrier below
       ok = wait_bar(&B->fg, c & 1, abort);
-      if (named_sync_or(2, 128, !ok)) { fail = true; break; }
       tc_fence_after();
       // E_U: U^T and U^T diag(dec) as bf16 pairs
       {
@@ -768,9 +787,9 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
         tmem_st32(lane_base + TM_UB, pu);
         tmem_st32(lane_base + TM_UD, pd);
       }
-      tmem_st_wait();
+      tmem_st_wait();         // also the rescaled S^T
       tc_fence_before();
-      named_sync(2, 128);
+      if (named_sync_or(2, 128, !ok)) { fail = true; break; }
       if (leader) {
         tc_fence_after();
         // S^T += (U^T diag(dec)) K: B = K tiles read MN-major
@@ -779,25 +798,34 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
 #pragma unroll
         for (int ks = 0; ks < CT / 16; ++ks) mma_bf16_ta(tbase + TM_S, tbase + TM_UD + ks * 8, bk + ks * 128, idh, 1u);
         mma_commit(&B->gh);
-        // O^T += U^T P^T
+        gh_issued = c + 1;
+      }
+      // the next chunk's stage and [U~^T | 0] product (normally complete by now) while the
+      // S^T update runs, then the update itself
+      ok = c + 1 >= n || wait_bar2(&B->stl[b ^ 1], ((c + 1) >> 1) & 1, &B->ready[b ^ 1], ((c + 1) >> 1) & 1, abort);
+      ok = ok && wait_bar(&B->gh, c & 1, abort);
+      if (leader && ok) {
+        // O^T += U^T P^T, issued behind the S^T update so that it runs while the next
+        // chunk's bf16 copy of S^T is made; the next [U^T | O^T] product's commit covers it
+        // before U^T is rewritten
+        tc_fence_after();
         const uint32_t idp = idesc_bf16(128, 64, false, false);
         const uint64_t bp = sdesc_sw128(sb + st + SG_P, 16, 1024);
 #pragma unroll
         for (int ks = 0; ks < CT / 16; ++ks)
           mma_bf16_ta(tbase + TM_ACC + b * 128 + 64, tbase + TM_UB + ks * 8, bp + ks * 2, idp, 1u);
         mma_commit(&B->ob[b]);
-        gh_issued = c + 1;
+        ob_issued = c + 1;
       }
-      ok = wait_bar(&B->gh, c & 1, abort);
-      if (named_sync_or(2, 128, !ok)) { fail = true; break; }
-      tc_fence_after();
     }
+    if (!fail) fail = named_sync_or(2, 128, !ok);     // the last chunk's waits
+    tc_fence_after();
     if (fail) {
       if (leader) {
         if (fg_issued > 0) mbar_wait(&B->fg, (fg_issued - 1) & 1, WAIT_LIMIT);
-        if (gh_issued > 0) {
-          const int k = gh_issued - 1;
-          mbar_wait(&B->gh, k & 1, WAIT_LIMIT);
+        if (gh_issued > 0) mbar_wait(&B->gh, (gh_issued - 1) & 1, WAIT_LIMIT);
+        if (ob_issued > 0) {
+          const int k = ob_issued - 1;
           mbar_wait(&B->ob[k & 1], (k >> 1) & 1, WAIT_LIMIT);
         }
       }

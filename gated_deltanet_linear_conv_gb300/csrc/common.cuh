@@ -11,6 +11,20 @@
 
 namespace gdn {
 
+// SM count of the current device, read once per device (grids of the
+// streaming kernels are sized as a multiple of it).
+inline int num_sms() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
 using bf16 = __nv_bfloat16;
 
 // Device error codes written to the sticky flag (first writer wins).

@@ -487,7 +487,7 @@ cudaError_t launch_typed(const ConvGatingArgs& p, cudaStream_t s) {
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TILE_SMEM);
       if (e != cudaSuccess) return e;
       const int ntiles = ((p.total + TT - 1) / TT) * (p.C / 1024);
-      const int blocks = std::min(ntiles, 152 * 2);
+      const int blocks = std::min(ntiles, num_sms() * 2);
       conv_gating_tile_kernel<Tout><<<blocks, 256, TILE_SMEM, s>>>(m, p);
       e = cudaGetLastError();
       if (e != cudaSuccess) return e;

@@ -4,9 +4,11 @@
 // Attention, self.norm(core_output, z)).
 //
 // Memory-bound: dim/8 lanes per row, 8 elements per lane (16-byte bf16
-// accesses), UNROLL row groups per warp iteration with every load issued
-// before the first use, shuffle reduction of the sum of squares, grid-stride
-// over rows with the grid sized to the SM count.
+// accesses), UNROLL row groups per warp iteration whose loads are all issued
+// one iteration ahead (the next rows are in flight while these are computed),
+// shuffle reduction of the sum of squares, element pairs through the packed
+// fp32x2 multiply (each half rounded as the scalar one), grid-stride over rows
+// with two resident CTAs per SM.
 
 #include "common.cuh"
 #include "launch.h"
@@ -58,7 +60,7 @@ template <> __device__ __forceinline__ float gate_silu<bf16>(float z) {
 template <> __device__ __forceinline__ float gate_silu<float>(float z) { return silu_fast(z); }
 
 template <typename Tx, typename Tz, typename Ty>
-__global__ void __launch_bounds__(256, 3)
+__global__ void __launch_bounds__(256, 2)
 gated_rmsnorm_kernel(RmsNormArgs p) {
   // rows in flight per warp step: 4 for bf16 x and z, fewer when wider types need the registers
   constexpr int UNROLL = sizeof(Tx) + sizeof(Tz) == 4 ? 4 : 2;
@@ -68,17 +70,21 @@ gated_rmsnorm_kernel(RmsNormArgs p) {
   const int lane = threadIdx.x & 31;
   const int sub = lane / lanes_per_row;
   const int col = (lane % lanes_per_row) * 8;
-  float w[8];
-  load8(p.w + col, w);
+  float2 w[4];
+  {
+    float wf[8];
+    load8(p.w + col, wf);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) w[i] = make_float2(wf[2 * i], wf[2 * i + 1]);
+  }
   const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
   const int64_t warp_id = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int64_t step = warps_total * rows_per_iter;
   const float inv_dim = 1.0f / (float)p.dim;
   const Tx* X = static_cast<const Tx*>(p.x);
   const Tz* Z = static_cast<const Tz*>(p.z);
   Ty* Y = static_cast<Ty*>(p.y);
-  for (int64_t r0 = warp_id * rows_per_iter; r0 < p.rows; r0 += warps_total * rows_per_iter) {
-    Raw8<Tx> xr[UNROLL];
-    Raw8<Tz> zr[UNROLL];
+  auto load = [&](int64_t r0, Raw8<Tx>(&xr)[UNROLL], Raw8<Tz>(&zr)[UNROLL]) {
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
       const int64_t row = r0 + u * rows_per_step + sub;
@@ -90,21 +96,46 @@ gated_rmsnorm_kernel(RmsNormArgs p) {
         zr[u].zero();
       }
     }
+  };
+  int64_t r0 = warp_id * rows_per_iter;
+  Raw8<Tx> xr[UNROLL];
+  Raw8<Tz> zr[UNROLL];
+  load(r0, xr, zr);
+  for (; r0 < p.rows; r0 += step) {
+    Raw8<Tx> xn[UNROLL];
+    Raw8<Tz> zn[UNROLL];
+    load(r0 + step, xn, zn);                 // the next rows go in flight first
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
       const int64_t row = r0 + u * rows_per_step + sub;
-      float x[8], z[8];
-      xr[u].get(x);
-      zr[u].get(z);
-      float ss = 0.f;
+      float xf[8], zf[8];
+      xr[u].get(xf);
+      zr[u].get(zf);
+      float2 x[4], z[4];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) ss = fmaf(x[c], x[c], ss);
-      ss = group_sum(ss, lanes_per_row);
+      for (int i = 0; i < 4; ++i) {
+        x[i] = make_float2(xf[2 * i], xf[2 * i + 1]);
+        z[i] = make_float2(zf[2 * i], zf[2 * i + 1]);
+      }
+      float2 ss2 = __fmul2_rn(x[0], x[0]);
+#pragma unroll
+      for (int i = 1; i < 4; ++i) ss2 = __ffma2_rn(x[i], x[i], ss2);
+      const float ss = group_sum(ss2.x + ss2.y, lanes_per_row);
       const float inv = rsqrtf(ss * inv_dim + p.eps);
+      const float2 inv2 = make_float2(inv, inv);
       float y[8];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) y[c] = x[c] * inv * w[c] * gate_silu<Ty>(z[c]);
+      for (int i = 0; i < 4; ++i) {
+        const float2 t = __fmul2_rn(__fmul2_rn(x[i], inv2), w[i]);
+        y[2 * i] = t.x * gate_silu<Ty>(z[i].x);
+        y[2 * i + 1] = t.y * gate_silu<Ty>(z[i].y);
+      }
       if (row < p.rows) store8(Y + row * p.dim + col, y);
+    }
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+      xr[u] = xn[u];
+      zr[u] = zn[u];
     }
   }
 }
@@ -122,7 +153,7 @@ cudaError_t launch_gated_rmsnorm(const RmsNormArgs& p, cudaStream_t s) {
   if (p.rows == 0) return cudaSuccess;
   const int rows_per_block = 8 * (32 / (p.dim / 8)) * 4;
   const int64_t need = (p.rows + rows_per_block - 1) / rows_per_block;
-  const int blocks = (int)std::min<int64_t>(need, 152 * 3);
+  const int blocks = (int)std::min<int64_t>(need, (int64_t)num_sms() * 2);   // two resident per SM
   if (p.x_bf16) {
     return p.z_bf16 ? launch_y<bf16, bf16>(p, s, blocks) : launch_y<bf16, float>(p, s, blocks);
   }
