@@ -41,6 +41,7 @@
 #include "tc_util.cuh"
 #include "tmap.cuh"
 
+#include <array>
 #include <mutex>
 
 namespace gdn {
@@ -297,12 +298,12 @@ __device__ bool solve_item(uint8_t* sm, int tid, uint32_t barid, uint64_t* bar, 
     tma_load_2d(sm + S1_QK + 16384, tmk, bar, hk * DK + 64, c0);
     tma_load_2d(sm + S1_QK + 24576, tmq, bar, hk * DK + 64, c0);
   }
-  {   // threads 0-63 read g, threads 64-127 read beta
-    const int r = tid & 63;
-    (tid < CT ? Gs : Bet)[r] = r < len ? (tid < CT ? p.g : p.beta)[(size_t)(c0 + r) * p.Nv + h] : 0.f;
-  }
-  for (int i = tid * 4; i < 64 * FS; i += 128 * 4)       // T starts at zero above its diagonal blocks
+  // threads 0-63 read g, threads 64-127 read beta; the zeroing of T (which starts at zero
+  // above its diagonal blocks) runs while the loads are in flight
+  const float gb = (tid & 63) < len ? (tid < CT ? p.g : p.beta)[(size_t)(c0 + (tid & 63)) * p.Nv + h] : 0.f;
+  for (int i = tid * 4; i < 64 * FS; i += 128 * 4)
     *reinterpret_cast<float4*>(TR + i) = make_float4(0.f, 0.f, 0.f, 0.f);
+  (tid < CT ? Gs : Bet)[tid & 63] = gb;
   named_sync(barid, 128);
   if (warp == 0) {
     chunk_cumsum(Gs, Gam, Dec, lane);
@@ -334,39 +335,54 @@ __device__ bool solve_item(uint8_t* sm, int tid, uint32_t barid, uint64_t* bar, 
       tm_ld64(lane_base, v);
       const int r = tid & 63;
       const float gr = Gs[r];
-      if (tid < CT) {                         // K K^T row r -> column r of A^T
-        const float br = Bet[r];
+      // e^(G_r - G_j) v_j for j < r (A^T, scaled by beta_r) or j <= r (P); the row of G is
+      // read into registers before any store, so the stores do not serialise the reads
+      const bool kk = tid < CT;
+      const float sc = kk ? Bet[r] : 1.f;
+      const int lim = kk ? r : r + 1;
 #pragma unroll
-        for (int j = 0; j < 64; ++j) AT[j * FS + r] = j < r ? br * __expf(gr - Gs[j]) * v[j] : 0.f;
-      } else {                                // Q K^T row r -> P = M o Q K^T
+      for (int jb = 0; jb < 64; jb += 16) {
+        float gj[16];
 #pragma unroll
-        for (int jb = 0; jb < 4; ++jb) {
-          if (jb * 16 <= r) {
-#pragma unroll
-            for (int j = jb * 16; j < jb * 16 + 16; ++j) v[j] = j <= r ? __expf(gr - Gs[j]) * v[j] : 0.f;
-          } else {
-#pragma unroll
-            for (int j = jb * 16; j < jb * 16 + 16; ++j) v[j] = 0.f;
-          }
+        for (int i = 0; i < 4; ++i) {
+          const float4 t = *reinterpret_cast<const float4*>(Gs + jb + 4 * i);
+          gj[4 * i] = t.x; gj[4 * i + 1] = t.y; gj[4 * i + 2] = t.z; gj[4 * i + 3] = t.w;
         }
+#pragma unroll
+        for (int j = jb; j < jb + 16; ++j) v[j] = j < lim ? sc * __expf(gr - gj[j - jb]) * v[j] : 0.f;
+      }
+      if (kk) {                               // K K^T row r -> column r of A^T
+#pragma unroll
+        for (int j = 0; j < 64; ++j) AT[j * FS + r] = v[j];
+      } else {                                // Q K^T row r -> P = M o Q K^T
         st_row64_global(ws + WS_P, r, v, 1.f);
       }
     }
     // diag(gamma) Q -> rows 64-127 of the two [-W; Q~] blocks (same swizzled rows as
     // the TMA tiles), then dec and gamma_L
-#pragma unroll 2
-    for (int i = tid; i < 1024; i += 128) {
-      const uint32_t off = (uint32_t)(i >> 9) * 16384u + (uint32_t)(i & 511) * 16u;
-      const float f = Gam[(i & 511) >> 3];
-      uint4 u = *reinterpret_cast<const uint4*>(sm + S1_QK + 8192 + off);
-      uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    {
+      uint4 qu[8];
+      float f[8];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float2 x = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w[j]));
-        __nv_bfloat162 y = __floats2bfloat162_rn(x.x * f, x.y * f);
-        w[j] = *reinterpret_cast<uint32_t*>(&y);
+      for (int k = 0; k < 8; ++k) {          // every read before the first store
+        const int i = tid + 128 * k;
+        const uint32_t off = (uint32_t)(i >> 9) * 16384u + (uint32_t)(i & 511) * 16u;
+        qu[k] = *reinterpret_cast<const uint4*>(sm + S1_QK + 8192 + off);
+        f[k] = Gam[(i & 511) >> 3];
       }
-      *reinterpret_cast<uint4*>(ws + WS_QW + 8192 + off) = make_uint4(w[0], w[1], w[2], w[3]);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int i = tid + 128 * k;
+        const uint32_t off = (uint32_t)(i >> 9) * 16384u + (uint32_t)(i & 511) * 16u;
+        uint32_t w[4] = {qu[k].x, qu[k].y, qu[k].z, qu[k].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 x = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w[j]));
+          __nv_bfloat162 y = __floats2bfloat162_rn(x.x * f[k], x.y * f[k]);
+          w[j] = *reinterpret_cast<uint32_t*>(&y);
+        }
+        *reinterpret_cast<uint4*>(ws + WS_QW + 8192 + off) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
     }
     if (tid < CT) reinterpret_cast<float*>(ws + WS_VEC)[tid] = Dec[tid];
     if (tid == 0) reinterpret_cast<float*>(ws + WS_VEC)[CT] = Gam[CT - 1];
@@ -375,26 +391,41 @@ __device__ bool solve_item(uint8_t* sm, int tid, uint32_t barid, uint64_t* bar, 
     invert_unit_lower(AT, TR, XS, tid, barid);
     // A^T is dead: its space becomes the [T diag(beta gamma); 0] operand
     uint8_t* tbg = sm + S1_AT;
-    for (int i = tid * 16; i < 8192; i += 128 * 16)
-      *reinterpret_cast<uint4*>(tbg + 8192 + i) = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll 2
-    for (int idx = tid; idx < CT * 8; idx += 128) {
-      const int r = idx >> 3, ch = idx & 7;
-      const float4 t0 = *reinterpret_cast<const float4*>(TR + r * FS + ch * 8);
-      const float4 t1 = *reinterpret_cast<const float4*>(TR + r * FS + ch * 8 + 4);
-      const float t[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
-      uint32_t wa[4], wb[4];
+    {
+      // thread (r, ch) = (tid / 8 + 16 k, tid % 8): every read of T, beta and beta gamma
+      // before the first store (the stores go over the dead A^T)
+      const int ch = tid & 7;
+      float4 t0[4], t1[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int j = ch * 8 + 2 * i;
-        __nv_bfloat162 ha = __floats2bfloat162_rn(t[2 * i] * Bet[j], t[2 * i + 1] * Bet[j + 1]);
-        __nv_bfloat162 hb = __floats2bfloat162_rn(t[2 * i] * BG[j], t[2 * i + 1] * BG[j + 1]);
-        wa[i] = *reinterpret_cast<uint32_t*>(&ha);
-        wb[i] = *reinterpret_cast<uint32_t*>(&hb);
+      for (int k = 0; k < 4; ++k) {
+        const int r = (tid >> 3) + 16 * k;
+        t0[k] = *reinterpret_cast<const float4*>(TR + r * FS + ch * 8);
+        t1[k] = *reinterpret_cast<const float4*>(TR + r * FS + ch * 8 + 4);
       }
-      const uint32_t sw = r * 128u + ((((uint32_t)ch ^ (uint32_t)(r & 7)) & 7u) << 4);
-      *reinterpret_cast<uint4*>(ws + WS_TB + sw) = make_uint4(wa[0], wa[1], wa[2], wa[3]);
-      *reinterpret_cast<uint4*>(tbg + sw) = make_uint4(wb[0], wb[1], wb[2], wb[3]);
+      const float4 be0 = *reinterpret_cast<const float4*>(Bet + ch * 8);
+      const float4 be1 = *reinterpret_cast<const float4*>(Bet + ch * 8 + 4);
+      const float4 bg0 = *reinterpret_cast<const float4*>(BG + ch * 8);
+      const float4 bg1 = *reinterpret_cast<const float4*>(BG + ch * 8 + 4);
+      const float be[8] = {be0.x, be0.y, be0.z, be0.w, be1.x, be1.y, be1.z, be1.w};
+      const float bgv[8] = {bg0.x, bg0.y, bg0.z, bg0.w, bg1.x, bg1.y, bg1.z, bg1.w};
+      for (int i = tid * 16; i < 8192; i += 128 * 16)
+        *reinterpret_cast<uint4*>(tbg + 8192 + i) = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int r = (tid >> 3) + 16 * k;
+        const float t[8] = {t0[k].x, t0[k].y, t0[k].z, t0[k].w, t1[k].x, t1[k].y, t1[k].z, t1[k].w};
+        uint32_t wa[4], wb[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          __nv_bfloat162 ha = __floats2bfloat162_rn(t[2 * i] * be[2 * i], t[2 * i + 1] * be[2 * i + 1]);
+          __nv_bfloat162 hb = __floats2bfloat162_rn(t[2 * i] * bgv[2 * i], t[2 * i + 1] * bgv[2 * i + 1]);
+          wa[i] = *reinterpret_cast<uint32_t*>(&ha);
+          wb[i] = *reinterpret_cast<uint32_t*>(&hb);
+        }
+        const uint32_t sw = r * 128u + ((((uint32_t)ch ^ (uint32_t)(r & 7)) & 7u) << 4);
+        *reinterpret_cast<uint4*>(ws + WS_TB + sw) = make_uint4(wa[0], wa[1], wa[2], wa[3]);
+        *reinterpret_cast<uint4*>(tbg + sw) = make_uint4(wb[0], wb[1], wb[2], wb[3]);
+      }
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -493,9 +524,11 @@ struct ScanBars {
   uint64_t fg;       // [U^T | O^T] += S^T [-W; Q~]^T complete
   uint64_t gh;       // state update complete
   uint64_t zb[2];    // z tile of a chunk landed in its output buffer (gated norm)
+  uint64_t ub[2];    // U^T of a chunk in tensor memory as bf16 and its S^T update issued
   uint32_t tslot;
   int abort;
 };
+static_assert(sizeof(ScanBars) <= 256, "scan barriers fit their slot");
 
 // Bounded wait that also gives up when another role aborted.
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort) {
@@ -567,7 +600,7 @@ __device__ __forceinline__ bool wait_flag(const int* f, volatile int* abort) {
 // warps may be present; they only join the final barrier).  sm is 1024-aligned
 // shared memory of K2 bytes.  With `flags`, every chunk's workspace tiles are
 // awaited before they are loaded (the solve runs concurrently in other CTAs).
-template <typename Tout>
+template <typename Tout, bool NORM>
 __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap* tmv, const CUtensorMap* tmo,
                           const CUtensorMap* tmz, const ChunkArgs& p, int h, int s, const int* flags) {
   ScanBars* B = reinterpret_cast<ScanBars*>(sm + K2_BAR);
@@ -594,6 +627,7 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
       mbar_init(&B->ready[i], 1);
       mbar_init(&B->ob[i], 1);
       mbar_init(&B->of[i], 1);
+      mbar_init(&B->ub[i], 1);
     }
     mbar_init(&B->fg, 1);
     mbar_init(&B->gh, 1);
@@ -645,6 +679,10 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
   // tiles and issues all of these loads, so no flag latency sits on PREP or OUT;
   // otherwise PREP issues the v loads and OUT the stage loads.
   const bool self_load = flags == nullptr;
+  // O^T += U^T P^T is issued by the output role, right behind the state role's S^T update;
+  // with the gated norm in the epilogue (NORM) the output role is the busier one, and the
+  // state role issues it after the update completes
+  constexpr bool out_issues_o = !NORM;
 
   if (warp == 9 && !self_load) {
     // ============================== LOADER ==============================
@@ -772,8 +810,10 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
           tmem_st32(lane_base + TM_S + half * 64 + 32, y);
         }
       }
-      // each thread awaits the product itself; a failed wait is carried by the barrier below
-      ok = wait_bar(&B->fg, c & 1, abort);
+      // each thread awaits the product itself (and the chunk before's O product, which reads
+      // the bf16 U^T rewritten below); a failed wait is carried by the barrier below
+      ok = (!out_issues_o || c == 0) ? wait_bar(&B->fg, c & 1, abort)
+                                     : wait_bar2(&B->fg, c & 1, &B->ob[(c - 1) & 1], ((c - 1) >> 1) & 1, abort);
       tc_fence_after();
       // E_U: U^T and U^T diag(dec) as bf16 pairs
       {
@@ -799,15 +839,18 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
         for (int ks = 0; ks < CT / 16; ++ks) mma_bf16_ta(tbase + TM_S, tbase + TM_UD + ks * 8, bk + ks * 128, idh, 1u);
         mma_commit(&B->gh);
         gh_issued = c + 1;
+        if (out_issues_o) {
+          tc_fence_before();
+          mbar_arrive(&B->ub[b]);     // the output role issues O^T += U^T P^T
+        }
       }
       // the next chunk's stage and [U~^T | 0] product (normally complete by now) while the
       // S^T update runs, then the update itself
       ok = c + 1 >= n || wait_bar2(&B->stl[b ^ 1], ((c + 1) >> 1) & 1, &B->ready[b ^ 1], ((c + 1) >> 1) & 1, abort);
       ok = ok && wait_bar(&B->gh, c & 1, abort);
-      if (leader && ok) {
-        // O^T += U^T P^T, issued behind the S^T update so that it runs while the next
-        // chunk's bf16 copy of S^T is made; the next [U^T | O^T] product's commit covers it
-        // before U^T is rewritten
+      if (!out_issues_o && leader && ok) {
+        // O^T += U^T P^T behind the S^T update (the next [U^T | O^T] product's commit covers
+        // it before U^T is rewritten)
         tc_fence_after();
         const uint32_t idp = idesc_bf16(128, 64, false, false);
         const uint64_t bp = sdesc_sw128(sb + st + SG_P, 16, 1024);
@@ -824,10 +867,7 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
       if (leader) {
         if (fg_issued > 0) mbar_wait(&B->fg, (fg_issued - 1) & 1, WAIT_LIMIT);
         if (gh_issued > 0) mbar_wait(&B->gh, (gh_issued - 1) & 1, WAIT_LIMIT);
-        if (ob_issued > 0) {
-          const int k = ob_issued - 1;
-          mbar_wait(&B->ob[k & 1], (k >> 1) & 1, WAIT_LIMIT);
-        }
+        if (ob_issued > 0) mbar_wait(&B->ob[(ob_issued - 1) & 1], ((ob_issued - 1) >> 1) & 1, WAIT_LIMIT);
       }
     } else if (p.ST) {
       float* dst = p.ST + ((size_t)s * p.Nv + h) * DK * DV + dv;
@@ -851,7 +891,7 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
     // Gated RMSNorm in the epilogue (when z is given): y = o / sqrt(mean_dv o^2 + eps) * w * silu(z);
     // the mean over a row is a sum over this warpgroup's 128 lanes.  The z tile of a chunk
     // arrives by TMA in the output buffer its y tile is later written over, one chunk ahead.
-    const bool norm = p.z != nullptr;
+    constexpr bool norm = NORM;
     int zissued = 0;
     auto issue_z = [&](int c) {
       uint8_t* os = sm + K2_OS + (uint32_t)(c & 1) * 16384u;
@@ -864,7 +904,7 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
       zissued = 1;
     }
     bool fail = false;
-    int c = 0;
+    int c = 0, g2_issued = 0;
     if (norm) {     // the weight as fp32 and as bf16 pairs, read by the row phase
       reinterpret_cast<float*>(sm + K2_RED)[dv] = p.norm_w[dv];
       reinterpret_cast<bf16*>(sm + K2_RED + 512)[dv] = __float2bfloat16_rn(p.norm_w[dv]);
@@ -875,7 +915,20 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
       const int b = c & 1;
       const int c0 = bos + c * CT, len = min(CT, eos - c0);
       const uint32_t st = K2_ST + (uint32_t)b * STAGE_BYTES;
-      const bool ok = wait_bar(&B->ob[b], (c >> 1) & 1, abort);
+      // O^T += U^T P^T once the state role has U^T as bf16 and its S^T update issued (the
+      // update goes first to the tensor pipe: it is on the chain to the next chunk)
+      bool ok = !out_issues_o || wait_bar(&B->ub[b], (c >> 1) & 1, abort);
+      if (out_issues_o && leader && ok) {
+        tc_fence_after();
+        const uint32_t idp = idesc_bf16(128, 64, false, false);
+        const uint64_t bp = sdesc_sw128(sb + st + SG_P, 16, 1024);
+#pragma unroll
+        for (int ks = 0; ks < CT / 16; ++ks)
+          mma_bf16_ta(tbase + TM_ACC + b * 128 + 64, tbase + TM_UB + ks * 8, bp + ks * 2, idp, 1u);
+        mma_commit(&B->ob[b]);
+        g2_issued = c + 1;
+      }
+      ok = ok && wait_bar(&B->ob[b], (c >> 1) & 1, abort);
       if (named_sync_or(3, 128, !ok)) { fail = true; break; }
       tc_fence_after();
       if (self_load && leader && c + 2 < n && issue_stage(c + 2)) issued = c + 3;   // stage b is free now
@@ -996,6 +1049,7 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
       if (fail) {
         for (int k = c; k < issued; ++k) mbar_wait(&B->stl[k & 1], (k >> 1) & 1, WAIT_LIMIT);
         for (int k = c; k < zissued; ++k) mbar_wait(&B->zb[k & 1], (k >> 1) & 1, WAIT_LIMIT);
+        if (g2_issued > 0) mbar_wait(&B->ob[(g2_issued - 1) & 1], ((g2_issued - 1) >> 1) & 1, WAIT_LIMIT);
       }
       bulk_wait_all();
     }
@@ -1007,13 +1061,13 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
   if (warp == 0) tmem_dealloc(tbase, 512);
 }
 
-template <typename Tout>
+template <typename Tout, bool NORM>
 __global__ void __launch_bounds__(NT2, 1)
 chunk_scan_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   const __grid_constant__ CUtensorMap tmo, const __grid_constant__ CUtensorMap tmz, ChunkArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  scan_body<Tout>(sm, &tmk, &tmv, &tmo, &tmz, p, blockIdx.x, blockIdx.y, nullptr);
+  scan_body<Tout, NORM>(sm, &tmk, &tmv, &tmo, &tmz, p, blockIdx.x, blockIdx.y, nullptr);
 }
 
 // ---------------------------------------------------------------------------
@@ -1035,7 +1089,7 @@ __device__ __forceinline__ void st_release(int* f, int v) {
   asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
 }
 
-template <typename Tout>
+template <typename Tout, bool NORM>
 __global__ void __launch_bounds__(NT3, 1)
 chunk_fused_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo,
@@ -1043,7 +1097,7 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   if ((int)blockIdx.x < nscan) {
-    scan_body<Tout>(sm, &tmk, &tmv, &tmo, &tmz, p, blockIdx.x % p.Nv, blockIdx.x / p.Nv, flags);
+    scan_body<Tout, NORM>(sm, &tmk, &tmv, &tmo, &tmz, p, blockIdx.x % p.Nv, blockIdx.x / p.Nv, flags);
     return;
   }
   const int g = threadIdx.x >> 7, tid = threadIdx.x & 127, warp = tid >> 5;
@@ -1090,11 +1144,11 @@ bool make_map(CUtensorMap* map, const void* base, int rows, int cols) {
 template <typename Tout>
 cudaError_t launch_scan(const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mo, const CUtensorMap& mz,
                         const ChunkArgs& p, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(chunk_scan_kernel<Tout>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)K2_SMEM);
+  const auto fn = p.z != nullptr ? chunk_scan_kernel<Tout, true> : chunk_scan_kernel<Tout, false>;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)K2_SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid(p.Nv, p.num_seqs);
-  chunk_scan_kernel<Tout><<<grid, NT2, K2_SMEM, s>>>(mk, mv, mo, mz, p);
+  fn<<<grid, NT2, K2_SMEM, s>>>(mk, mv, mo, mz, p);
   return cudaGetLastError();
 }
 
@@ -1121,6 +1175,14 @@ struct FusedDevice {
 std::mutex g_fused_mu;
 FusedDevice g_fused[64];
 
+// [bf16 out, fp32 out] x [plain, gated norm]
+std::array<const void*, 4> fused_kernels() {
+  return {reinterpret_cast<const void*>(chunk_fused_kernel<bf16, false>),
+          reinterpret_cast<const void*>(chunk_fused_kernel<bf16, true>),
+          reinterpret_cast<const void*>(chunk_fused_kernel<float, false>),
+          reinterpret_cast<const void*>(chunk_fused_kernel<float, true>)};
+}
+
 bool fused_device(int* sms) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
@@ -1128,16 +1190,15 @@ bool fused_device(int* sms) {
   FusedDevice& f = g_fused[dev];
   if (!f.init) {
     f.init = true;
-    int coop = 0, n = 0, nb0 = 0, nb1 = 0;
-    if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) == cudaSuccess && coop &&
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
-        cudaFuncSetAttribute(chunk_fused_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)K3_SMEM) == cudaSuccess &&
-        cudaFuncSetAttribute(chunk_fused_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)K3_SMEM) == cudaSuccess &&
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb0, chunk_fused_kernel<bf16>, NT3, K3_SMEM) == cudaSuccess &&
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb1, chunk_fused_kernel<float>, NT3, K3_SMEM) == cudaSuccess &&
-        nb0 >= 1 && nb1 >= 1) {
+    int coop = 0, n = 0;
+    bool ok = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) == cudaSuccess && coop &&
+              cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess;
+    for (const void* fn : fused_kernels()) {
+      int nb = 0;
+      ok = ok && cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)K3_SMEM) == cudaSuccess &&
+           cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, NT3, K3_SMEM) == cudaSuccess && nb >= 1;
+    }
+    if (ok) {
       f.ok = true;
       f.sms = n;
     }
@@ -1176,8 +1237,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs& p, cudaStream_t s) {
     if (p.out_bf16 && !make_map(&mo, p.o, p.total, p.Nv * DV)) return cudaErrorInvalidValue;
     ChunkArgs pc = p;
     void* args[] = {&mq, &mk, &mv, &mo, &mz, &pc, &nscan, &nitems, &flags};
-    const void* fn = p.out_bf16 ? reinterpret_cast<const void*>(chunk_fused_kernel<bf16>)
-                                : reinterpret_cast<const void*>(chunk_fused_kernel<float>);
+    const void* fn = fused_kernels()[(p.out_bf16 ? 0 : 2) + (p.z != nullptr ? 1 : 0)];
     return cudaLaunchCooperativeKernel(fn, dim3(sms), dim3(NT3), args, K3_SMEM, s);
   }
   cudaError_t e = cudaFuncSetAttribute(chunk_solve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -325,7 +325,6 @@ conv_gating_tile_kernel(const __grid_constant__ CUtensorMap tmx, ConvGatingArgs 
   }
   __syncthreads();
   float2 wt[4][4], bias[4];                          // [channel pair][tap]
-  auto W = [&](int c, int j) { return (c & 1) ? wt[c >> 1][j].y : wt[c >> 1][j].x; };
   int wct = -1;                                      // channel block the weights belong to
   int k = 0;
   for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k) {
@@ -417,7 +416,8 @@ conv_gating_tile_kernel(const __grid_constant__ CUtensorMap tmx, ConvGatingArgs 
           float cur[8], y8[8];
           load8(xg + (size_t)t * p.C + c0, cur);
 #pragma unroll
-          for (int c = 0; c < 8; ++c) y8[c] = fmaf(W(c, 3), cur[c], (c & 1) ? bias[c >> 1].y : bias[c >> 1].x);
+          for (int c = 0; c < 8; ++c)
+            y8[c] = fmaf((c & 1) ? wt[c >> 1][3].y : wt[c >> 1][3].x, cur[c], (c & 1) ? bias[c >> 1].y : bias[c >> 1].x);
 #pragma unroll
           for (int j = 0; j < 3; ++j) {
             const int si = pos + j;
@@ -430,7 +430,7 @@ conv_gating_tile_kernel(const __grid_constant__ CUtensorMap tmx, ConvGatingArgs 
               load8(xg + (size_t)(t - 3 + j) * p.C + c0, xv);
             }
 #pragma unroll
-            for (int c = 0; c < 8; ++c) y8[c] = fmaf(W(c, j), xv[c], y8[c]);
+            for (int c = 0; c < 8; ++c) y8[c] = fmaf((c & 1) ? wt[c >> 1][j].y : wt[c >> 1][j].x, xv[c], y8[c]);
           }
           float2 y[4];
 #pragma unroll
