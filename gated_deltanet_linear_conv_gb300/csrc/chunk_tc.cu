@@ -86,6 +86,8 @@ __device__ __forceinline__ void tm_ld64(uint32_t taddr, float (&v)[64]) {
   tmem_ld32(taddr, a);
   tmem_ld32(taddr + 32, b);
   tmem_ld_wait();
+  tmem_ld_fence(a);
+  tmem_ld_fence(b);
 #pragma unroll
   for (int i = 0; i < 32; ++i) { v[i] = a[i]; v[32 + i] = b[i]; }
 }
@@ -773,6 +775,8 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
         tmem_ld32(lane_base + TM_S + half * 64, x);
         tmem_ld32(lane_base + TM_S + half * 64 + 32, y);
         tmem_ld_wait();
+        tmem_ld_fence(x);
+        tmem_ld_fence(y);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           pk[i] = __uint_as_float(pack_bf16(x[2 * i], x[2 * i + 1]));
@@ -804,6 +808,8 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
           tmem_ld32(lane_base + TM_S + half * 64, x);
           tmem_ld32(lane_base + TM_S + half * 64 + 32, y);
           tmem_ld_wait();
+          tmem_ld_fence(x);
+          tmem_ld_fence(y);
 #pragma unroll
           for (int i = 0; i < 32; ++i) { x[i] *= gl; y[i] *= gl; }
           tmem_st32(lane_base + TM_S + half * 64, x);
@@ -876,6 +882,7 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
         float v[32];
         tmem_ld32(lane_base + TM_S + c0, v);
         tmem_ld_wait();
+        tmem_ld_fence(v);
 #pragma unroll
         for (int i = 0; i < 32; ++i) dst[(size_t)(c0 + i) * DV] = v[i];
       }
