@@ -111,7 +111,7 @@ __device__ __forceinline__ void scale_box(uint8_t* sm, uint32_t box, const float
 
 // Inclusive prefix sum of g over the chunk by one warp (lane l owns l, l+32);
 // writes G, gamma = exp(G) and dec = exp(G_L - G).
-__device__ __forceinline__ void chunk_cumsum(float* Gs, float* Gam, float* Dec, int lane) {
+__device__ __forceinline__ void chunk_cumsum(float* Gs, float* Gam, float* Dec, float* Alp, int lane) {
   float a0 = Gs[lane], a1 = Gs[lane + 32];
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -121,12 +121,17 @@ __device__ __forceinline__ void chunk_cumsum(float* Gs, float* Gam, float* Dec, 
   }
   a1 += __shfl_sync(0xffffffffu, a0, 31);
   const float gl = __shfl_sync(0xffffffffu, a1, 31);
+  // per-token factors e^(G_t - G_(t-1)): their products over t = j+1..r telescope to e^(G_r - G_j)
+  const float p0 = __shfl_up_sync(0xffffffffu, a0, 1), p1 = __shfl_up_sync(0xffffffffu, a1, 1);
+  const float a0_31 = __shfl_sync(0xffffffffu, a0, 31);
   Gs[lane] = a0;
   Gs[lane + 32] = a1;
   Gam[lane] = __expf(a0);
   Gam[lane + 32] = __expf(a1);
   Dec[lane] = __expf(gl - a0);
   Dec[lane + 32] = __expf(gl - a1);
+  Alp[lane] = lane > 0 ? __expf(a0 - p0) : __expf(a0);
+  Alp[lane + 32] = __expf(a1 - (lane > 0 ? p1 : a0_31));
 }
 
 // Workspace slot of chunk c of sequence s: floor(bos_s / 64) + s + c.  Slots
@@ -146,8 +151,8 @@ constexpr uint32_t S1_QK = 0;                       // K box0 | Q box0 | K box1 
 constexpr uint32_t S1_AT = 32768;                   // A^T fp32 [k][i]; later [T diag(beta gamma); 0] bf16
 constexpr uint32_t S1_TR = S1_AT + 64 * FS * 4;     // T fp32 [i][j]
 constexpr uint32_t S1_XS = S1_TR + 64 * FS * 4;     // block-product scratch, fp32 32 x 36
-constexpr uint32_t S1_VEC = S1_XS + 32 * 36 * 4;    // G, beta, beta*gamma, gamma, dec (5 x 64 floats)
-constexpr uint32_t S1_BAR = S1_VEC + 5 * 64 * 4;
+constexpr uint32_t S1_VEC = S1_XS + 32 * 36 * 4;    // G, beta, beta*gamma, gamma, dec, alpha (6 x 64 floats)
+constexpr uint32_t S1_BAR = S1_VEC + 6 * 64 * 4;
 constexpr uint32_t S1_SMEM = S1_BAR + 64 + 1024;
 static_assert(S1_TR % 1024 == 0 && S1_AT % 1024 == 0, "tile alignment");
 
@@ -176,23 +181,30 @@ __device__ __forceinline__ void st_row64_global(uint8_t* dst, uint32_t row, cons
 __device__ __forceinline__ void invert_unit_lower(const float* AT, float* TR, float* XS, int tid, uint32_t barid) {
   if (tid < 64) {
     const int b = (tid >> 4) * 16, c = tid & 15;
-    float x[16];
+    float2 x[8];                                       // x[i / 2] holds elements i, i + 1
 #pragma unroll
-    for (int i = 0; i < 16; ++i) x[i] = i == c ? 1.f : 0.f;
+    for (int i = 0; i < 8; ++i) x[i] = make_float2(2 * i == c ? 1.f : 0.f, 2 * i + 1 == c ? 1.f : 0.f);
 #pragma unroll
     for (int k = 0; k < 15; ++k) {
-      const float xk = x[k];
+      const float xk = (k & 1) ? x[k >> 1].y : x[k >> 1].x;
+      const float2 nxk = make_float2(-xk, -xk);
 #pragma unroll
       for (int i4 = ((k + 1) >> 2) << 2; i4 < 16; i4 += 4) {
         const float4 a = *reinterpret_cast<const float4*>(AT + (b + k) * FS + b + i4);
-        if (i4 + 0 > k) x[i4 + 0] = fmaf(-a.x, xk, x[i4 + 0]);
-        if (i4 + 1 > k) x[i4 + 1] = fmaf(-a.y, xk, x[i4 + 1]);
-        if (i4 + 2 > k) x[i4 + 2] = fmaf(-a.z, xk, x[i4 + 2]);
-        if (i4 + 3 > k) x[i4 + 3] = fmaf(-a.w, xk, x[i4 + 3]);
+#pragma unroll
+        for (int hp = 0; hp < 2; ++hp) {             // the pair (i, i + 1), i = i4 + 2 hp
+          const int i = i4 + 2 * hp;
+          const float2 ap = hp ? make_float2(a.z, a.w) : make_float2(a.x, a.y);
+          if (i > k) x[i >> 1] = __ffma2_rn(ap, nxk, x[i >> 1]);
+          else if (i + 1 > k) x[i >> 1].y = fmaf(ap.y, -xk, x[i >> 1].y);
+        }
       }
     }
 #pragma unroll
-    for (int i = 0; i < 16; ++i) TR[(b + i) * FS + b + c] = x[i];
+    for (int i = 0; i < 8; ++i) {
+      TR[(b + 2 * i) * FS + b + c] = x[i].x;
+      TR[(b + 2 * i + 1) * FS + b + c] = x[i].y;
+    }
   }
   named_sync(barid, 128);
   {   // 16 -> 32: pair pr = tid / 64, block rows R = 16 (2 pr + 1), columns C = 32 pr
@@ -200,62 +212,62 @@ __device__ __forceinline__ void invert_unit_lower(const float* AT, float* TR, fl
     const int r0 = 2 * (u >> 3), c0 = 2 * (u & 7);
     const int R = 16 * (2 * pr + 1), C = 32 * pr;
     float* X = XS + pr * 16 * 20;
-    float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
+    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);   // rows r0, r0 + 1
 #pragma unroll 4
     for (int k = 0; k < 16; ++k) {
       const float2 a = *reinterpret_cast<const float2*>(AT + (C + k) * FS + R + r0);
       const float2 t = *reinterpret_cast<const float2*>(TR + (C + k) * FS + C + c0);
-      a00 = fmaf(a.x, t.x, a00); a01 = fmaf(a.x, t.y, a01);
-      a10 = fmaf(a.y, t.x, a10); a11 = fmaf(a.y, t.y, a11);
+      acc0 = __ffma2_rn(make_float2(a.x, a.x), t, acc0);
+      acc1 = __ffma2_rn(make_float2(a.y, a.y), t, acc1);
     }
-    *reinterpret_cast<float2*>(X + r0 * 20 + c0) = make_float2(a00, a01);
-    *reinterpret_cast<float2*>(X + (r0 + 1) * 20 + c0) = make_float2(a10, a11);
+    *reinterpret_cast<float2*>(X + r0 * 20 + c0) = acc0;
+    *reinterpret_cast<float2*>(X + (r0 + 1) * 20 + c0) = acc1;
     named_sync(barid, 128);
-    a00 = a01 = a10 = a11 = 0.f;
+    acc0 = acc1 = make_float2(0.f, 0.f);
 #pragma unroll 4
     for (int k = 0; k < 16; ++k) {
       const float t0 = TR[(R + r0) * FS + R + k], t1 = TR[(R + r0 + 1) * FS + R + k];
       const float2 y = *reinterpret_cast<const float2*>(X + k * 20 + c0);
-      a00 = fmaf(t0, y.x, a00); a01 = fmaf(t0, y.y, a01);
-      a10 = fmaf(t1, y.x, a10); a11 = fmaf(t1, y.y, a11);
+      acc0 = __ffma2_rn(make_float2(t0, t0), y, acc0);
+      acc1 = __ffma2_rn(make_float2(t1, t1), y, acc1);
     }
-    *reinterpret_cast<float2*>(TR + (R + r0) * FS + C + c0) = make_float2(-a00, -a01);
-    *reinterpret_cast<float2*>(TR + (R + r0 + 1) * FS + C + c0) = make_float2(-a10, -a11);
+    *reinterpret_cast<float2*>(TR + (R + r0) * FS + C + c0) = make_float2(-acc0.x, -acc0.y);
+    *reinterpret_cast<float2*>(TR + (R + r0 + 1) * FS + C + c0) = make_float2(-acc1.x, -acc1.y);
   }
   named_sync(barid, 128);
   {   // 32 -> 64: 2 x 4 outputs per thread
     const int r0 = 2 * (tid >> 3), c0 = 4 * (tid & 7);
-    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    float2 acc[2][2] = {{make_float2(0.f, 0.f), make_float2(0.f, 0.f)}, {make_float2(0.f, 0.f), make_float2(0.f, 0.f)}};
 #pragma unroll 8
     for (int k = 0; k < 32; ++k) {
       const float2 a = *reinterpret_cast<const float2*>(AT + k * FS + 32 + r0);
       const float4 t = *reinterpret_cast<const float4*>(TR + k * FS + c0);
-      acc[0][0] = fmaf(a.x, t.x, acc[0][0]); acc[0][1] = fmaf(a.x, t.y, acc[0][1]);
-      acc[0][2] = fmaf(a.x, t.z, acc[0][2]); acc[0][3] = fmaf(a.x, t.w, acc[0][3]);
-      acc[1][0] = fmaf(a.y, t.x, acc[1][0]); acc[1][1] = fmaf(a.y, t.y, acc[1][1]);
-      acc[1][2] = fmaf(a.y, t.z, acc[1][2]); acc[1][3] = fmaf(a.y, t.w, acc[1][3]);
+      const float2 tl = make_float2(t.x, t.y), th = make_float2(t.z, t.w);
+      acc[0][0] = __ffma2_rn(make_float2(a.x, a.x), tl, acc[0][0]);
+      acc[0][1] = __ffma2_rn(make_float2(a.x, a.x), th, acc[0][1]);
+      acc[1][0] = __ffma2_rn(make_float2(a.y, a.y), tl, acc[1][0]);
+      acc[1][1] = __ffma2_rn(make_float2(a.y, a.y), th, acc[1][1]);
     }
 #pragma unroll
     for (int a = 0; a < 2; ++a)
-      *reinterpret_cast<float4*>(XS + (r0 + a) * 36 + c0) = make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
+      *reinterpret_cast<float4*>(XS + (r0 + a) * 36 + c0) = make_float4(acc[a][0].x, acc[a][0].y, acc[a][1].x, acc[a][1].y);
     named_sync(barid, 128);
 #pragma unroll
-    for (int a = 0; a < 2; ++a)
-#pragma unroll
-      for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
+    for (int a = 0; a < 2; ++a) acc[a][0] = acc[a][1] = make_float2(0.f, 0.f);
 #pragma unroll 8
     for (int k = 0; k < 32; ++k) {
       const float t0 = TR[(32 + r0) * FS + 32 + k], t1 = TR[(32 + r0 + 1) * FS + 32 + k];
       const float4 y = *reinterpret_cast<const float4*>(XS + k * 36 + c0);
-      acc[0][0] = fmaf(t0, y.x, acc[0][0]); acc[0][1] = fmaf(t0, y.y, acc[0][1]);
-      acc[0][2] = fmaf(t0, y.z, acc[0][2]); acc[0][3] = fmaf(t0, y.w, acc[0][3]);
-      acc[1][0] = fmaf(t1, y.x, acc[1][0]); acc[1][1] = fmaf(t1, y.y, acc[1][1]);
-      acc[1][2] = fmaf(t1, y.z, acc[1][2]); acc[1][3] = fmaf(t1, y.w, acc[1][3]);
+      const float2 yl = make_float2(y.x, y.y), yh = make_float2(y.z, y.w);
+      acc[0][0] = __ffma2_rn(make_float2(t0, t0), yl, acc[0][0]);
+      acc[0][1] = __ffma2_rn(make_float2(t0, t0), yh, acc[0][1]);
+      acc[1][0] = __ffma2_rn(make_float2(t1, t1), yl, acc[1][0]);
+      acc[1][1] = __ffma2_rn(make_float2(t1, t1), yh, acc[1][1]);
     }
 #pragma unroll
     for (int a = 0; a < 2; ++a)
       *reinterpret_cast<float4*>(TR + (32 + r0 + a) * FS + c0) =
-          make_float4(-acc[a][0], -acc[a][1], -acc[a][2], -acc[a][3]);
+          make_float4(-acc[a][0].x, -acc[a][0].y, -acc[a][1].x, -acc[a][1].y);
   }
   named_sync(barid, 128);
 }
@@ -275,6 +287,7 @@ __device__ bool solve_item(uint8_t* sm, int tid, uint32_t barid, uint64_t* bar, 
   float* BG = Bet + CT;
   float* Gam = BG + CT;
   float* Dec = Gam + CT;
+  float* Alp = Dec + CT;                 // e^(G_t - G_(t-1))
   const int warp = tid >> 5, lane = tid & 31;
   const int hk = h / (p.Nv / p.Nk);
 
@@ -308,7 +321,7 @@ __device__ bool solve_item(uint8_t* sm, int tid, uint32_t barid, uint64_t* bar, 
   (tid < CT ? Gs : Bet)[tid & 63] = gb;
   named_sync(barid, 128);
   if (warp == 0) {
-    chunk_cumsum(Gs, Gam, Dec, lane);
+    chunk_cumsum(Gs, Gam, Dec, Alp, lane);
     BG[lane] = Bet[lane] * Gam[lane];
     BG[lane + 32] = Bet[lane + 32] * Gam[lane + 32];
   }
@@ -335,28 +348,51 @@ __device__ bool solve_item(uint8_t* sm, int tid, uint32_t barid, uint64_t* bar, 
     {
       float v[64];
       tm_ld64(lane_base, v);
-      const int r = tid & 63;
-      const float gr = Gs[r];
-      // e^(G_r - G_j) v_j for j < r (A^T, scaled by beta_r) or j <= r (P); the row of G is
-      // read into registers before any store, so the stores do not serialise the reads
-      const bool kk = tid < CT;
-      const float sc = kk ? Bet[r] : 1.f;
-      const int lim = kk ? r : r + 1;
+      // The decay e^(G_r - G_j), j <= r, is a running product of the per-token factors
+      // (no exponential per element).
+      if (tid < CT) {
+        // K K^T is symmetric: this thread's row j of it is column j, and column j of
+        // A (A[r][j] = beta_r (k_r . k_j) e^(G_r - G_j), r > j) is row j of A^T
+        const int j = tid;
+        float cur = 1.f;
 #pragma unroll
-      for (int jb = 0; jb < 64; jb += 16) {
-        float gj[16];
+        for (int rb = 0; rb < 64; rb += 16) {
+          float al[16], be[16];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float4 t = *reinterpret_cast<const float4*>(Gs + jb + 4 * i);
-          gj[4 * i] = t.x; gj[4 * i + 1] = t.y; gj[4 * i + 2] = t.z; gj[4 * i + 3] = t.w;
+          for (int i = 0; i < 4; ++i) {
+            const float4 ta = *reinterpret_cast<const float4*>(Alp + rb + 4 * i);
+            const float4 tb = *reinterpret_cast<const float4*>(Bet + rb + 4 * i);
+            al[4 * i] = ta.x; al[4 * i + 1] = ta.y; al[4 * i + 2] = ta.z; al[4 * i + 3] = ta.w;
+            be[4 * i] = tb.x; be[4 * i + 1] = tb.y; be[4 * i + 2] = tb.z; be[4 * i + 3] = tb.w;
+          }
+#pragma unroll
+          for (int r = rb; r < rb + 16; ++r) {
+            cur = r > j ? cur * al[r - rb] : cur;
+            v[r] = r > j ? be[r - rb] * v[r] * cur : 0.f;
+          }
         }
 #pragma unroll
-        for (int j = jb; j < jb + 16; ++j) v[j] = j < lim ? sc * __expf(gr - gj[j - jb]) * v[j] : 0.f;
-      }
-      if (kk) {                               // K K^T row r -> column r of A^T
+        for (int r = 0; r < 64; r += 4)
+          *reinterpret_cast<float4*>(AT + j * FS + r) = make_float4(v[r], v[r + 1], v[r + 2], v[r + 3]);
+      } else {
+        // row r of P = M o Q K^T: (q_r . k_j) e^(G_r - G_j) for j <= r, the product taken from j = r down
+        const int r = tid - CT;
+        float cur = 1.f;
 #pragma unroll
-        for (int j = 0; j < 64; ++j) AT[j * FS + r] = v[j];
-      } else {                                // Q K^T row r -> P = M o Q K^T
+        for (int jb = 48; jb >= 0; jb -= 16) {
+          float al[17];                       // alpha[jb + 1 .. jb + 16]
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float4 ta = *reinterpret_cast<const float4*>(Alp + jb + 4 * i);
+            al[4 * i] = ta.x; al[4 * i + 1] = ta.y; al[4 * i + 2] = ta.z; al[4 * i + 3] = ta.w;
+          }
+          al[16] = jb + 16 < 64 ? Alp[jb + 16] : 1.f;
+#pragma unroll
+          for (int j = jb + 15; j >= jb; --j) {
+            cur = j < r ? cur * al[j + 1 - jb] : cur;
+            v[j] = j <= r ? v[j] * cur : 0.f;
+          }
+        }
         st_row64_global(ws + WS_P, r, v, 1.f);
       }
     }
