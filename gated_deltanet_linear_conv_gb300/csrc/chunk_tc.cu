@@ -586,8 +586,11 @@ __device__ __forceinline__ bool wait_bar2(uint64_t* b1, uint32_t p1, uint64_t* b
   return (t1 || wait_bar(b1, p1, abort)) && (t2 || wait_bar(b2, p2, abort));
 }
 
-// silu(z) = h + h tanh(h), h = z / 2, with the hardware tanh when the result is
-// rounded to bf16 (relative error about 2^-11, below half a bf16 ulp); exact division for fp32.
+// silu(z) = h + h tanh(h), h = z / 2, with the hardware tanh when the result is rounded
+// to bf16, exact division for fp32.  The tanh's relative error (about 2^-11) leaves silu an
+// absolute error of at most about 2^-11 |h|: within half a bf16 ulp of the result for z >= -2;
+// below that silu is near zero and the error, though still far below the bf16 rounding of
+// O(1) values, is no longer small relative to the result itself.
 __device__ __forceinline__ float tanh_hw(float x) {
   float y;
   asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -233,8 +233,11 @@ __device__ __forceinline__ float tanh_approx(float x) {
   return y;
 }
 // SiLU for the tiled path: x sigmoid(x) = h + h tanh(h), h = x / 2, with the
-// hardware tanh when the result is rounded to bf16 anyway (its relative error,
-// about 2^-11, stays below half a bf16 ulp); the exact-division form for fp32.
+// hardware tanh when the result is rounded to bf16, the exact-division form for
+// fp32.  The tanh's relative error (about 2^-11) gives an absolute error of at
+// most about 2^-11 |h|: within half a bf16 ulp of the result for x >= -2; for
+// more negative x silu is near zero and the error, still far below the bf16
+// rounding of O(1) values, is no longer small relative to the result.
 template <typename Tout> __device__ __forceinline__ float silu_out(float x);
 template <> __device__ __forceinline__ float silu_out<bf16>(float x) {
   const float h = 0.5f * x;

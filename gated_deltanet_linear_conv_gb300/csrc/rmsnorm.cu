@@ -51,7 +51,10 @@ __device__ __forceinline__ float tanh_approx(float x) {
   return y;
 }
 // silu(z) = h + h tanh(h), h = z / 2: the hardware tanh when y is rounded to
-// bf16 (relative error about 2^-11, below half a bf16 ulp), exact division for fp32.
+// bf16, exact division for fp32.  The tanh's relative error (about 2^-11) gives
+// an absolute error of at most about 2^-11 |h|: within half a bf16 ulp of the
+// result for z >= -2; for more negative z silu is near zero and the error, still
+// far below the bf16 rounding of O(1) values, is no longer small relative to it.
 template <typename Ty> __device__ __forceinline__ float gate_silu(float z);
 template <> __device__ __forceinline__ float gate_silu<bf16>(float z) {
   const float h = 0.5f * z;
