@@ -148,7 +148,7 @@ __device__ __forceinline__ int slot_base(const ChunkArgs& p, int s) {
 // ---------------------------------------------------------------------------
 constexpr int FS = 68;                              // fp32 row stride: 16-byte rows, conflict-free columns
 constexpr uint32_t S1_QK = 0;                       // K box0 | Q box0 | K box1 | Q box1 (32 KB)
-constexpr uint32_t S1_AT = 32768;                   // A^T fp32 [k][i]; later [T diag(beta gamma); 0] bf16
+constexpr uint32_t S1_AT = 32768;                   // A^T fp32 [k][i]; later [T diag(beta gamma)] twice, bf16
 constexpr uint32_t S1_TR = S1_AT + 64 * FS * 4;     // T fp32 [i][j]
 constexpr uint32_t S1_XS = S1_TR + 64 * FS * 4;     // block-product scratch, fp32 32 x 36
 constexpr uint32_t S1_VEC = S1_XS + 32 * 36 * 4;    // G, beta, beta*gamma, gamma, dec, alpha (6 x 64 floats)
@@ -427,7 +427,8 @@ __device__ bool solve_item(uint8_t* sm, int tid, uint32_t barid, uint64_t* bar, 
     tc_fence_before();
     named_sync(barid, 128);
     invert_unit_lower(AT, TR, XS, tid, barid);
-    // A^T is dead: its space becomes the [T diag(beta gamma); 0] operand
+    // A^T is dead: its space becomes the [T diag(beta gamma); T diag(beta gamma)] operand (the
+    // rows twice, so that all four warps take a share of W out of tensor memory)
     uint8_t* tbg = sm + S1_AT;
     {
       // thread (r, ch) = (tid / 8 + 16 k, tid % 8): every read of T, beta and beta gamma
@@ -446,8 +447,6 @@ __device__ bool solve_item(uint8_t* sm, int tid, uint32_t barid, uint64_t* bar, 
       const float4 bg1 = *reinterpret_cast<const float4*>(BG + ch * 8 + 4);
       const float be[8] = {be0.x, be0.y, be0.z, be0.w, be1.x, be1.y, be1.z, be1.w};
       const float bgv[8] = {bg0.x, bg0.y, bg0.z, bg0.w, bg1.x, bg1.y, bg1.z, bg1.w};
-      for (int i = tid * 16; i < 8192; i += 128 * 16)
-        *reinterpret_cast<uint4*>(tbg + 8192 + i) = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int r = (tid >> 3) + 16 * k;
@@ -463,6 +462,7 @@ __device__ bool solve_item(uint8_t* sm, int tid, uint32_t barid, uint64_t* bar, 
         const uint32_t sw = r * 128u + ((((uint32_t)ch ^ (uint32_t)(r & 7)) & 7u) << 4);
         *reinterpret_cast<uint4*>(ws + WS_TB + sw) = make_uint4(wa[0], wa[1], wa[2], wa[3]);
         *reinterpret_cast<uint4*>(tbg + sw) = make_uint4(wb[0], wb[1], wb[2], wb[3]);
+        *reinterpret_cast<uint4*>(tbg + 8192 + sw) = make_uint4(wb[0], wb[1], wb[2], wb[3]);
       }
     }
     fence_proxy_async_smem();
@@ -470,7 +470,7 @@ __device__ bool solve_item(uint8_t* sm, int tid, uint32_t barid, uint64_t* bar, 
     named_sync(barid, 128);
     tc_fence_after();
     if (tid == 0) {
-      // W = [T diag(beta gamma); 0] K  (rows 0-63 of the 128 x 128 result)
+      // W = T diag(beta gamma) K, in rows 0-63 and again in rows 64-127 of the 128 x 128 result
       const uint32_t id = idesc_bf16(128, 128, false, true);
       const uint64_t a = sdesc_sw128(sb + S1_AT, 16, 1024);
       const uint64_t b = sdesc_sw128(sb + S1_QK, 16384, 1024);
@@ -481,13 +481,11 @@ __device__ bool solve_item(uint8_t* sm, int tid, uint32_t barid, uint64_t* bar, 
     ok = mbar_wait(bar, ph & 1u, WAIT_LIMIT);
     if (!named_sync_or(barid, 128, !ok)) {
       tc_fence_after();
-      if (warp < 2) {
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          float v[64];
-          tm_ld64(lane_base + half * 64, v);
-          st_row64_global(ws + WS_QW + half * 16384, tid, v, -1.f);
-        }
+      {   // warps 0-1: columns 0-63 of rows 0-63; warps 2-3: columns 64-127 of the copy
+        const int half = tid >> 6;
+        float v[64];
+        tm_ld64(lane_base + half * 64, v);
+        st_row64_global(ws + WS_QW + half * 16384, tid & 63, v, -1.f);
       }
       done = true;
     }
