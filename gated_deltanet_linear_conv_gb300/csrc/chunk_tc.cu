@@ -1116,10 +1116,13 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
 
 // ---------------------------------------------------------------------------
 // Solve and scan in one cooperative launch, for a single sequence: the first
-// `nscan` CTAs run the scan of one value head each; every other CTA runs three
-// independent 128-thread solve groups (own shared memory slice, 128 tensor-
-// memory columns, named barrier) that claim (chunk slot, value head) items in
-// chunk order and publish a ready flag per item.  A scan CTA awaits a chunk's
+// `nscan` CTAs run the scan of one value head each; every other CTA runs up to
+// three independent 128-thread solve groups (own shared memory slice, 128
+// tensor-memory columns, named barrier) that claim (chunk slot, value head)
+// items in chunk order and publish a ready flag per item.  Groups on one SM
+// slow each other down (an item takes about 1.7x as long with three as with
+// one), so `ngroups` of them claim items: enough for the solve to stay ahead
+// of the scans, and no more, which shortens the wait for the first chunk.  A scan CTA awaits a chunk's
 // flag before loading its tiles, so the solve of later chunks overlaps the
 // scan of earlier ones.  All CTAs are resident at once (cooperative launch
 // with one CTA per SM), so these waits always end; each is bounded anyway.
@@ -1137,7 +1140,8 @@ template <typename Tout, bool NORM>
 __global__ void __launch_bounds__(NT3, 1)
 chunk_fused_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo,
-                   const __grid_constant__ CUtensorMap tmz, ChunkArgs p, int nscan, int nitems, int* flags) {
+                   const __grid_constant__ CUtensorMap tmz, ChunkArgs p, int nscan, int nitems, int* flags,
+                   int ngroups) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   if ((int)blockIdx.x < nscan) {
@@ -1161,7 +1165,7 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
   const uint32_t tbase = *tslot + 128u * (uint32_t)g;
   int* counter = flags + nitems;
   uint32_t ph = 0;
-  for (;;) {
+  for (; g < ngroups;) {
     if (tid == 0) *item_slot = atomicAdd(counter, 1);
     named_sync(barid, 128);
     const int item = *item_slot;
@@ -1280,7 +1284,12 @@ cudaError_t launch_chunk_tc(const ChunkArgs& p, cudaStream_t s) {
     CUtensorMap mo = mk;                               // fp32 rows are stored directly
     if (p.out_bf16 && !make_map(&mo, p.o, p.total, p.Nv * DV)) return cudaErrorInvalidValue;
     ChunkArgs pc = p;
-    void* args[] = {&mq, &mk, &mv, &mo, &mz, &pc, &nscan, &nitems, &flags};
+    // Solve groups per CTA: the scans take Nv items per period (about 1.5 us), and one, two
+    // or three groups per SM deliver an item per about 6, 8 or 10.6 us each; take the fewest
+    // that keep the solve about 1.3x ahead.
+    const double per_scan = (double)(sms - nscan) / (double)nscan;
+    int ngroups = per_scan >= 5.3 ? 1 : (per_scan >= 3.55 ? 2 : 3);
+    void* args[] = {&mq, &mk, &mv, &mo, &mz, &pc, &nscan, &nitems, &flags, &ngroups};
     const void* fn = fused_kernels()[(p.out_bf16 ? 0 : 2) + (p.z != nullptr ? 1 : 0)];
     return cudaLaunchCooperativeKernel(fn, dim3(sms), dim3(NT3), args, K3_SMEM, s);
   }
