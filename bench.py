@@ -319,10 +319,13 @@ def run_ours(args):
     t_norm = timed(run['norm'])
     t_fused = timed(run['fused'])
     ms_step = max_over_ranks(statistics.mean(t_step))
-    # conv tile + conv state, chunk prefill (one sequence: one cooperative solve + scan launch), rmsnorm
-    # conv tile + conv state, chunk prefill (one sequence: one cooperative launch), gated norm;
-    # timed: the step replays, then the replays of each call and of the fused chunk + norm call
-    launches_prefill = 4 * args.steps * 2 + args.steps
+    # Kernels of this library per call: conv_gating is one (the tiled pass writes the new conv
+    # state itself when there is no state in, as here), chunk prefill one (one sequence: one
+    # cooperative solve + scan launch), gated norm one, the fused chunk + norm call one.
+    # Timed: the step replays, then the replays of each call and of the fused call.
+    k_conv, k_chunk, k_norm, k_fused = 1, 1, 1, 1
+    k_step = k_conv + k_chunk + k_norm
+    launches_prefill = args.steps * (k_step + k_conv + k_chunk + k_norm + k_fused)
 
     # ---------------- decode workload (fused step, state in place; 512 MiB state > L2)
     del flush, flush_rd
@@ -434,7 +437,7 @@ def run_ours(args):
                                 'bytes_per_launch': dbytes}},
         'e2e': {'value': ws * T / (ms_e2e * 1e-3), 'unit': 'tokens/s', 'h2d_bytes_per_step': h2d,
                 'd2h_bytes_per_step': d2h, 'ms_per_step': ms_e2e},
-        'gpu_launches': launches_prefill + dsteps + 4 * args.steps,
+        'gpu_launches': launches_prefill + dsteps + k_step * args.steps,
         'clocks': clocks,
     }
     if ws == 1 and not args.no_cpu_baseline:

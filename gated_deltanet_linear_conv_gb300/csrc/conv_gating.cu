@@ -305,6 +305,21 @@ conv_gating_tile_kernel(const __grid_constant__ CUtensorMap tmx, ConvGatingArgs 
     tc::fence_barrier_init();
     if (blockIdx.x < ntiles) issue(blockIdx.x, 0);
   }
+  // Without a state in, the new conv state comes from the staged rows of the tile holding a
+  // sequence's last token (with one, a separate pass reads the old state first, so that it may
+  // be updated in place).  Empty sequences keep a zero state: written here.
+  const bool write_state = p.state_out != nullptr && p.state_in == nullptr;
+  if (write_state) {
+    for (int sq = blockIdx.x; sq < p.num_seqs; sq += gridDim.x) {
+      int bos, eos;
+      if (!seq_bounds(p.cu, p.num_seqs, p.total, sq, bos, eos)) {
+        if (threadIdx.x == 0) raise_error(p.err, kDevErrSeqlens);
+      } else if (bos == eos) {
+        bf16* so = static_cast<bf16*>(p.state_out) + (size_t)sq * p.C * 3;
+        for (int i = threadIdx.x; i < p.C * 3; i += blockDim.x) so[i] = __float2bfloat16_rn(0.f);
+      }
+    }
+  }
   // gates (token, head) in a grid-stride loop, two items per thread with both loads issued first
   {
     const bf16* a = static_cast<const bf16*>(p.a);
@@ -443,6 +458,29 @@ conv_gating_tile_kernel(const __grid_constant__ CUtensorMap tmx, ConvGatingArgs 
         }
       }
     }
+    if (write_state && (p.num_seqs > 1 || t_end == p.total)) {
+      // new conv state (no state in: zeros before a sequence's first token) of each non-empty
+      // sequence whose last token is in this tile (all lie between the sequences of the
+      // tile's first and last tokens), from the staged rows: thread = 4 channels of the 1024
+      const int sa = find_seq(p.cu, p.num_seqs, p.total, t0);
+      const int sb = find_seq(p.cu, p.num_seqs, p.total, t_end - 1);
+      const int ch = threadIdx.x * 4;
+      const uint8_t* box = sm + buf * TILE_BYTES + (ch >> 8) * STRIP_BYTES + (ch & 255) * 2;
+      for (int sq = sa; sq <= sb; ++sq) {
+        int bos, eos;
+        if (!seq_bounds(p.cu, p.num_seqs, p.total, sq, bos, eos) || eos == bos || eos <= t0 || eos > t_end) continue;
+        bf16* so = static_cast<bf16*>(p.state_out) + ((size_t)sq * p.C + ct * 1024 + ch) * 3;
+#pragma unroll
+        for (int j = 0; j < 3; ++j) {
+          const int t = eos - 3 + j;                 // staged row t - t0 + 3
+          const bool in_seq = t >= bos;
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            so[c * 3 + j] = in_seq ? *reinterpret_cast<const bf16*>(box + (t - t0 + 3) * 512 + c * 2)
+                                   : __float2bfloat16_rn(0.f);
+        }
+      }
+    }
     __syncthreads();     // the tile is read; the next TMA may overwrite it
   }
 }
@@ -506,7 +544,7 @@ cudaError_t launch_typed(const ConvGatingArgs& p, cudaStream_t s) {
       if (e != cudaSuccess) return e;
     }
   }
-  if (p.state_out != nullptr) {
+  if (p.state_out != nullptr && !(tiled && p.state_in == nullptr)) {
     dim3 grid((p.C + 255) / 256, p.num_seqs);
     conv_state_kernel<Tin><<<grid, 256, 0, s>>>(p);
     return cudaGetLastError();

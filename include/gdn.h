@@ -111,8 +111,12 @@ int gdn_check_device_error(void* stream);
  *   q, k           [tokens, Nk, Dk]     out_dtype
  *   v              [tokens, Nv, Dv]     out_dtype
  *   g, beta        [tokens, Nv]         float32
- * Two kernels are enqueued: the conv/norm/gating pass, then (only when
- * conv_state_out is not NULL) the conv-state update.
+ * One kernel is enqueued for the conv/norm/gating pass.  A second one, the
+ * conv-state update, follows when conv_state_out is not NULL and either
+ * conv_state_in is not NULL (it reads the old state first, so the update may
+ * be in place) or the inputs do not take the tiled bf16 path (C a multiple of
+ * 1024, Nk*Dk a multiple of 256); otherwise the first kernel writes the new
+ * state from its staged input rows.
  * ------------------------------------------------------------------------ */
 int gdn_conv_gating(const gdn_dims* dims, const int32_t* cu_seqlens,
                     const void* mixed_qkv, int in_dtype,

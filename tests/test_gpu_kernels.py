@@ -115,6 +115,22 @@ def test_conv_gating_in_place_state_and_bf16_out(shape):
         assert rel_l2(np64(got), ref[name]) <= TOL_BF16, name
 
 
+@pytest.mark.parametrize('lengths', [[1, 2, 5, 0, 37, 64, 130, 3], [0, 16, 0, 2, 30, 0], [40]],
+                         ids=['mixed', 'empties', 'one'])
+def test_conv_gating_state_out_without_state_in(lengths):
+    """The tiled bf16 path writes the new conv state from its staged rows when there is no
+    state in (zeros before a sequence's first token, and for empty sequences)."""
+    shape = SHAPES[0]
+    inp = _conv_case(shape, torch.bfloat16, lengths, seed=14, state=False)
+    cu = inp.cu_seqlens()
+    (q, k, v, g, beta), cs_out = _run_conv(inp, cu, torch.bfloat16, state=False)
+    ref = _oracle_conv(inp, cu, state=False)
+    np.testing.assert_array_equal(np64(cs_out), ref['conv_state'])
+    for name, got in (('q', q), ('k', k), ('v', v)):
+        assert rel_l2(np64(got), ref[name]) <= TOL_BF16, name
+    gdn.check_device_error()
+
+
 def test_conv_gating_equal_batches_no_state():
     shape = SHAPES[0]
     inp = _conv_case(shape, torch.bfloat16, [33, 33, 33], seed=13, state=False, bias=False)
