@@ -8,7 +8,7 @@
 // one iteration ahead (the next rows are in flight while these are computed),
 // shuffle reduction of the sum of squares, element pairs through the packed
 // fp32x2 multiply (each half rounded as the scalar one), grid-stride over rows
-// with two resident CTAs per SM.
+// with three resident CTAs per SM.
 
 #include "common.cuh"
 #include "launch.h"
@@ -63,10 +63,11 @@ template <> __device__ __forceinline__ float gate_silu<bf16>(float z) {
 template <> __device__ __forceinline__ float gate_silu<float>(float z) { return silu_fast(z); }
 
 template <typename Tx, typename Tz, typename Ty>
-__global__ void __launch_bounds__(256, 2)
+__global__ void __launch_bounds__(256, 3)
 gated_rmsnorm_kernel(RmsNormArgs p) {
-  // rows in flight per warp step: 4 for bf16 x and z, fewer when wider types need the registers
-  constexpr int UNROLL = sizeof(Tx) + sizeof(Tz) == 4 ? 4 : 2;
+  // rows per warp step: 2 for bf16 x and z, 1 for wider types (with the next step's rows
+  // also in flight, this keeps three CTAs per SM: more resident warps beat deeper unrolling)
+  constexpr int UNROLL = sizeof(Tx) + sizeof(Tz) == 4 ? 2 : 1;
   const int lanes_per_row = p.dim / 8;
   const int rows_per_step = 32 / lanes_per_row;          // rows per warp per unrolled step
   const int rows_per_iter = rows_per_step * UNROLL;
@@ -156,7 +157,7 @@ cudaError_t launch_gated_rmsnorm(const RmsNormArgs& p, cudaStream_t s) {
   if (p.rows == 0) return cudaSuccess;
   const int rows_per_block = 8 * (32 / (p.dim / 8)) * 4;
   const int64_t need = (p.rows + rows_per_block - 1) / rows_per_block;
-  const int blocks = (int)std::min<int64_t>(need, (int64_t)num_sms() * 2);   // two resident per SM
+  const int blocks = (int)std::min<int64_t>(need, (int64_t)num_sms() * 3);   // three resident per SM
   if (p.x_bf16) {
     return p.z_bf16 ? launch_y<bf16, bf16>(p, s, blocks) : launch_y<bf16, float>(p, s, blocks);
   }
