@@ -25,8 +25,9 @@
 //    chunks with S^T resident in tensor memory.  PREP (warp 0) forms
 //    [U~^T | 0]; STATE (warps 1-4) runs the S-dependent products, whose A
 //    operands (bf16 S^T and U^T) it writes back into tensor memory; OUT
-//    (warps 5-8) loads each chunk's tiles and stores the output rows.  Every
-//    product is an M = 128 tcgen05.mma with Dv on the tensor-memory lanes.
+//    (warps 5-8) issues the O product and stores the output rows; a LOADER
+//    warp (fused launch) brings each chunk's tiles in.  Every product is an
+//    M = 128 tcgen05.mma with Dv on the tensor-memory lanes.
 // A single sequence runs both parts in one cooperative launch: the scan CTAs
 // take the chunks' tiles as soon as solve groups on the other SMs publish
 // them.  Packed batches run the solve kernel, then the scan kernel.
@@ -522,14 +523,18 @@ chunk_solve_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
 
 // ---------------------------------------------------------------------------
 // kernel 2: the scan over chunks
-//   warp 0     PREP   loads v and T diag(beta), [U~^T | 0] = V^T [T diag(beta); 0]^T
-//   warps 1-4  STATE  the S-dependent products and their epilogues
-//   warps 5-8  OUT    loads each chunk's stage, stores the output rows
+//   warp 0     PREP    [U~^T | 0] = V^T [T diag(beta); 0]^T once a chunk's v tiles land
+//   warps 1-4  STATE   the S-dependent products and their epilogues
+//   warps 5-8  OUT     the product O^T += U^T P^T (the STATE leader issues it when the
+//                      gated norm is in the epilogue), then the output rows
+//   warp 9     LOADER  (fused launch only) awaits each chunk's ready flag and issues its
+//                      copies; without it PREP issues the v copies and OUT the stage copies
 // The state lives in tensor memory transposed (lane dv, column dk, fp32).
 // Per chunk, STATE writes S^T and U^T back into tensor memory as bf16 and
 // every S-dependent product reads its A operand from there:
 //   [U^T | O^T] += S^T [-W; Q~]^T          (N = 128, K = Dk)
-//   S^T = gamma_L S^T + (U^T diag(dec)) K  (N = 128, K = 64)
+//   S^T = gamma_L S^T + (U^T diag(dec)) K  (N = 128, K = 64; the scaling by gamma_L runs
+//                                           in place while the product above is in flight)
 //   O^T += U^T P^T                         (N = 64,  K = 64)
 // ---------------------------------------------------------------------------
 constexpr int NT2 = 288;
