@@ -218,8 +218,8 @@ conv_gating_kernel(ConvGatingArgs p) {
 // go through the packed fp32x2 FMA (each lane holds an even/odd channel pair
 // as one float2), which rounds each half as the scalar FMA does.  Tokens in
 // the first 3 positions of a sequence are recomputed with their conv state
-// afterwards.  The gates, which depend on the token and head only, are a
-// grid-stride prologue whose loads overlap the first tile's copy.
+// afterwards.  The gates, which depend on the token and head only, are
+// computed after the tile loop by the CTAs that ran one tile fewer.
 constexpr int TT = 16;                         // tokens per tile
 constexpr int TROWS = TT + 3;
 constexpr int RPW = TT / 2;                    // tokens per warp
@@ -279,6 +279,28 @@ __device__ __forceinline__ void l2norm8x2(float2 (&y)[4], int lanes_per_head, fl
   for (int i = 0; i < 4; ++i) y[i] = __fmul2_rn(y[i], make_float2(inv, inv));
 }
 
+// Gates (token, head) items first .. n - 1 step `stride`, two per thread with all loads
+// issued first.
+__device__ __forceinline__ void gates_range(const ConvGatingArgs& p, int64_t first, int64_t stride) {
+  const bf16* a = static_cast<const bf16*>(p.a);
+  const bf16* b = static_cast<const bf16*>(p.b);
+  const int64_t n = (int64_t)p.total * p.Nv;
+  for (int64_t i0 = first; i0 < n; i0 += 2 * stride) {
+    const int64_t i1 = i0 + stride;
+    const bool has1 = i1 < n;
+    const float a0 = __bfloat162float(a[i0]), b0 = __bfloat162float(b[i0]);
+    const float a1 = has1 ? __bfloat162float(a[i1]) : 0.f, b1 = has1 ? __bfloat162float(b[i1]) : 0.f;
+    const int h0 = (int)(i0 % p.Nv);
+    p.beta[i0] = sigmoidf_(b0);
+    p.g[i0] = -expf(p.A_log[h0]) * softplusf_(a0 + p.dt_bias[h0]);
+    if (has1) {
+      const int h1 = (int)(i1 % p.Nv);
+      p.beta[i1] = sigmoidf_(b1);
+      p.g[i1] = -expf(p.A_log[h1]) * softplusf_(a1 + p.dt_bias[h1]);
+    }
+  }
+}
+
 template <typename Tout>
 __global__ void __launch_bounds__(256, 2)
 conv_gating_tile_kernel(const __grid_constant__ CUtensorMap tmx, ConvGatingArgs p) {
@@ -317,27 +339,6 @@ conv_gating_tile_kernel(const __grid_constant__ CUtensorMap tmx, ConvGatingArgs 
       } else if (bos == eos) {
         bf16* so = static_cast<bf16*>(p.state_out) + (size_t)sq * p.C * 3;
         for (int i = threadIdx.x; i < p.C * 3; i += blockDim.x) so[i] = __float2bfloat16_rn(0.f);
-      }
-    }
-  }
-  // gates (token, head) in a grid-stride loop, two items per thread with both loads issued first
-  {
-    const bf16* a = static_cast<const bf16*>(p.a);
-    const bf16* b = static_cast<const bf16*>(p.b);
-    const int64_t n = (int64_t)p.total * p.Nv;
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i0 < n; i0 += 2 * stride) {
-      const int64_t i1 = i0 + stride;
-      const bool has1 = i1 < n;
-      const float a0 = __bfloat162float(a[i0]), b0 = __bfloat162float(b[i0]);
-      const float a1 = has1 ? __bfloat162float(a[i1]) : 0.f, b1 = has1 ? __bfloat162float(b[i1]) : 0.f;
-      const int h0 = (int)(i0 % p.Nv);
-      p.beta[i0] = sigmoidf_(b0);
-      p.g[i0] = -expf(p.A_log[h0]) * softplusf_(a0 + p.dt_bias[h0]);
-      if (has1) {
-        const int h1 = (int)(i1 % p.Nv);
-        p.beta[i1] = sigmoidf_(b1);
-        p.g[i1] = -expf(p.A_log[h1]) * softplusf_(a1 + p.dt_bias[h1]);
       }
     }
   }
@@ -482,6 +483,14 @@ conv_gating_tile_kernel(const __grid_constant__ CUtensorMap tmx, ConvGatingArgs 
       }
     }
     __syncthreads();     // the tile is read; the next TMA may overwrite it
+  }
+  // The gates, which depend on the token and head only, are left to the CTAs that ran one
+  // tile fewer (they would idle while the others finish), or to all CTAs when the tiles
+  // divide evenly.
+  const int fewer_from = ntiles % (int)gridDim.x;
+  if ((int)blockIdx.x >= fewer_from) {
+    const int64_t nctas = (int64_t)gridDim.x - fewer_from;
+    gates_range(p, ((int64_t)blockIdx.x - fewer_from) * blockDim.x + threadIdx.x, nctas * blockDim.x);
   }
 }
 
