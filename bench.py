@@ -147,6 +147,33 @@ def dist_setup():
     return ws, rank, local
 
 
+def make_ranks(dist, device):
+    """barrier() and max_over_ranks(x) of the bench's replicas: `dist` is torch.distributed with
+    an initialised process group (NCCL on GPUs, gloo in the CPU tests) or None for one process;
+    `device` holds the reduction tensor and, when it is a GPU, is synchronised by barrier()."""
+    import torch
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        if device.type == 'cuda':
+            torch.cuda.synchronize(device)
+
+    def max_over_ranks(x):
+        if dist is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    return barrier, max_over_ranks
+
+
+def whole_job_rate(units_per_rank, world_size, ms_max):
+    """Units processed by all ranks per second, over the slowest rank's time (weak scaling)."""
+    return units_per_rank * world_size / (ms_max * 1e-3)
+
+
 # ------------------------------------------------------------------ reference arm
 
 def cpu_threads():
@@ -223,17 +250,7 @@ def run_ours(args):
         import torch.distributed as dist
         dist.init_process_group('nccl', device_id=torch.device('cuda', local))
 
-    def barrier():
-        if dist is not None:
-            dist.barrier()
-        torch.cuda.synchronize()
-
-    def max_over_ranks(x):
-        if dist is None:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device='cuda')
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    barrier, max_over_ranks = make_ranks(dist, torch.device('cuda', local))
 
     hbm_peak, tc_peak, tc_sust, peak_src = load_peaks()
     sampler = ClockSampler(local)
@@ -417,7 +434,7 @@ def run_ours(args):
                 traffic = rec['bytes_per_launch']
     line = {
         'metric': METRIC,
-        'value': ws * T / (ms_step * 1e-3),
+        'value': whole_job_rate(T, ws, ms_step),
         'unit': 'tokens/s',
         'n_gpus': ws, 'steps': args.steps, 'warmup': args.warmup,
         'ms_per_step': ms_step,
@@ -440,11 +457,11 @@ def run_ours(args):
                               'frac_hbm': nb / (us_norm * 1e-6) / 1e9 / hbm_peak, 'bytes': nb},
             'chunk_prefill_gated_norm': {'us': us_fused, 'note': 'one call: chunk prefill with the norm in its epilogue'}},
         'decode': {'workload': 'decode_b256', 'kernel': 'gdn_decode_fused', 'steps': dsteps,
-                   'us_per_step': ms_dec * 1e3, 'tokens_per_s': ws * B / (ms_dec * 1e-3),
+                   'us_per_step': ms_dec * 1e3, 'tokens_per_s': whole_job_rate(B, ws, ms_dec),
                    'roofline': {'bound': 'hbm', 'achieved': dec_gbs, 'peak': hbm_peak, 'unit': 'GB/s',
                                 'frac': dec_gbs / hbm_peak, 'frac_of_8tbs': dec_gbs / NOMINAL_HBM_GBS,
                                 'bytes_per_launch': dbytes}},
-        'e2e': {'value': ws * T / (ms_e2e * 1e-3), 'unit': 'tokens/s', 'h2d_bytes_per_step': h2d,
+        'e2e': {'value': whole_job_rate(T, ws, ms_e2e), 'unit': 'tokens/s', 'h2d_bytes_per_step': h2d,
                 'd2h_bytes_per_step': d2h, 'ms_per_step': ms_e2e},
         'gpu_launches': launches_prefill + dsteps + k_step * args.steps,
         'clocks': clocks,
