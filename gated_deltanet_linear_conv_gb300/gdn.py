@@ -297,10 +297,12 @@ def mixer_prefill(mixed_qkv, conv_w, a, b, A_log, dt_bias, z, norm_w, Nk, Nv, Dk
                   cu_seqlens=None, num_seqs=1, conv_bias=None, conv_state_in=None,
                   conv_state_out=None, initial_state=None, final_state=None, q_scale=None,
                   l2_eps=1e-6, norm_eps=1e-6, act_dtype=torch.bfloat16, out_dtype=torch.bfloat16,
-                  bufs=None, fuse_norm=True):
-    """The prefill path: conv_gating -> chunk_prefill -> gated_rmsnorm, with the norm
-    fused into the chunk prefill's output (gdn_chunk_prefill_gated_norm) when
-    ``fuse_norm`` and the shapes run on the tensor cores (bf16, 128-wide heads).
+                  bufs=None, fuse_norm=False):
+    """The prefill path: conv_gating -> chunk_prefill -> gated_rmsnorm.  With ``fuse_norm``
+    (and shapes that run on the tensor cores: bf16, 128-wide heads) the norm is applied in
+    the chunk prefill's output epilogue instead (gdn_chunk_prefill_gated_norm), so o is
+    never stored; on one GB300 that call is slower than the two separate ones (the norm
+    epilogue paces the sequential scan), hence off by default.
 
     ``bufs`` (optional dict) supplies preallocated q, k, v, g, beta, o, y."""
     bufs = bufs or {}

@@ -20,7 +20,7 @@ def cuda(t):
     return None if t is None else t.cuda()
 
 
-def _gpu_prefill(inp, final_state=True):
+def _gpu_prefill(inp, final_state=True, fuse_norm=False):
     sh = inp.shape
     cu = inp.cu_seqlens()
     cs_out = torch.empty(inp.num_seqs, sh.C, 3, dtype=inp.mixed_qkv.dtype, device='cuda')
@@ -28,7 +28,7 @@ def _gpu_prefill(inp, final_state=True):
                              cuda(inp.A_log), cuda(inp.dt_bias), cuda(inp.z), cuda(inp.norm_w),
                              sh.Nk, sh.Nv, sh.Dk, sh.Dv, cu_seqlens=cuda(cu),
                              conv_state_in=cuda(inp.conv_state), conv_state_out=cs_out,
-                             initial_state=cuda(inp.S0), out_dtype=torch.bfloat16)
+                             initial_state=cuda(inp.S0), out_dtype=torch.bfloat16, fuse_norm=fuse_norm)
     torch.cuda.synchronize()
     gdn.check_device_error()
     return y, S, cs_out
@@ -56,9 +56,10 @@ def _oracle_seq(inp, s, keep=None, segment=4096):
     return ys, S[0], cs[0]
 
 
-def test_prefill_t4096():
+@pytest.mark.parametrize('fuse_norm', [False, True], ids=['separate_norm', 'fused_norm'])
+def test_prefill_t4096(fuse_norm):
     inp = I.workload('prefill_t4096')
-    y, S, cs = _gpu_prefill(inp)
+    y, S, cs = _gpu_prefill(inp, fuse_norm=fuse_norm)
     ys, S_ref, cs_ref = _oracle_seq(inp, 0)
     assert rel_l2(np64(y), ys[0]) <= TOL_BF16
     assert rel_l2(np64(S[0]), S_ref) <= TOL_BF16
