@@ -7,7 +7,10 @@ gdn_conv_gating (+ conv-state output) -> gdn_chunk_prefill -> gdn_gated_rmsnorm.
 The single call gdn_chunk_prefill_gated_norm (chunk prefill with the norm in its
 epilogue) is timed beside it.
 The fused decode step (B=256, one token each, fp32 state in place) is timed in
-the same run and reported under "decode".
+the same run and reported under "decode".  "e2e" is the same prefill step through
+the public API with the inputs copied in from pinned host memory and y read back
+every step; the copies of step i+1 run on a copy stream under step i's compute
+(two device buffer sets), as a pipelined caller would run them.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -387,21 +390,56 @@ def run_ours(args):
     h2d = sum(t.numel() * t.element_size() for t in (hx, ha, hb, hz))
     d2h = hy.numel() * hy.element_size()
 
-    def e2e_step():
-        x.copy_(hx, non_blocking=True)
-        a.copy_(ha, non_blocking=True)
-        b.copy_(hb, non_blocking=True)
-        z.copy_(hz, non_blocking=True)
-        prefill_step()
-        hy.copy_(bufs['y'], non_blocking=True)
+    # Two sets of device inputs and outputs: step i's host->device copies run on a copy stream
+    # while step i-1 computes, and step i's device->host read follows its compute there.  The
+    # copy stream's order is H2D(0), H2D(1), D2H(0), H2D(2), D2H(1), ...; every step still
+    # moves its own inputs and result inside the timed region.
+    sets = [(x, a, b, z, bufs['y'])]
+    sets.append(tuple(torch.empty_like(t) for t in sets[0]))
+    hys = [hy, torch.empty_like(hy).pin_memory()]
+    copy_stream = torch.cuda.Stream()
+    h2d_done = [torch.cuda.Event(), torch.cuda.Event()]
+    comp_done = [torch.cuda.Event(), torch.cuda.Event()]
+    d2h_done = torch.cuda.Event()
 
-    for _ in range(args.warmup):
-        e2e_step()
+    def e2e_h2d(j):
+        with torch.cuda.stream(copy_stream):
+            for dst, src in zip(sets[j][:4], (hx, ha, hb, hz)):
+                dst.copy_(src, non_blocking=True)
+            h2d_done[j].record(copy_stream)
+
+    def e2e_compute(j):
+        xj, aj, bj, zj, yj = sets[j]
+        stream.wait_event(h2d_done[j])
+        gdn.conv_gating(xj, w, aj, bj, A_log, dt_bias, sh.Nk, sh.Nv, sh.Dk, sh.Dv, num_seqs=1,
+                        conv_state_out=conv_state_out,
+                        out=(bufs['q'], bufs['k'], bufs['v'], bufs['g'], bufs['beta']))
+        chunk_call()
+        gdn.gated_rmsnorm(bufs['o'], zj, nw, 1e-6, bf, yj)
+        comp_done[j].record(stream)
+
+    def e2e_d2h(j):
+        with torch.cuda.stream(copy_stream):
+            copy_stream.wait_event(comp_done[j])
+            hys[j].copy_(sets[j][4], non_blocking=True)
+            d2h_done.record(copy_stream)
+
+    def e2e_steps(n, start=None):
+        if start is not None:          # the first copy starts inside the timed region
+            copy_stream.wait_event(start)
+        e2e_h2d(0)
+        for i in range(n):
+            e2e_compute(i & 1)
+            if i + 1 < n:
+                e2e_h2d((i + 1) & 1)
+            e2e_d2h(i & 1)
+        stream.wait_event(d2h_done)
+
+    e2e_steps(args.warmup)
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
+    e2e_steps(args.steps, e0)
     e1.record(stream)
     barrier()
     ms_e2e = max_over_ranks(e0.elapsed_time(e1) / args.steps)
