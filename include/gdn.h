@@ -98,6 +98,10 @@ int gdn_check_device_error(void* stream);
  *   k[t, i]  =           y_k / sqrt(sum(y_k^2) + l2_eps)   per key head i
  *   v[t, h]  = y_v                                          per value head h
  *   beta     = sigmoid(b);  g = -exp(A_log) * softplus(a + dt_bias)  (fp32)
+ * With bf16 outputs silu(x) is evaluated as h + h tanh(h), h = x / 2, with the
+ * hardware tanh: its absolute error is at most about 2^-11 |h|, within half a
+ * bf16 ulp of the result for x >= -2 (for more negative x the result is near
+ * zero and its relative error grows); fp32 outputs use x / (1 + e^-x).
  *   conv_state_out[s] = the last 3 entries of xpad (raw inputs, oldest first)
  *
  *   mixed_qkv      [tokens, C]          in_dtype
@@ -185,6 +189,10 @@ int gdn_chunk_prefill(const gdn_dims* dims, const int32_t* cu_seqlens,
  * self.norm(core_output, z)).  The core output o is never stored; it is
  * rounded to bf16 (as a stored bf16 o would be) and normalised:
  *   y[t, h] = o[t, h] / sqrt(mean(o[t, h]^2) + norm_eps) * norm_w * silu(z[t, h])
+ * For bf16 y the gate norm_w * silu(z) is evaluated in bf16x2 arithmetic (the
+ * tanh form of gdn_conv_gating at bf16 precision); fp32 y keeps fp32 throughout.
+ * On one GB300 this call is slower than gdn_chunk_prefill + gdn_gated_rmsnorm
+ * (the norm epilogue paces the sequential scan); it saves the o round trip.
  * Arguments as gdn_chunk_prefill, with o replaced by
  *   z              [tokens, Nv, Dv]     bf16 (else GDN_ERR_UNSUPPORTED)
  *   norm_w         [Dv]                 float32
@@ -281,6 +289,8 @@ int gdn_recurrent_decode_steps(const gdn_dims* dims, const int32_t* cu_seqlens,
  *   y[r, :] = x[r, :] / sqrt(mean(x[r, :]^2) + eps) * w * silu(z[r, :])
  *   x [rows, dim] x_dtype; z [rows, dim] z_dtype; w [dim] float32;
  *   y [rows, dim] out_dtype.  dim in {64, 128}.
+ * silu(z) as in gdn_conv_gating: the hardware-tanh form for bf16 y (absolute
+ * error at most about 2^-11 |z| / 2), z / (1 + e^-z) for fp32 y.
  * ------------------------------------------------------------------------ */
 int gdn_gated_rmsnorm(int64_t rows, int32_t dim, const void* x, int x_dtype,
                       const void* z, int z_dtype, const float* w, float eps,
