@@ -98,10 +98,11 @@ int gdn_check_device_error(void* stream);
  *   k[t, i]  =           y_k / sqrt(sum(y_k^2) + l2_eps)   per key head i
  *   v[t, h]  = y_v                                          per value head h
  *   beta     = sigmoid(b);  g = -exp(A_log) * softplus(a + dt_bias)  (fp32)
- * With bf16 outputs silu(x) is evaluated as h + h tanh(h), h = x / 2, with the
- * hardware tanh: its absolute error is at most about 2^-11 |h|, within half a
- * bf16 ulp of the result for x >= -2 (for more negative x the result is near
- * zero and its relative error grows); fp32 outputs use x / (1 + e^-x).
+ * On the tiled bf16 path (see the launches below) with bf16 outputs, silu(x) is
+ * evaluated as h + h tanh(h), h = x / 2, with the hardware tanh: its absolute
+ * error is at most about 2^-11 |h|, within half a bf16 ulp of the result for
+ * x >= -2 (for more negative x the result is near zero and its relative error
+ * grows); otherwise silu(x) = x / (1 + e^-x).
  *   conv_state_out[s] = the last 3 entries of xpad (raw inputs, oldest first)
  *
  *   mixed_qkv      [tokens, C]          in_dtype
