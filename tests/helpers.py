@@ -24,3 +24,45 @@ def rel_l2(x, ref):
 # the bf16 tensor-core chunk path.
 TOL_F32 = 1e-4
 TOL_BF16 = 1e-2
+
+# Per-row bars.  Every row -- every vector along the last axis: one (token, head)
+# of an output, one key row of a state -- must also be close on its own, so that
+# a wrong row, head or chunk cannot hide inside the tensor-level norm (one wholly
+# wrong (token, head) row of a 4096 x 32-head output moves the tensor rel-L2 by
+# only ~0.006).  A row's error is taken relative to max(its norm, ROW_FLOOR x the
+# median row norm): rows far smaller than typical carry the same absolute
+# rounding error as the rest.  The bars are 10x (fp32) and 5x (bf16) the tensor
+# bars; a wrong row scores ~1.
+TOL_ROW_F32 = 1e-3
+TOL_ROW_BF16 = 5e-2
+ROW_FLOOR = 0.25
+
+
+def row_rel_err(x, ref):
+    """max over rows (last axis) of ||x_r - ref_r|| / max(||ref_r||, ROW_FLOOR * median row norm)."""
+    x = np.asarray(x, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert x.shape == ref.shape, (x.shape, ref.shape)
+    if x.size == 0:
+        return 0.0
+    n = ref.shape[-1] if ref.ndim else 1
+    x = x.reshape(-1, n)
+    ref = ref.reshape(-1, n)
+    d = np.linalg.norm(x - ref, axis=1)
+    rn = np.linalg.norm(ref, axis=1)
+    den = np.maximum(rn, ROW_FLOOR * np.median(rn))
+    den = np.where(den > 0, den, 1.0)
+    return float((d / den).max())
+
+
+def assert_close(x, ref, tol, row_tol=None, what=''):
+    """Tensor-level rel-L2 <= tol and per-row error <= row_tol (by default the row bar
+    that goes with tol)."""
+    x = np.asarray(x, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    e = rel_l2(x, ref)
+    assert e <= tol, ('rel-L2', what, e, tol)
+    if row_tol is None:
+        row_tol = TOL_ROW_F32 if tol <= TOL_F32 else TOL_ROW_BF16
+    r = row_rel_err(x, ref)
+    assert r <= row_tol, ('row', what, r, row_tol)

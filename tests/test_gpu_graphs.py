@@ -11,7 +11,7 @@ import torch
 import oracle as O
 from gated_deltanet_linear_conv_gb300 import gdn
 from gated_deltanet_linear_conv_gb300 import inputs as I
-from helpers import TOL_BF16, TOL_F32, np64, rel_l2
+from helpers import TOL_BF16, TOL_F32, assert_close, np64
 
 pytestmark = pytest.mark.gpu
 
@@ -52,8 +52,8 @@ def _check_prefill(d, inp):
                           np64(inp.A_log), np64(inp.dt_bias), np64(inp.z), np64(inp.norm_w),
                           sh.Nk, sh.Nv, sh.Dk, sh.Dv, cu_seqlens=inp.cu_seqlens().numpy(),
                           conv_state=np64(inp.conv_state), initial_state=np64(inp.S0))
-    assert rel_l2(np64(d['bufs']['y']), ref['y']) <= TOL_BF16
-    assert rel_l2(np64(d['ST']), ref['state']) <= TOL_BF16
+    assert_close(np64(d['bufs']['y']), ref['y'], TOL_BF16)
+    assert_close(np64(d['ST']), ref['state'], TOL_BF16)
     np.testing.assert_array_equal(np64(d['cs_out']), ref['conv_state'])
 
 
@@ -97,7 +97,7 @@ def test_mixed_prefill_and_decode_in_one_graph():
         ref = O.decode_step(np64(inp.mixed_qkv), np64(inp.conv_w), np64(inp.conv_state), np64(inp.a),
                             np64(inp.b), np64(inp.A_log), np64(inp.dt_bias), np64(inp.S0), np64(inp.z),
                             np64(inp.norm_w), sh.Nk, sh.Nv, sh.Dk, sh.Dv)
-        assert rel_l2(np64(Dy), ref['y']) <= TOL_F32
-        assert rel_l2(np64(D['S0']), ref['state']) <= TOL_F32
+        assert_close(np64(Dy), ref['y'], TOL_F32)
+        assert_close(np64(D['S0']), ref['state'], TOL_F32)
         np.testing.assert_array_equal(np64(D['conv_state']), ref['conv_state'])
     gdn.check_device_error()

@@ -382,3 +382,41 @@ def test_conv_gating_split_and_scale():
     out, _ = O.causal_conv1d(c['mixed_qkv'], c['conv_w'], None, c['conv_state'][0])
     np.testing.assert_allclose(cg['v'].reshape(T, -1), O.silu(out[:, 2 * Nk * Dk:]), rtol=1e-14)
     assert cg['g'].shape == (T, Nv) and np.all(cg['g'] < 0)
+
+
+def _split_case():
+    d = json.load(open(os.path.join(GOLDEN, 'qkv_split_hand.json')))
+    dims = d['dims']
+    x = np.array(d['x'])
+    C = x.shape[1]
+    w = np.zeros((C, 4))
+    w[:, 3] = 1.0                                   # only the current token
+    z = np.zeros((x.shape[0], dims['Nv']))
+    return d, dims, x, w, z
+
+
+def test_conv_gating_split_hand_example():
+    # q = channels [0, Nk*Dk), k = the next Nk*Dk, v = the rest, each head-major
+    d, dims, x, w, z = _split_case()
+    cg = O.conv_gating(x, w, z, z, np.zeros(dims['Nv']), np.zeros(dims['Nv']), dims['Nk'], dims['Nv'],
+                       dims['Dk'], dims['Dv'], q_scale=1 / math.sqrt(dims['Dk']), l2_eps=1e-6)
+    np.testing.assert_allclose(cg['q'], d['q'], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(cg['k'], d['k'], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(cg['v'], d['v'], rtol=0, atol=1e-12)
+
+
+def test_split_hand_example_tells_alternatives_apart():
+    # the golden values differ from what a swapped [k | q] split or a (seq, head_dim, heads)
+    # reshape would give, so either mistake in conv_gating fails the test above
+    d, dims, x, w, z = _split_case()
+    Nk, Dk, Nv, Dv = dims['Nk'], dims['Dk'], dims['Nv'], dims['Dv']
+    y = O.silu(x)
+    kd = Nk * Dk
+    def norm(t):
+        return O.l2norm(t, 1e-6)
+    swapped_q = norm(y[:, kd:2 * kd].reshape(-1, Nk, Dk)) / math.sqrt(Dk)
+    dim_major_q = norm(y[:, :kd].reshape(-1, Dk, Nk).transpose(0, 2, 1)) / math.sqrt(Dk)
+    dim_major_v = y[:, 2 * kd:].reshape(-1, Dv, Nv).transpose(0, 2, 1)
+    assert np.abs(swapped_q - np.array(d['q'])).max() > 0.1
+    assert np.abs(dim_major_q - np.array(d['q'])).max() > 0.1
+    assert np.abs(dim_major_v - np.array(d['v'])).max() > 0.1

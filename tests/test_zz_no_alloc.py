@@ -13,7 +13,7 @@ import torch
 
 from gated_deltanet_linear_conv_gb300 import gdn
 from gated_deltanet_linear_conv_gb300 import inputs as I
-from helpers import TOL_BF16, np64, rel_l2
+from helpers import TOL_BF16, assert_close, np64
 
 pytestmark = pytest.mark.gpu
 
@@ -46,8 +46,8 @@ def test_static_scratch_matches_workspace_call_twice():
         ST = torch.empty_like(S_ref)
         _static_call(q, k, v, g, beta, 1 / math.sqrt(128), S0, ST, o, cu, len(lengths))
         torch.cuda.synchronize()
-        assert rel_l2(np64(o), np64(o_ref)) <= TOL_BF16, call
-        assert rel_l2(np64(ST), np64(S_ref)) <= TOL_BF16, call
+        assert_close(np64(o), np64(o_ref), TOL_BF16, what=call)
+        assert_close(np64(ST), np64(S_ref), TOL_BF16, what=call)
     gdn.check_device_error()
 
 
