@@ -7,7 +7,12 @@ gdn_conv_gating (+ conv-state output) -> gdn_chunk_prefill -> gdn_gated_rmsnorm.
 The single call gdn_chunk_prefill_gated_norm (chunk prefill with the norm in its
 epilogue) is timed beside it.
 The fused decode step (B=256, one token each, fp32 state in place) is timed in
-the same run and reported under "decode".  "e2e" is the same prefill step through
+the same run and reported under "decode" (median of per-step events, with the
+spread), and the same prefill path on the packed workload (16 sequences,
+lengths ~ U[512, 8192]) and on the long one (T=131072) under "varlen" and
+"long_context" (tokens/s, the chunk call's TFLOP/s and fraction of peak, and
+the oracle's tokens/s on a bounded sample).  Every device time is the median of
+--steps timed replays.  "e2e" is the same prefill step through
 the public API with the inputs copied in from pinned host memory and y read back
 every step; the copies of step i+1 run on a copy stream under step i's compute
 (two device buffer sets), as a pipelined caller would run them.
@@ -187,30 +192,121 @@ def cpu_threads():
 
 
 def oracle_prefill_sample(inp, ntok):
-    """The oracle's prefill over the first ntok tokens of the workload (all heads)."""
+    """The oracle's prefill over the first ntok tokens of the workload's first sequence (all
+    heads, from that sequence's initial recurrent state)."""
     import numpy as np
     import oracle as O
     sh = inp.shape
+    ntok = min(ntok, inp.lengths[0])
     f = lambda t: t[:ntok].to(dtype=__import__('torch').float64).numpy()  # noqa: E731
     g = lambda t: t.to(dtype=__import__('torch').float64).numpy()  # noqa: E731
+    S0 = None if inp.S0 is None else g(inp.S0[:1])
     r = O.mixer_prefill(f(inp.mixed_qkv), g(inp.conv_w), f(inp.a), f(inp.b), g(inp.A_log),
-                        g(inp.dt_bias), f(inp.z), g(inp.norm_w), sh.Nk, sh.Nv, sh.Dk, sh.Dv)
+                        g(inp.dt_bias), f(inp.z), g(inp.norm_w), sh.Nk, sh.Nv, sh.Dk, sh.Dv,
+                        initial_state=S0)
     return np.asarray(r['y']).shape[0]
 
 
-def cpu_baseline(inp, budget_s=12.0):
-    """Oracle tokens/s on a bounded prefix of the prefill workload."""
+def cpu_baseline(inp, budget_s=12.0, name='prefill_t4096'):
+    """Oracle tokens/s on a bounded prefix of the workload's first sequence."""
     n = 32
     t0 = time.perf_counter()
     oracle_prefill_sample(inp, n)
     dt = time.perf_counter() - t0
-    ntok = int(max(32, min(inp.total_tokens, n * budget_s / max(dt, 1e-3))))
+    ntok = int(max(32, min(inp.lengths[0], n * budget_s / max(dt, 1e-3))))
     t0 = time.perf_counter()
-    oracle_prefill_sample(inp, ntok)
+    ntok = oracle_prefill_sample(inp, ntok)
     dt = time.perf_counter() - t0
     return {'value': ntok / dt, 'unit': 'tokens/s', 'cores': cpu_threads(), 'kind': 'oracle',
             'sample': 'fp64 NumPy oracle prefill (conv_gating + token-by-token recurrence + gated '
-                      'RMSNorm) over the first %d of 4096 tokens, all 32 heads, %.1f s' % (ntok, dt)}
+                      'RMSNorm) over the first %d tokens of %s (first sequence), all %d heads, %.1f s'
+                      % (ntok, name, inp.shape.Nv, dt)}
+
+
+# Kernels of this library per call on the tensor-core path: conv_gating launches one (with no
+# conv state in, its tiled pass writes the new state); chunk prefill launches one for a single
+# sequence (the cooperative solve + scan launch) and two for a packed batch (solve, then scan);
+# the gated norm one.
+def chunk_launches(num_seqs):
+    return 1 if num_seqs == 1 else 2
+
+
+def time_prefill_workload(name, steps, warmup, barrier, max_over_ranks, tc_peak):
+    """The prefill path (conv_gating -> chunk_prefill -> gated_rmsnorm) on a workload whose
+    inputs exceed L2 (no flush needed between steps): median device time of the step and of
+    the chunk call alone, each replayed from a CUDA graph with one event pair per replay."""
+    import torch
+    from gated_deltanet_linear_conv_gb300 import gdn
+    from gated_deltanet_linear_conv_gb300 import inputs as I
+
+    inp = I.workload(name)
+    sh = inp.shape
+    T, N = inp.total_tokens, inp.num_seqs
+    bf = torch.bfloat16
+    dev = lambda t: None if t is None else t.cuda()  # noqa: E731
+    x, w, a, b = dev(inp.mixed_qkv), dev(inp.conv_w), dev(inp.a), dev(inp.b)
+    A_log, dt_bias, z, nw = dev(inp.A_log), dev(inp.dt_bias), dev(inp.z), dev(inp.norm_w)
+    cu = dev(inp.cu_seqlens()) if N > 1 else None
+    S0 = dev(inp.S0)
+    ST = torch.empty(N, sh.Nv, sh.Dk, sh.Dv, device='cuda')
+    cs_out = torch.empty(N, sh.C, 3, dtype=bf, device='cuda')
+    bufs = dict(q=torch.empty(T, sh.Nk, sh.Dk, dtype=bf, device='cuda'),
+                k=torch.empty(T, sh.Nk, sh.Dk, dtype=bf, device='cuda'),
+                v=torch.empty(T, sh.Nv, sh.Dv, dtype=bf, device='cuda'),
+                g=torch.empty(T, sh.Nv, device='cuda'), beta=torch.empty(T, sh.Nv, device='cuda'),
+                o=torch.empty(T, sh.Nv, sh.Dv, dtype=bf, device='cuda'),
+                y=torch.empty(T, sh.Nv, sh.Dv, dtype=bf, device='cuda'))
+    ws_bytes = gdn.chunk_prefill_workspace_size(N, T, sh.Nk, sh.Nv, sh.Dk, sh.Dv)
+    wsp = torch.empty(ws_bytes, dtype=torch.uint8, device='cuda') if ws_bytes else None
+
+    def chunk_call():
+        gdn.chunk_prefill(bufs['q'], bufs['k'], bufs['v'], bufs['g'], bufs['beta'], 1.0, S0, ST, cu, N,
+                          bf, bufs['o'], wsp)
+
+    def step():
+        gdn.conv_gating(x, w, a, b, A_log, dt_bias, sh.Nk, sh.Nv, sh.Dk, sh.Dv, cu_seqlens=cu, num_seqs=N,
+                        conv_state_out=cs_out, out=(bufs['q'], bufs['k'], bufs['v'], bufs['g'], bufs['beta']))
+        chunk_call()
+        gdn.gated_rmsnorm(bufs['o'], z, nw, 1e-6, bf, bufs['y'])
+
+    for _ in range(warmup):
+        step()
+    barrier()
+    graphs = {}
+    for key, fn in (('step', step), ('chunk', chunk_call)):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        graphs[key] = g
+    stream = torch.cuda.current_stream()
+    res = {}
+    for key, g in graphs.items():
+        g.replay()
+        barrier()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for e0, e1 in evs:
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        barrier()
+        res[key] = max_over_ranks(statistics.median(e0.elapsed_time(e1) for e0, e1 in evs))
+    gdn.check_device_error()
+    flops = chunk_flops(inp.lengths, sh.Nv, sh.Dk, sh.Dv)
+    tflops = flops / (res['chunk'] * 1e-3) / 1e12
+    launches = (steps + warmup) * (2 + chunk_launches(N)) + steps * chunk_launches(N)
+    out = {'workload': name, 'num_seqs': N, 'tokens': T,
+           'lengths': inp.lengths if N > 1 else None,
+           'tokens_per_s': whole_job_rate(T, 1, res['step']),
+           'us_per_step': res['step'] * 1e3, 'us_chunk_prefill': res['chunk'] * 1e3,
+           'chunk_prefill': {'TFLOP/s': tflops, 'frac_tc': tflops / tc_peak,
+                             'algorithmic_flops': flops,
+                             'flops_formula': 'per sequence ceil(L/64) chunks x Nv x '
+                                              '(2*64^2*(3Dk+2Dv) + 6*64*Dk*Dv + 64^3/3)'},
+           'workspace_bytes': ws_bytes,
+           'timing': 'cuda-graph replay, median of %d, inputs larger than L2 (no flush)' % steps}
+    del graphs, bufs, wsp, x, z
+    torch.cuda.empty_cache()
+    return out, inp, launches
 
 
 def run_reference(args):
@@ -348,7 +444,7 @@ def run_ours(args):
     t_chunk = timed(run['chunk'])
     t_norm = timed(run['norm'])
     t_fused = timed(run['fused'])
-    ms_step = max_over_ranks(statistics.mean(t_step))
+    ms_step = max_over_ranks(statistics.median(t_step))
     # Kernels of this library per call: conv_gating is one (the tiled pass writes the new conv
     # state itself when there is no state in, as here), chunk prefill one (one sequence: one
     # cooperative solve + scan launch), gated norm one, the fused chunk + norm call one.
@@ -374,13 +470,16 @@ def run_ours(args):
     for _ in range(args.warmup):
         decode_step()
     barrier()
-    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    d0.record(stream)
-    for _ in range(dsteps):
+    # one event pair per step, the steps back to back (the 512 MiB state exceeds L2)
+    dev_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(dsteps)]
+    for e0_, e1_ in dev_evs:
+        e0_.record(stream)
         decode_step()
-    d1.record(stream)
+        e1_.record(stream)
     barrier()
-    ms_dec = max_over_ranks(d0.elapsed_time(d1) / dsteps)
+    t_dec = [a.elapsed_time(b) for a, b in dev_evs]
+    ms_dec = max_over_ranks(statistics.median(t_dec))
     del dS, dcs
 
     # ---------------- end to end through the public API with host buffers
@@ -443,6 +542,16 @@ def run_ours(args):
     e1.record(stream)
     barrier()
     ms_e2e = max_over_ranks(e0.elapsed_time(e1) / args.steps)
+    # ---------------- the packed and the long-context prefill workloads (inputs > L2)
+    del sets, hys
+    torch.cuda.empty_cache()
+    extra = {}
+    extra_launches = 0
+    for key, name in (('varlen', 'varlen_16seq'), ('long_context', 'prefill_t131072')):
+        res, winp, nl = time_prefill_workload(name, args.steps, args.warmup, barrier, max_over_ranks, tc_peak)
+        res['tokens_per_s'] = whole_job_rate(res['tokens'], ws, res['us_per_step'] * 1e-3)
+        extra[key] = (res, winp)
+        extra_launches += nl
     clocks = sampler.stop()
     gdn.check_device_error()
 
@@ -452,10 +561,10 @@ def run_ours(args):
         return
 
     flops = chunk_flops(inp.lengths, sh.Nv, sh.Dk, sh.Dv)
-    us_chunk = statistics.mean(t_chunk) * 1e3
-    us_conv = statistics.mean(t_conv) * 1e3
-    us_norm = statistics.mean(t_norm) * 1e3
-    us_fused = statistics.mean(t_fused) * 1e3
+    us_chunk = statistics.median(t_chunk) * 1e3
+    us_conv = statistics.median(t_conv) * 1e3
+    us_norm = statistics.median(t_norm) * 1e3
+    us_fused = statistics.median(t_fused) * 1e3
     nb = rmsnorm_bytes(T * sh.Nv, sh.Dv)
     tflops = flops / (us_chunk * 1e-6) / 1e12
     cb = conv_gating_bytes(T, 1, sh.C, sh.Nk, sh.Nv, sh.Dk, sh.Dv)
@@ -496,14 +605,21 @@ def run_ours(args):
             'chunk_prefill_gated_norm': {'us': us_fused, 'note': 'one call: chunk prefill with the norm in its epilogue'}},
         'decode': {'workload': 'decode_b256', 'kernel': 'gdn_decode_fused', 'steps': dsteps,
                    'us_per_step': ms_dec * 1e3, 'tokens_per_s': whole_job_rate(B, ws, ms_dec),
+                   'us_per_step_spread': {'min': min(t_dec) * 1e3, 'median': ms_dec * 1e3,
+                                          'p90': sorted(t_dec)[int(0.9 * (len(t_dec) - 1))] * 1e3,
+                                          'max': max(t_dec) * 1e3},
                    'roofline': {'bound': 'hbm', 'achieved': dec_gbs, 'peak': hbm_peak, 'unit': 'GB/s',
                                 'frac': dec_gbs / hbm_peak, 'frac_of_8tbs': dec_gbs / NOMINAL_HBM_GBS,
                                 'bytes_per_launch': dbytes}},
         'e2e': {'value': whole_job_rate(T, ws, ms_e2e), 'unit': 'tokens/s', 'h2d_bytes_per_step': h2d,
                 'd2h_bytes_per_step': d2h, 'ms_per_step': ms_e2e},
-        'gpu_launches': launches_prefill + dsteps + k_step * args.steps,
+        'gpu_launches': launches_prefill + dsteps + k_step * args.steps + extra_launches,
         'clocks': clocks,
     }
+    for key, (res, winp) in extra.items():
+        if ws == 1 and not args.no_cpu_baseline:
+            res['cpu_baseline'] = cpu_baseline(winp, 5.0, res['workload'])
+        line[key] = res
     if ws == 1 and not args.no_cpu_baseline:
         line['cpu_baseline'] = cpu_baseline(inp)
     print(json.dumps(line))

@@ -329,6 +329,30 @@ int gdn_chunk_prefill_static(const gdn_dims* dims, const int32_t* cu_seqlens, co
   return GDN_OK;
 }
 
+int gdn_test_chunk_wait_timeout(const gdn_dims* dims, const void* q, const void* k, const void* v,
+                                const float* g, const float* beta, void* o, void* workspace,
+                                size_t workspace_bytes, int64_t wait_ns, void* stream) {
+  const char* fn = "gdn_test_chunk_wait_timeout";
+  gdn::ChunkArgs p;
+  int st = chunk_common(fn, dims, nullptr, q, k, v, GDN_BF16, g, beta, nullptr, nullptr, o, GDN_BF16, &p);
+  if (st != GDN_OK) return st;
+  if (dims->num_seqs != 1 || dims->total_tokens < 1 || !gdn::chunk_tc_supported(p))
+    return fail(GDN_ERR_UNSUPPORTED, "%s: needs one sequence of bf16 q/k/v with 128-wide heads", fn);
+  if (wait_ns < 1000000 || wait_ns > 10000000000ll)
+    return fail(GDN_ERR_INVALID_ARG, "%s: wait_ns must lie in [1 ms, 10 s]", fn);
+  const size_t need = gdn::chunk_tc_workspace_bytes(dims->num_seqs, dims->total_tokens, dims->num_v_heads);
+  if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))
+    return fail(GDN_ERR_INVALID_ARG, "%s: workspace of %zu bytes (16-byte aligned) required", fn, need);
+  p.scale = 1.0f;
+  p.workspace = workspace;
+  p.workspace_bytes = workspace_bytes;
+  p.wait_ns = (unsigned long long)wait_ns;
+  p.no_solve = 1;
+  cudaError_t e = gdn::launch_chunk_tc(p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  return GDN_OK;
+}
+
 static int recurrent_decode(const char* fn, const gdn_dims* dims, const int32_t* cu_seqlens, const void* q,
                             const void* k, const void* v, int in_dtype, const float* g,
                             const float* beta, float scale, float* state, float* step_states, void* o,

@@ -571,22 +571,38 @@ struct ScanBars {
 };
 static_assert(sizeof(ScanBars) <= 256, "scan barriers fit their slot");
 
-// Bounded wait that also gives up when another role aborted.
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort) {
+// The scan's waits are bounded in time: each gives up after limit_ns of device
+// time (%globaltimer) since it started, or at once when another role of the CTA
+// aborted.  A poll cap far above any limit in use ends the loop even if the timer
+// were not to advance.
+struct WaitCtl {
+  volatile int* abort;
+  uint64_t limit_ns;
+};
+constexpr uint32_t POLL_CAP = 1u << 28;
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const WaitCtl& w) {
   if (mbar_test_wait(bar, parity)) return true;      // already complete: no suspension
-  for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 1; i < POLL_CAP; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 1023u) == 1023u && *abort) return false;
+    if ((i & 1023u) == 0u && (*w.abort || global_ns() - t0 > w.limit_ns)) break;
   }
-  *abort = 1;
+  *w.abort = 1;
   return false;
 }
 
 // Both phases at once: the two completed-phase tests are issued back to back.
-__device__ __forceinline__ bool wait_bar2(uint64_t* b1, uint32_t p1, uint64_t* b2, uint32_t p2, volatile int* abort) {
+__device__ __forceinline__ bool wait_bar2(uint64_t* b1, uint32_t p1, uint64_t* b2, uint32_t p2, const WaitCtl& w) {
   const bool t1 = mbar_test_wait(b1, p1), t2 = mbar_test_wait(b2, p2);
   if (t1 && t2) return true;
-  return (t1 || wait_bar(b1, p1, abort)) && (t2 || wait_bar(b2, p2, abort));
+  return (t1 || wait_bar(b1, p1, w)) && (t2 || wait_bar(b2, p2, w));
 }
 
 // silu(z) = h + h tanh(h), h = z / 2, with the hardware tanh when the result is rounded
@@ -624,19 +640,19 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 // Bounded wait until the solve of one (chunk slot, value head) published
 // its workspace tiles (1), or reported a failure (-1).
-constexpr uint32_t FLAG_WAIT_LIMIT = 1u << 21;
-__device__ __forceinline__ bool wait_flag(const int* f, volatile int* abort) {
-  for (uint32_t i = 0; i < FLAG_WAIT_LIMIT; ++i) {
+__device__ __forceinline__ bool wait_flag(const int* f, const WaitCtl& w) {
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 0; i < POLL_CAP; ++i) {
     int v;
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
     if (v > 0) {
       asm volatile("fence.proxy.async.global;" ::: "memory");   // the tiles are read by the copy engine
       return true;
     }
-    if (v < 0 || *abort) break;
+    if (v < 0 || *w.abort || global_ns() - t0 > w.limit_ns) break;
     __nanosleep(100);
   }
-  *abort = 1;
+  *w.abort = 1;
   return false;
 }
 
@@ -649,6 +665,7 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
                           const CUtensorMap* tmz, const ChunkArgs& p, int h, int s, const int* flags) {
   ScanBars* B = reinterpret_cast<ScanBars*>(sm + K2_BAR);
   volatile int* abort = &B->abort;
+  const WaitCtl wc{abort, p.wait_ns};
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -736,12 +753,12 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
       for (int c = 0; c < n && ok; ++c) {
         // the v tiles first: their buffer frees (the [U~^T | 0] product of chunk c - 2) a
         // period before the stage buffer does
-        ok = wait_flag(flags + (size_t)(slot0 + c) * p.Nv + h, abort);
-        if (ok && c >= 2) ok = wait_bar(&B->ready[c & 1], ((c - 2) >> 1) & 1, abort);   // v tiles free
+        ok = wait_flag(flags + (size_t)(slot0 + c) * p.Nv + h, wc);
+        if (ok && c >= 2) ok = wait_bar(&B->ready[c & 1], ((c - 2) >> 1) & 1, wc);   // v tiles free
         if (!ok) break;
         issue_vt(c);
         vt_issued = c + 1;
-        if (c >= 2) ok = wait_bar(&B->ob[c & 1], ((c - 2) >> 1) & 1, abort);           // stage free
+        if (c >= 2) ok = wait_bar(&B->ob[c & 1], ((c - 2) >> 1) & 1, wc);           // stage free
         if (!ok) break;
         issue_stage(c);
         st_issued = c + 1;
@@ -760,8 +777,8 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
       bool ok = true;
       for (; c < n; ++c) {
         const int b = c & 1;
-        ok = wait_bar(&B->vt[b], (c >> 1) & 1, abort);
-        if (ok && c >= 2) ok = wait_bar(&B->of[b], ((c >> 1) - 1) & 1, abort);   // accumulator b free
+        ok = wait_bar(&B->vt[b], (c >> 1) & 1, wc);
+        if (ok && c >= 2) ok = wait_bar(&B->of[b], ((c >> 1) - 1) & 1, wc);   // accumulator b free
         if (!ok) break;
         tc_fence_after();
         // [U~^T | 0] = V^T [T diag(beta); 0]^T: A = V tiles read MN-major, B = [T diag(beta); 0]
@@ -774,7 +791,7 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
         mma_commit(&B->ready[b]);
         committed = c + 1;
         if (self_load && c + 2 < n) {
-          ok = wait_bar(&B->ready[b], (c >> 1) & 1, abort) && issue_vt(c + 2);   // tiles b consumed
+          ok = wait_bar(&B->ready[b], (c >> 1) & 1, wc) && issue_vt(c + 2);   // tiles b consumed
           if (!ok) break;
           issued = c + 3;
         }
@@ -804,7 +821,7 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
     int c = 0;
     // ok carries each thread's waits of the chunk before (its S^T update, and this chunk's
     // stage and [U~^T | 0] product) into the barrier that precedes this chunk's first product
-    bool ok = n == 0 || wait_bar2(&B->stl[0], 0, &B->ready[0], 0, abort);
+    bool ok = n == 0 || wait_bar2(&B->stl[0], 0, &B->ready[0], 0, wc);
     for (; c < n; ++c) {
       const int b = c & 1;
       const uint32_t st = K2_ST + (uint32_t)b * STAGE_BYTES;
@@ -860,8 +877,8 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
       }
       // each thread awaits the product itself (and the chunk before's O product, which reads
       // the bf16 U^T rewritten below); a failed wait is carried by the barrier below
-      ok = (!out_issues_o || c == 0) ? wait_bar(&B->fg, c & 1, abort)
-                                     : wait_bar2(&B->fg, c & 1, &B->ob[(c - 1) & 1], ((c - 1) >> 1) & 1, abort);
+      ok = (!out_issues_o || c == 0) ? wait_bar(&B->fg, c & 1, wc)
+                                     : wait_bar2(&B->fg, c & 1, &B->ob[(c - 1) & 1], ((c - 1) >> 1) & 1, wc);
       tc_fence_after();
       // E_U: U^T and U^T diag(dec) as bf16 pairs
       {
@@ -894,8 +911,8 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
       }
       // the next chunk's stage and [U~^T | 0] product (normally complete by now) while the
       // S^T update runs, then the update itself
-      ok = c + 1 >= n || wait_bar2(&B->stl[b ^ 1], ((c + 1) >> 1) & 1, &B->ready[b ^ 1], ((c + 1) >> 1) & 1, abort);
-      ok = ok && wait_bar(&B->gh, c & 1, abort);
+      ok = c + 1 >= n || wait_bar2(&B->stl[b ^ 1], ((c + 1) >> 1) & 1, &B->ready[b ^ 1], ((c + 1) >> 1) & 1, wc);
+      ok = ok && wait_bar(&B->gh, c & 1, wc);
       if (!out_issues_o && leader && ok) {
         // O^T += U^T P^T behind the S^T update (the next [U^T | O^T] product's commit covers
         // it before U^T is rewritten)
@@ -966,7 +983,7 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
       const uint32_t st = K2_ST + (uint32_t)b * STAGE_BYTES;
       // O^T += U^T P^T once the state role has U^T as bf16 and its S^T update issued (the
       // update goes first to the tensor pipe: it is on the chain to the next chunk)
-      bool ok = !out_issues_o || wait_bar(&B->ub[b], (c >> 1) & 1, abort);
+      bool ok = !out_issues_o || wait_bar(&B->ub[b], (c >> 1) & 1, wc);
       if (out_issues_o && leader && ok) {
         tc_fence_after();
         const uint32_t idp = idesc_bf16(128, 64, false, false);
@@ -977,7 +994,7 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
         mma_commit(&B->ob[b]);
         g2_issued = c + 1;
       }
-      ok = ok && wait_bar(&B->ob[b], (c >> 1) & 1, abort);
+      ok = ok && wait_bar(&B->ob[b], (c >> 1) & 1, wc);
       if (named_sync_or(3, 128, !ok)) { fail = true; break; }
       tc_fence_after();
       if (self_load && leader && c + 2 < n && issue_stage(c + 2)) issued = c + 3;   // stage b is free now
@@ -1005,7 +1022,7 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
             *reinterpret_cast<bf16*>(box + off) = __float2bfloat16_rn(p.scale * v[r]);
           }
         }
-        const bool zok = wait_bar(&B->zb[b], (c >> 1) & 1, abort);   // z of this chunk in buffer b
+        const bool zok = wait_bar(&B->zb[b], (c >> 1) & 1, wc);   // z of this chunk in buffer b
         if (named_sync_or(3, 128, !zok)) { fail = true; break; }     // (also: the o rows are written)
         // row phase: thread (r, bx) = (ot % 64, ot / 64) owns the 64 Dv columns of row r in
         // box bx (a quarter-warp spans 8 rows of one box: conflict-free 16-byte accesses);
@@ -1262,7 +1279,9 @@ bool fused_device(int* sms) {
 }
 }  // namespace
 
-cudaError_t launch_chunk_tc(const ChunkArgs& p, cudaStream_t s) {
+cudaError_t launch_chunk_tc(const ChunkArgs& args, cudaStream_t s) {
+  ChunkArgs p = args;
+  if (p.wait_ns == 0) p.wait_ns = kDefaultWaitNs;
   if (p.total == 0) {
     // no tokens: the final state is the initial state
     if (p.ST && p.ST != p.S0) {
@@ -1294,10 +1313,12 @@ cudaError_t launch_chunk_tc(const ChunkArgs& p, cudaStream_t s) {
     // that keep the solve about 1.3x ahead.
     const double per_scan = (double)(sms - nscan) / (double)nscan;
     int ngroups = per_scan >= 5.3 ? 1 : (per_scan >= 3.55 ? 2 : 3);
+    if (p.no_solve) ngroups = 0;           // test hook: no flag is ever published
     void* args[] = {&mq, &mk, &mv, &mo, &mz, &pc, &nscan, &nitems, &flags, &ngroups};
     const void* fn = fused_kernels()[(p.out_bf16 ? 0 : 2) + (p.z != nullptr ? 1 : 0)];
     return cudaLaunchCooperativeKernel(fn, dim3(sms), dim3(NT3), args, K3_SMEM, s);
   }
+  if (p.no_solve) return cudaErrorNotSupported;     // the test hook needs the one-sequence launch
   cudaError_t e = cudaFuncSetAttribute(chunk_solve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)S1_SMEM);
   if (e != cudaSuccess) return e;

@@ -83,7 +83,11 @@ struct ChunkArgs {
   const void* z;                                 // [T, Nv, Dv] bf16, or null (plain o)
   const float* norm_w;                           // [Dv]
   float norm_eps;
+  // bound of each wait of the scan on a flag or barrier, in ns of device time (0: the default)
+  unsigned long long wait_ns;
+  int no_solve;                                  // test hook: the one-sequence launch runs no solve
 };
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
 // Portable fp32 CUDA-core implementation of the chunk form.
 cudaError_t launch_chunk_simt(const ChunkArgs& p, cudaStream_t s);
 // tcgen05 tensor-core implementation (bf16 q/k/v, Dk = Dv = 128).

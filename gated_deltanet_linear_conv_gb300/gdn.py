@@ -23,7 +23,7 @@ EXPORTS = ('gdn_version', 'gdn_last_error_string', 'gdn_check_device_error', 'gd
            'gdn_gating', 'gdn_chunk_prefill_workspace_size', 'gdn_chunk_prefill',
            'gdn_chunk_prefill_fp32', 'gdn_chunk_prefill_static', 'gdn_chunk_prefill_gated_norm',
            'gdn_recurrent_decode', 'gdn_recurrent_decode_steps',
-           'gdn_gated_rmsnorm', 'gdn_decode_fused')
+           'gdn_gated_rmsnorm', 'gdn_decode_fused', 'gdn_test_chunk_wait_timeout')
 
 
 class gdn_dims(ctypes.Structure):
@@ -58,6 +58,7 @@ _SIGS = {
     'gdn_gated_rmsnorm': ([_I64, ctypes.c_int32, _P, _I, _P, _I, _P, _F, _P, _I, _P], _I),
     'gdn_decode_fused': ([_DIMS, _P, _I, _P, _P, _P, _P, _P, _P, _P, _F, _F, _P, _P, _P, _F,
                           _P, _I, _P], _I),
+    'gdn_test_chunk_wait_timeout': ([_DIMS, _P, _P, _P, _P, _P, _P, _P, _SZ, _I64, _P], _I),
 }
 
 

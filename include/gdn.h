@@ -32,6 +32,12 @@
  *    that is not monotone or does not end at total_tokens) is detected on the
  *    device: the offending kernel skips the bad sequence and raises a sticky
  *    device error flag, read (and cleared) by gdn_check_device_error().
+ *  - On its first use on a device the library looks up (once, with that device
+ *    current) the device addresses of its own module variables: the error
+ *    flag and the scratch array of gdn_chunk_prefill_static.  Those addresses
+ *    belong to the device's primary context, so resetting the device
+ *    (cudaDeviceReset) or destroying its primary context after the first call
+ *    is not supported: later calls would use stale addresses.
  *
  * Supported sizes: Dk, Dv in {64, 128}; Nv a multiple of Nk; conv kernel 4;
  * chunk 64.  Other sizes return GDN_ERR_UNSUPPORTED.
@@ -318,6 +324,28 @@ int gdn_decode_fused(const gdn_dims* dims,
                      float q_scale, float l2_eps,
                      float* state, const void* z, const float* norm_w, float norm_eps,
                      void* y, int out_dtype, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Test hook (no counterpart on the source pages): failure detection of the
+ * bounded device waits.  Every wait of the chunk-prefill scan on a ready flag
+ * or an mbarrier gives up after a bound of device time (2 s in the calls
+ * above); the CTA then lets its copies and products in flight land, releases
+ * its tensor memory, raises the device error flag with code 2 ("bounded wait
+ * timed out") and exits, and the context stays usable.
+ *
+ * gdn_test_chunk_wait_timeout enqueues the one-sequence chunk-prefill launch
+ * of gdn_chunk_prefill with no solve work, so that no chunk's ready flag is
+ * ever published, and with each wait bounded by wait_ns (1 ms .. 10 s): every
+ * scan's first flag wait runs out while none of its copies or products is in
+ * flight.  Arguments as gdn_chunk_prefill (one sequence, bf16 q/k/v and o,
+ * Dk = Dv = 128, no states); o is not written.  The caller then reads
+ * GDN_ERR_DEVICE from gdn_check_device_error().  Returns GDN_ERR_UNSUPPORTED
+ * when the device cannot hold the one-sequence launch (fewer SMs than value
+ * heads + 1, or no cooperative launch).
+ * ------------------------------------------------------------------------ */
+int gdn_test_chunk_wait_timeout(const gdn_dims* dims, const void* q, const void* k, const void* v,
+                                const float* g, const float* beta, void* o, void* workspace,
+                                size_t workspace_bytes, int64_t wait_ns, void* stream);
 
 #ifdef __cplusplus
 }

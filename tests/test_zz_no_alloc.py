@@ -11,6 +11,7 @@ import math
 import pytest
 import torch
 
+import oracle as O
 from gated_deltanet_linear_conv_gb300 import gdn
 from gated_deltanet_linear_conv_gb300 import inputs as I
 from helpers import TOL_BF16, assert_close, np64
@@ -48,6 +49,33 @@ def test_static_scratch_matches_workspace_call_twice():
         torch.cuda.synchronize()
         assert_close(np64(o), np64(o_ref), TOL_BF16, what=call)
         assert_close(np64(ST), np64(S_ref), TOL_BF16, what=call)
+    gdn.check_device_error()
+
+
+def test_static_scratch_one_sequence_twice():
+    """One sequence takes the one-sequence launch (solve and scan overlapped, the ready
+    flags and the item counter cleared in the shared array by every call): two calls in
+    a row with different data, at the full head count, against the workspace call and
+    the oracle."""
+    shape = I.MixerShape(16, 32, 128, 128)
+    T = 1000
+    assert gdn.chunk_prefill_workspace_size(1, T, 16, 32, 128, 128) <= 32 << 20
+    for call, seed in enumerate((93, 94)):
+        c = I.make_core_inputs(seed, [T], shape, dtype=torch.bfloat16, S0_std=0.05)
+        g, beta = O.gating(np64(c.a), np64(c.b), np64(c.A_log), np64(c.dt_bias))
+        gt, bt = torch.tensor(g, dtype=torch.float32).cuda(), torch.tensor(beta, dtype=torch.float32).cuda()
+        q, k, v, S0 = c.q.cuda(), c.k.cuda(), c.v.cuda(), c.S0.cuda()
+        scale = 1 / math.sqrt(128)
+        o_ref, S_ref = gdn.chunk_prefill(q, k, v, gt, bt, scale, initial_state=S0, out_dtype=torch.float32)
+        o = torch.empty_like(o_ref)
+        ST = torch.empty_like(S_ref)
+        _static_call(q, k, v, gt, bt, scale, S0, ST, o, None, 1)
+        torch.cuda.synchronize()
+        assert_close(np64(o), np64(o_ref), TOL_BF16, what=call)
+        assert_close(np64(ST), np64(S_ref), TOL_BF16, what=call)
+        ro, rS = O.chunk_gated_delta_rule(np64(c.q), np64(c.k), np64(c.v), g, beta, scale, np64(c.S0))
+        assert_close(np64(o), ro, TOL_BF16, what=call)
+        assert_close(np64(ST), rS, TOL_BF16, what=call)
     gdn.check_device_error()
 
 
