@@ -36,6 +36,13 @@ TOL_BF16 = 1e-2
 TOL_ROW_F32 = 1e-3
 TOL_ROW_BF16 = 5e-2
 ROW_FLOOR = 0.25
+# Rows of y = gated_rmsnorm(o, z): the norm divides each row by its own RMS, so a
+# row whose core output o is small by cancellation (q nearly orthogonal to the
+# state's rows) keeps the state's bf16 rounding error relative to itself, and the
+# floor above cannot act (every y row has a typical norm); the o rows themselves
+# are checked at TOL_ROW_BF16.  Measured at the full workloads: worst y row 0.11
+# of the 131,072 rows of prefill_t4096.  An entirely wrong row scores about sqrt(2).
+TOL_ROW_Y_BF16 = 0.25
 
 
 def row_rel_err(x, ref):
