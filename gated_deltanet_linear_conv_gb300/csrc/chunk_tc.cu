@@ -93,23 +93,6 @@ __device__ __forceinline__ void tm_ld64(uint32_t taddr, float (&v)[64]) {
   for (int i = 0; i < 32; ++i) { v[i] = a[i]; v[32 + i] = b[i]; }
 }
 
-// Scale the 64 rows of a swizzled 8 KB bf16 box in place: row r times f[r].
-__device__ __forceinline__ void scale_box(uint8_t* sm, uint32_t box, const float* f, int t, int nt) {
-  for (int off = t * 16; off < 8192; off += nt * 16) {
-    const int row = off >> 7;
-    uint4 u = *reinterpret_cast<const uint4*>(sm + box + off);
-    const float sc = f[row];
-    uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float2 x = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w[i]));
-      __nv_bfloat162 y = __floats2bfloat162_rn(x.x * sc, x.y * sc);
-      w[i] = *reinterpret_cast<uint32_t*>(&y);
-    }
-    *reinterpret_cast<uint4*>(sm + box + off) = make_uint4(w[0], w[1], w[2], w[3]);
-  }
-}
-
 // Inclusive prefix sum of g over the chunk by one warp (lane l owns l, l+32);
 // writes G, gamma = exp(G) and dec = exp(G_L - G).
 __device__ __forceinline__ void chunk_cumsum(float* Gs, float* Gam, float* Dec, float* Alp, int lane) {
@@ -156,21 +139,6 @@ constexpr uint32_t S1_VEC = S1_XS + 32 * 36 * 4;    // G, beta, beta*gamma, gamm
 constexpr uint32_t S1_BAR = S1_VEC + 6 * 64 * 4;
 constexpr uint32_t S1_SMEM = S1_BAR + 64 + 1024;
 static_assert(S1_TR % 1024 == 0 && S1_AT % 1024 == 0, "tile alignment");
-
-// Write 64 bf16 values as swizzled row `row` of a 64-column block in global memory.
-__device__ __forceinline__ void st_row64_global(uint8_t* dst, uint32_t row, const float* v, float sc) {
-#pragma unroll
-  for (int ch = 0; ch < 8; ++ch) {
-    uint32_t w[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      __nv_bfloat162 h = __floats2bfloat162_rn(sc * v[ch * 8 + 2 * i], sc * v[ch * 8 + 2 * i + 1]);
-      w[i] = *reinterpret_cast<uint32_t*>(&h);
-    }
-    const uint32_t off = row * 128u + ((((uint32_t)ch ^ (row & 7u)) & 7u) << 4);
-    *reinterpret_cast<uint4*>(dst + off) = make_uint4(w[0], w[1], w[2], w[3]);
-  }
-}
 
 // T = (I + A)^-1 for a 64 x 64 strictly lower A given transposed (AT[k][i] =
 // A[i][k], stride FS), by 128 threads into TR (row-major, stride FS; TR must
@@ -273,13 +241,62 @@ __device__ __forceinline__ void invert_unit_lower(const float* AT, float* TR, fl
   named_sync(barid, 128);
 }
 
+// Token range of chunk slot `slot`: false when the slot holds no chunk (past the end
+// of its sequence, or a sequence whose bounds are inconsistent: the scan reports that).
+__device__ __forceinline__ bool slot_chunk(const ChunkArgs& p, int slot, int& c0, int& len) {
+  int lo = 0, hi = p.num_seqs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (slot_base(p, mid) <= slot) lo = mid; else hi = mid - 1;
+  }
+  const int s = lo, c = slot - slot_base(p, s);
+  int bos, eos;
+  if (!seq_bounds(p.cu, p.num_seqs, p.total, s, bos, eos)) return false;
+  if (c < 0 || c * CT >= eos - bos) return false;
+  c0 = bos + c * CT;
+  len = min(CT, eos - c0);
+  return true;
+}
+
+// This thread's gate value of an item: g (threads 0-63) or beta (threads 64-127) of
+// token c0 + tid % 64 of value head h; 0 past the chunk's end.
+__device__ __forceinline__ float solve_gate(const ChunkArgs& p, int tid, int c0, int len, int h) {
+  return (tid & 63) < len ? __ldg((tid < CT ? p.g : p.beta) + (size_t)(c0 + (tid & 63)) * p.Nv + h) : 0.f;
+}
+
+// The Q and K tiles of an item into the group's QK buffer (thread 0).
+__device__ __forceinline__ void solve_load_tiles(uint8_t* sm, uint64_t* bar, const CUtensorMap* tmq,
+                                                 const CUtensorMap* tmk, const ChunkArgs& p, int c0, int h) {
+  const int hk = h / (p.Nv / p.Nk);
+  mbar_arrive_expect_tx(bar, 32768);
+  tma_load_2d(sm + S1_QK, tmk, bar, hk * DK, c0);
+  tma_load_2d(sm + S1_QK + 8192, tmq, bar, hk * DK, c0);
+  tma_load_2d(sm + S1_QK + 16384, tmk, bar, hk * DK + 64, c0);
+  tma_load_2d(sm + S1_QK + 24576, tmq, bar, hk * DK + 64, c0);
+}
+
+// Loads of the next item that a group issues while it works on the current one.
+struct SolveAhead {
+  bool tiles;    // its Q, K tiles were issued into the QK buffer (on the group's mbarrier)
+  bool gate;     // gb holds this thread's gate value of it
+  float gb;
+};
+
 // One (chunk slot, value head) by 128 threads (tid 0-127 of a group that
 // synchronises on named barrier barid).  sm is the group's 1024-aligned
 // shared memory (S1_BYTES), bar an initialised mbarrier whose next phase
 // parity is ph & 1 (ph advances by three), tbase 128 allocated tensor-memory
-// columns.  Returns false, with the device error flag raised, on a timeout.
+// columns.  The item's tiles are built in shared memory and written to the
+// workspace by bulk copies of whole tiles (P staged in the T buffer, T diag(beta)
+// there too, diag(gamma) Q over the Q tiles and -W over the K tiles, so that the
+// 32 KB [-W | Q~] block leaves in one copy); thread 0 has waited for every copy to
+// complete when this returns.  `ahead` carries the loads of the next item
+// (nslot < 0: none) that this item issues: its gate values during the inverse,
+// and its Q, K tiles once this item's copies have left the QK buffer.
+// Returns false, with the device error flag raised, on a timeout.
 __device__ bool solve_item(uint8_t* sm, int tid, uint32_t barid, uint64_t* bar, uint32_t& ph, uint32_t tbase,
-                           const CUtensorMap* tmq, const CUtensorMap* tmk, const ChunkArgs& p, int slot, int h) {
+                           const CUtensorMap* tmq, const CUtensorMap* tmk, const ChunkArgs& p, int slot, int h,
+                           SolveAhead& ahead, int nslot, int nh) {
   float* AT = reinterpret_cast<float*>(sm + S1_AT);
   float* TR = reinterpret_cast<float*>(sm + S1_TR);
   float* XS = reinterpret_cast<float*>(sm + S1_XS);
@@ -290,35 +307,21 @@ __device__ bool solve_item(uint8_t* sm, int tid, uint32_t barid, uint64_t* bar, 
   float* Dec = Gam + CT;
   float* Alp = Dec + CT;                 // e^(G_t - G_(t-1))
   const int warp = tid >> 5, lane = tid & 31;
-  const int hk = h / (p.Nv / p.Nk);
-
-  // slot -> (sequence, chunk)
-  int lo = 0, hi = p.num_seqs - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (slot_base(p, mid) <= slot) lo = mid; else hi = mid - 1;
+  int c0 = 0, len = 0;
+  const bool used = slot_chunk(p, slot, c0, len);
+  int nc0 = 0, nlen = 0;
+  const bool nused = nslot >= 0 && slot_chunk(p, nslot, nc0, nlen);
+  if (!used) {                // nothing to solve (tiles are only ever prefetched for used slots)
+    ahead.gate = false;
+    return true;
   }
-  const int s = lo, c = slot - slot_base(p, s);
-  int bos, eos;
-  if (!seq_bounds(p.cu, p.num_seqs, p.total, s, bos, eos)) return true;   // reported by the scan
-  if (c < 0 || c * CT >= eos - bos) return true;                           // slot not used
-  const int c0 = bos + c * CT, len = min(CT, eos - c0);
   uint8_t* ws = static_cast<uint8_t*>(p.workspace) + ((size_t)slot * p.Nv + h) * TILE_T_BYTES;
   const uint32_t lane_base = tbase + ((uint32_t)(warp * 32) << 16);
   const uint32_t sb = smem_u32(sm);
 
-  if (tid == 0) {
-    mbar_arrive_expect_tx(bar, 32768);
-    tma_load_2d(sm + S1_QK, tmk, bar, hk * DK, c0);
-    tma_load_2d(sm + S1_QK + 8192, tmq, bar, hk * DK, c0);
-    tma_load_2d(sm + S1_QK + 16384, tmk, bar, hk * DK + 64, c0);
-    tma_load_2d(sm + S1_QK + 24576, tmq, bar, hk * DK + 64, c0);
-  }
-  // threads 0-63 read g, threads 64-127 read beta; the zeroing of T (which starts at zero
-  // above its diagonal blocks) runs while the loads are in flight
-  const float gb = (tid & 63) < len ? (tid < CT ? p.g : p.beta)[(size_t)(c0 + (tid & 63)) * p.Nv + h] : 0.f;
-  for (int i = tid * 4; i < 64 * FS; i += 128 * 4)
-    *reinterpret_cast<float4*>(TR + i) = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (tid == 0 && !ahead.tiles) solve_load_tiles(sm, bar, tmq, tmk, p, c0, h);
+  // threads 0-63 hold g, threads 64-127 beta (loaded during the item before, else now)
+  const float gb = ahead.gate ? ahead.gb : solve_gate(p, tid, c0, len, h);
   (tid < CT ? Gs : Bet)[tid & 63] = gb;
   named_sync(barid, 128);
   if (warp == 0) {
@@ -343,6 +346,9 @@ __device__ bool solve_item(uint8_t* sm, int tid, uint32_t barid, uint64_t* bar, 
     ok = mbar_wait(bar, ph & 1u, WAIT_LIMIT);
   }
   ph += 1;
+  // the next item's gate value, in flight under this item's work
+  ahead.gate = nused;
+  if (nused) ahead.gb = solve_gate(p, tid, nc0, nlen, nh);
   bool done = false;
   if (!named_sync_or(barid, 128, !ok)) {
     tc_fence_after();
@@ -376,7 +382,8 @@ __device__ bool solve_item(uint8_t* sm, int tid, uint32_t barid, uint64_t* bar, 
         for (int r = 0; r < 64; r += 4)
           *reinterpret_cast<float4*>(AT + j * FS + r) = make_float4(v[r], v[r + 1], v[r + 2], v[r + 3]);
       } else {
-        // row r of P = M o Q K^T: (q_r . k_j) e^(G_r - G_j) for j <= r, the product taken from j = r down
+        // row r of P = M o Q K^T: (q_r . k_j) e^(G_r - G_j) for j <= r, the product taken from j = r
+        // down; staged as a swizzled bf16 row in the T buffer (zeroed again before the inverse)
         const int r = tid - CT;
         float cur = 1.f;
 #pragma unroll
@@ -394,11 +401,10 @@ __device__ bool solve_item(uint8_t* sm, int tid, uint32_t barid, uint64_t* bar, 
             v[j] = j <= r ? v[j] * cur : 0.f;
           }
         }
-        st_row64_global(ws + WS_P, r, v, 1.f);
+        st_row64(sm, S1_TR, r, v);
       }
     }
-    // diag(gamma) Q -> rows 64-127 of the two [-W; Q~] blocks (same swizzled rows as
-    // the TMA tiles), then dec and gamma_L
+    // diag(gamma) Q in place over the Q tiles (same swizzled rows), then dec and gamma_L
     {
       uint4 qu[8];
       float f[8];
@@ -420,20 +426,31 @@ __device__ bool solve_item(uint8_t* sm, int tid, uint32_t barid, uint64_t* bar, 
           __nv_bfloat162 y = __floats2bfloat162_rn(x.x * f[k], x.y * f[k]);
           w[j] = *reinterpret_cast<uint32_t*>(&y);
         }
-        *reinterpret_cast<uint4*>(ws + WS_QW + 8192 + off) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(sm + S1_QK + 8192 + off) = make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
     if (tid < CT) reinterpret_cast<float*>(ws + WS_VEC)[tid] = Dec[tid];
     if (tid == 0) reinterpret_cast<float*>(ws + WS_VEC)[CT] = Gam[CT - 1];
+    fence_proxy_async_smem();        // P is read by the copy engine next
     tc_fence_before();
+    named_sync(barid, 128);
+    if (tid == 0) {
+      bulk_store(ws + WS_P, sm + S1_TR, 8192);
+      bulk_commit_group();
+      bulk_wait_read<0>();           // the T buffer is free again
+    }
+    named_sync(barid, 128);
+    for (int i = tid * 4; i < 64 * FS; i += 128 * 4)   // T starts at zero above its diagonal blocks
+      *reinterpret_cast<float4*>(TR + i) = make_float4(0.f, 0.f, 0.f, 0.f);
     named_sync(barid, 128);
     invert_unit_lower(AT, TR, XS, tid, barid);
     // A^T is dead: its space becomes the [T diag(beta gamma); T diag(beta gamma)] operand (the
-    // rows twice, so that all four warps take a share of W out of tensor memory)
+    // rows twice, so that all four warps take a share of W out of tensor memory); T diag(beta)
+    // is staged over T
     uint8_t* tbg = sm + S1_AT;
     {
-      // thread (r, ch) = (tid / 8 + 16 k, tid % 8): every read of T, beta and beta gamma
-      // before the first store (the stores go over the dead A^T)
+      // thread (r, ch) = (tid / 8 + 16 k, tid % 8): every read of T, beta and beta gamma,
+      // then a barrier, then the stores
       const int ch = tid & 7;
       float4 t0[4], t1[4];
 #pragma unroll
@@ -448,6 +465,7 @@ __device__ bool solve_item(uint8_t* sm, int tid, uint32_t barid, uint64_t* bar, 
       const float4 bg1 = *reinterpret_cast<const float4*>(BG + ch * 8 + 4);
       const float be[8] = {be0.x, be0.y, be0.z, be0.w, be1.x, be1.y, be1.z, be1.w};
       const float bgv[8] = {bg0.x, bg0.y, bg0.z, bg0.w, bg1.x, bg1.y, bg1.z, bg1.w};
+      named_sync(barid, 128);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int r = (tid >> 3) + 16 * k;
@@ -461,7 +479,7 @@ __device__ bool solve_item(uint8_t* sm, int tid, uint32_t barid, uint64_t* bar, 
           wb[i] = *reinterpret_cast<uint32_t*>(&hb);
         }
         const uint32_t sw = r * 128u + ((((uint32_t)ch ^ (uint32_t)(r & 7)) & 7u) << 4);
-        *reinterpret_cast<uint4*>(ws + WS_TB + sw) = make_uint4(wa[0], wa[1], wa[2], wa[3]);
+        *reinterpret_cast<uint4*>(sm + S1_TR + sw) = make_uint4(wa[0], wa[1], wa[2], wa[3]);
         *reinterpret_cast<uint4*>(tbg + sw) = make_uint4(wb[0], wb[1], wb[2], wb[3]);
         *reinterpret_cast<uint4*>(tbg + 8192 + sw) = make_uint4(wb[0], wb[1], wb[2], wb[3]);
       }
@@ -471,6 +489,8 @@ __device__ bool solve_item(uint8_t* sm, int tid, uint32_t barid, uint64_t* bar, 
     named_sync(barid, 128);
     tc_fence_after();
     if (tid == 0) {
+      bulk_store(ws + WS_TB, sm + S1_TR, 8192);
+      bulk_commit_group();
       // W = T diag(beta gamma) K, in rows 0-63 and again in rows 64-127 of the 128 x 128 result
       const uint32_t id = idesc_bf16(128, 128, false, true);
       const uint64_t a = sdesc_sw128(sb + S1_AT, 16, 1024);
@@ -482,22 +502,48 @@ __device__ bool solve_item(uint8_t* sm, int tid, uint32_t barid, uint64_t* bar, 
     ok = mbar_wait(bar, ph & 1u, WAIT_LIMIT);
     if (!named_sync_or(barid, 128, !ok)) {
       tc_fence_after();
-      {   // warps 0-1: columns 0-63 of rows 0-63; warps 2-3: columns 64-127 of the copy
+      {   // -W over the K tiles: warps 0-1 columns 0-63 of rows 0-63, warps 2-3 columns 64-127 of the copy
         const int half = tid >> 6;
         float v[64];
         tm_ld64(lane_base + half * 64, v);
-        st_row64_global(ws + WS_QW + half * 16384, tid & 63, v, -1.f);
+#pragma unroll
+        for (int i = 0; i < 64; ++i) v[i] = -v[i];
+        st_row64(sm, S1_QK + half * 16384, tid & 63, v);
+      }
+      fence_proxy_async_smem();
+      named_sync(barid, 128);
+      if (tid == 0) {
+        bulk_store(ws + WS_QW, sm + S1_QK, 32768);   // [-W | Q~ | -W | Q~]
+        bulk_commit_group();
       }
       done = true;
     }
   }
   ph += 1;
   if (!done && tid == 0) raise_error(p.err, kDevErrTimeout);
+  if (tid == 0) {
+    bulk_wait_all();                 // every copy of this item complete (its writes performed)
+    fence_proxy_async_global();
+  }
+  __threadfence();                   // this thread's direct stores (dec, gamma_L) likewise
   // the next item may reuse this shared and tensor memory
   tc_fence_before();
   named_sync(barid, 128);
   tc_fence_after();
+  ahead.tiles = false;
   return done;
+}
+
+// After the item's flag is published: thread 0 issues the next item's tile loads into
+// the (now free) QK buffer.
+__device__ __forceinline__ void solve_prefetch_tiles(uint8_t* sm, int tid, uint64_t* bar, const CUtensorMap* tmq,
+                                                     const CUtensorMap* tmk, const ChunkArgs& p, SolveAhead& ahead,
+                                                     int nslot, int nh) {
+  int nc0 = 0, nlen = 0;
+  if (nslot >= 0 && slot_chunk(p, nslot, nc0, nlen)) {
+    if (tid == 0) solve_load_tiles(sm, bar, tmq, tmk, p, nc0, nh);
+    ahead.tiles = true;
+  }
 }
 
 __global__ void __launch_bounds__(128, 3)
@@ -517,7 +563,8 @@ chunk_solve_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
   __syncthreads();
   tc_fence_after();
   uint32_t ph = 0;
-  solve_item(sm, tid, 1, bar, ph, *tslot, &tmq, &tmk, p, blockIdx.x, blockIdx.y);
+  SolveAhead ahead{false, false, 0.f};
+  solve_item(sm, tid, 1, bar, ph, *tslot, &tmq, &tmk, p, blockIdx.x, blockIdx.y, ahead, -1, 0);
   if ((tid >> 5) == 0) tmem_dealloc(*tslot, 128);
 }
 
@@ -656,13 +703,35 @@ __device__ __forceinline__ bool wait_flag(const int* f, const WaitCtl& w) {
   return false;
 }
 
+// What one scan CTA covers of its (sequence, value head): a range of its chunks,
+// the state it starts from, and where its final state and output rows go.
+//  - the whole sequence: S0 = the caller's initial state (or zeros), outputs to o;
+//  - a later segment of a split sequence, from a zero state (its part of the state
+//    and of the outputs that does not depend on the state it is entered with);
+//  - that segment's transition map: the identity as the state (Dk = Dv) and no V
+//    term, so that its "state" after chunk c is the product A_c ... A_first of the
+//    chunk maps S -> A S of the homogeneous recurrence, and its "output" rows are
+//    the response R of the chunk's outputs to the entry state (o += R S_entry).
+struct ScanSeg {
+  int c_begin, c_end;        // chunk range [c_begin, c_end) of the sequence (clipped to its end)
+  const float* S0;           // initial state [Dk][Dv] of this (sequence, head), or null (zeros)
+  bool identity;             // start from the identity instead (the transition map)
+  bool zero_v;               // no V term: U~ = 0
+  float* ST;                 // final state [Dk][Dv], or null (not written)
+  void* out;                 // output rows [rows, Nv, Dv]: Tout, or bf16 when out_bf16
+  bool out_bf16;             // the rows are bf16 whatever Tout is
+  const CUtensorMap* tmo;    // bf16 map over `out` (used for bf16 rows of whole chunks)
+  int row_off;               // token t is output row t - row_off
+};
+
 // The scan of one (sequence s, value head h) by the CTA's warps 0-8 (more
 // warps may be present; they only join the final barrier).  sm is 1024-aligned
 // shared memory of K2 bytes.  With `flags`, every chunk's workspace tiles are
 // awaited before they are loaded (the solve runs concurrently in other CTAs).
 template <typename Tout, bool NORM>
-__device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap* tmv, const CUtensorMap* tmo,
+__device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap* tmv, const ScanSeg& sg,
                           const CUtensorMap* tmz, const ChunkArgs& p, int h, int s, const int* flags) {
+  const CUtensorMap* tmo = sg.tmo;
   ScanBars* B = reinterpret_cast<ScanBars*>(sm + K2_BAR);
   volatile int* abort = &B->abort;
   const WaitCtl wc{abort, p.wait_ns};
@@ -676,8 +745,13 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
     if (tid == 0 && h == 0) raise_error(p.err, kDevErrSeqlens);
     return;
   }
+  const int slot0 = slot_base(p, s) + sg.c_begin;
+  {
+    const int seq_bos = bos;
+    bos = min(eos, seq_bos + sg.c_begin * CT);
+    if (sg.c_end < (eos - seq_bos + CT - 1) / CT) eos = seq_bos + sg.c_end * CT;
+  }
   const int n = (eos - bos + CT - 1) / CT;
-  const int slot0 = slot_base(p, s);
   const uint8_t* wsb = static_cast<const uint8_t*>(p.workspace);
   auto ws_tile = [&](int c) { return wsb + ((size_t)(slot0 + c) * p.Nv + h) * TILE_T_BYTES; };
 
@@ -754,10 +828,13 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
         // the v tiles first: their buffer frees (the [U~^T | 0] product of chunk c - 2) a
         // period before the stage buffer does
         ok = wait_flag(flags + (size_t)(slot0 + c) * p.Nv + h, wc);
-        if (ok && c >= 2) ok = wait_bar(&B->ready[c & 1], ((c - 2) >> 1) & 1, wc);   // v tiles free
+        if (!sg.zero_v) {
+          if (ok && c >= 2) ok = wait_bar(&B->ready[c & 1], ((c - 2) >> 1) & 1, wc);   // v tiles free
+          if (!ok) break;
+          issue_vt(c);
+          vt_issued = c + 1;
+        }
         if (!ok) break;
-        issue_vt(c);
-        vt_issued = c + 1;
         if (c >= 2) ok = wait_bar(&B->ob[c & 1], ((c - 2) >> 1) & 1, wc);           // stage free
         if (!ok) break;
         issue_stage(c);
@@ -766,6 +843,17 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
       if (!ok) {     // let the copies in flight land (the waits are bounded)
         for (int k = max(st_issued - 2, 0); k < st_issued; ++k) mbar_wait(&B->stl[k & 1], (k >> 1) & 1, WAIT_LIMIT);
         for (int k = max(vt_issued - 2, 0); k < vt_issued; ++k) mbar_wait(&B->vt[k & 1], (k >> 1) & 1, WAIT_LIMIT);
+      }
+    }
+  } else if (warp == 0 && sg.zero_v) {
+    // ============================== PREP (no V term) ==============================
+    // the [U^T | O^T] product starts its accumulator afresh; PREP only hands each
+    // accumulator on once OUT has finished reading it
+    if (lane == 0) {
+      for (int c = 0; c < n; ++c) {
+        const int b = c & 1;
+        if (c >= 2 && !wait_bar(&B->of[b], ((c >> 1) - 1) & 1, wc)) break;
+        mbar_arrive(&B->ready[b]);
       }
     }
   } else if (warp == 0) {
@@ -805,13 +893,14 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
     // ============================== STATE ==============================
     const bool leader = tid == 32;
     {
-      // S^T <- initial state (S0 is [dk][dv]: thread dv reads a column)
-      const float* src = p.S0 ? p.S0 + ((size_t)s * p.Nv + h) * DK * DV + dv : nullptr;
+      // S^T <- initial state (S0 is [dk][dv]: thread dv reads a column), or the identity
+      const float* src = sg.S0 ? sg.S0 + dv : nullptr;
 #pragma unroll
       for (int c0 = 0; c0 < DK; c0 += 32) {
         float v[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = src ? __ldg(src + (size_t)(c0 + i) * DV) : 0.f;
+        for (int i = 0; i < 32; ++i)
+          v[i] = sg.identity ? (c0 + i == dv ? 1.f : 0.f) : (src ? __ldg(src + (size_t)(c0 + i) * DV) : 0.f);
         tmem_st32(lane_base + TM_S + c0, v);
       }
       tmem_st_wait();
@@ -853,7 +942,8 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
         const uint64_t bq = sdesc_sw128(sb + st, 16, 1024);
 #pragma unroll
         for (int ks = 0; ks < DK / 16; ++ks)
-          mma_bf16_ta(tbase + TM_ACC + b * 128, tbase + TM_SB + ks * 8, bq + (ks >> 2) * 1024 + (ks & 3) * 2, id, 1u);
+          mma_bf16_ta(tbase + TM_ACC + b * 128, tbase + TM_SB + ks * 8, bq + (ks >> 2) * 1024 + (ks & 3) * 2, id,
+                      (ks > 0 || !sg.zero_v) ? 1u : 0u);
         mma_commit(&B->fg);
         fg_issued = c + 1;
       }
@@ -934,8 +1024,8 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
         if (gh_issued > 0) mbar_wait(&B->gh, (gh_issued - 1) & 1, WAIT_LIMIT);
         if (ob_issued > 0) mbar_wait(&B->ob[(ob_issued - 1) & 1], ((ob_issued - 1) >> 1) & 1, WAIT_LIMIT);
       }
-    } else if (p.ST) {
-      float* dst = p.ST + ((size_t)s * p.Nv + h) * DK * DV + dv;
+    } else if (sg.ST) {
+      float* dst = sg.ST + dv;
 #pragma unroll
       for (int c0 = 0; c0 < DK; c0 += 32) {
         float v[32];
@@ -949,8 +1039,9 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
   } else if (warp <= 8) {
     // ============================== OUT ==============================
     const bool leader = tid == 160;
-    Tout* o = static_cast<Tout*>(p.o);
+    Tout* o = static_cast<Tout*>(sg.out);
     constexpr bool kBf16Out = sizeof(Tout) == 2;
+    const bool rows_bf16 = kBf16Out || sg.out_bf16;
     int issued = 0;
     if (leader && self_load)
       while (issued < n && issued < 2 && issue_stage(issued)) ++issued;
@@ -1000,7 +1091,7 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
       if (self_load && leader && c + 2 < n && issue_stage(c + 2)) issued = c + 3;   // stage b is free now
       float v[64];
       tm_ld64(lane_base + TM_ACC + b * 128 + 64, v);   // lane dv holds O[0..63][dv]
-      const bool use_tma = kBf16Out && len == CT;
+      const bool use_tma = rows_bf16 && len == CT;
       if (leader) {
         // the stores that read the buffers have left them (with the norm, the other
         // buffer holds this chunk's o rows next)
@@ -1100,15 +1191,22 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
         fence_proxy_async_smem();
         named_sync(3, 128);
         if (leader) {
-          tma_store_2d(tmo, os, h * DV, c0);
-          tma_store_2d(tmo, os + 8192, h * DV + 64, c0);
+          tma_store_2d(tmo, os, h * DV, c0 - sg.row_off);
+          tma_store_2d(tmo, os + 8192, h * DV + 64, c0 - sg.row_off);
           bulk_commit_group();
         }
       } else {
-        Tout* dst = o + ((size_t)c0 * p.Nv + h) * DV + dv;
+        if (rows_bf16) {          // (bf16 rows with fp32 outputs: the map scan's response rows)
+          bf16* dst = static_cast<bf16*>(sg.out) + ((size_t)(c0 - sg.row_off) * p.Nv + h) * DV + dv;
 #pragma unroll
-        for (int r = 0; r < CT; ++r)
-          if (r < len) dst[(size_t)r * p.Nv * DV] = from_f32<Tout>(p.scale * v[r]);
+          for (int r = 0; r < CT; ++r)
+            if (r < len) dst[(size_t)r * p.Nv * DV] = __float2bfloat16_rn(p.scale * v[r]);
+        } else {
+          Tout* dst = o + ((size_t)(c0 - sg.row_off) * p.Nv + h) * DV + dv;
+#pragma unroll
+          for (int r = 0; r < CT; ++r)
+            if (r < len) dst[(size_t)r * p.Nv * DV] = from_f32<Tout>(p.scale * v[r]);
+        }
       }
     }
     if (leader) {
@@ -1127,13 +1225,31 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
   if (warp == 0) tmem_dealloc(tbase, 512);
 }
 
+// The whole of sequence s for value head h: the caller's states and output rows.
+__device__ __forceinline__ ScanSeg whole_seq(const ChunkArgs& p, int h, int s, const CUtensorMap* tmo) {
+  ScanSeg sg;
+  const size_t hs = ((size_t)s * p.Nv + h) * DK * DV;
+  sg.c_begin = 0;
+  sg.c_end = 0x7fffffff;
+  sg.S0 = p.S0 ? p.S0 + hs : nullptr;
+  sg.identity = false;
+  sg.zero_v = false;
+  sg.ST = p.ST ? p.ST + hs : nullptr;
+  sg.out = p.o;
+  sg.out_bf16 = false;
+  sg.tmo = tmo;
+  sg.row_off = 0;
+  return sg;
+}
+
 template <typename Tout, bool NORM>
 __global__ void __launch_bounds__(NT2, 1)
 chunk_scan_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   const __grid_constant__ CUtensorMap tmo, const __grid_constant__ CUtensorMap tmz, ChunkArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  scan_body<Tout, NORM>(sm, &tmk, &tmv, &tmo, &tmz, p, blockIdx.x, blockIdx.y, nullptr);
+  const ScanSeg sg = whole_seq(p, blockIdx.x, blockIdx.y, &tmo);
+  scan_body<Tout, NORM>(sm, &tmk, &tmv, sg, &tmz, p, blockIdx.x, blockIdx.y, nullptr);
 }
 
 // ---------------------------------------------------------------------------
@@ -1158,22 +1274,79 @@ __device__ __forceinline__ void st_release(int* f, int v) {
   asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
 }
 
+// A sequence split in two segments (nseg = 2): chunks [0, m) and [m, n).  Scratch in
+// the workspace: the first segment's final state S_mid, the second's final state from
+// zero Bst and its transition map Phi ([Nv][Dk][Dv] fp32 each), and the map scan's
+// response rows R (bf16 [tokens - 64 m, Nv, Dk]).
+struct SplitArgs {
+  int nseg, m, n;
+  float* S_mid;
+  float* Bst;
+  float* Phi;
+  bf16* R;
+};
+
+// Solve item k of the one-sequence launch -> (chunk, value head).  Split in two
+// segments, the chunks of both are interleaved (chunk c of the first segment, then
+// chunk m + c of the second), so that both segments' scans get their tiles in order.
+__device__ __forceinline__ void item_chunk(const SplitArgs& sp, int Nv, int k, int& c, int& h) {
+  if (sp.nseg == 1) {
+    c = k / Nv;
+    h = k % Nv;
+    return;
+  }
+  const int n1 = sp.n - sp.m;                 // chunks of the second segment (<= m)
+  const int inter = 2 * n1 * Nv;
+  if (k < inter) {
+    const int pr = k / (2 * Nv), seg = (k / Nv) & 1;
+    h = k % Nv;
+    c = seg ? sp.m + pr : pr;
+  } else {
+    const int k2 = k - inter;
+    c = n1 + k2 / Nv;
+    h = k2 % Nv;
+  }
+}
+
 template <typename Tout, bool NORM>
 __global__ void __launch_bounds__(NT3, 1)
 chunk_fused_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo,
-                   const __grid_constant__ CUtensorMap tmz, ChunkArgs p, int nscan, int nitems, int* flags,
-                   int ngroups) {
+                   const __grid_constant__ CUtensorMap tmz, const __grid_constant__ CUtensorMap tmr, ChunkArgs p,
+                   SplitArgs sp, int nscan, int nitems, int* flags, int ngroups) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   if ((int)blockIdx.x < nscan) {
-    scan_body<Tout, NORM>(sm, &tmk, &tmv, &tmo, &tmz, p, blockIdx.x % p.Nv, blockIdx.x / p.Nv, flags);
+    const int role = blockIdx.x / p.Nv, h = blockIdx.x % p.Nv;
+    ScanSeg sg = whole_seq(p, h, 0, &tmo);
+    if (sp.nseg == 2) {
+      const size_t hs = (size_t)h * DK * DV;
+      if (role == 0) {                       // first segment: the caller's initial state
+        sg.c_end = sp.m;
+        sg.ST = sp.S_mid + hs;
+      } else if (role == 1) {                // second segment from a zero state
+        sg.c_begin = sp.m;
+        sg.S0 = nullptr;
+        sg.ST = sp.Bst + hs;
+      } else {                               // second segment's transition map
+        sg.c_begin = sp.m;
+        sg.S0 = nullptr;
+        sg.identity = true;
+        sg.zero_v = true;
+        sg.ST = sp.Phi + hs;
+        sg.out = sp.R;
+        sg.out_bf16 = true;
+        sg.tmo = &tmr;
+        sg.row_off = sp.m * CT;
+      }
+    }
+    scan_body<Tout, NORM>(sm, &tmk, &tmv, sg, &tmz, p, h, 0, flags);
     return;
   }
-  const int g = threadIdx.x >> 7, tid = threadIdx.x & 127, warp = tid >> 5;
+  const int g = threadIdx.x >> 7, tid = threadIdx.x & 127;
   uint8_t* gsm = sm + g * S1_GROUP;
   uint64_t* bar = reinterpret_cast<uint64_t*>(gsm + S1_BAR);
-  volatile int* item_slot = reinterpret_cast<volatile int*>(gsm + S1_BAR + 32);
+  volatile int* item_slot = reinterpret_cast<volatile int*>(gsm + S1_BAR + 32);   // two slots
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S1_BAR + 16);        // in group 0's slice
   const uint32_t barid = 1 + g;
   if (tid == 0) {
@@ -1187,21 +1360,216 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
   const uint32_t tbase = *tslot + 128u * (uint32_t)g;
   int* counter = flags + nitems;
   uint32_t ph = 0;
-  for (; g < ngroups;) {
-    if (tid == 0) *item_slot = atomicAdd(counter, 1);
-    named_sync(barid, 128);
-    const int item = *item_slot;
-    named_sync(barid, 128);
-    if (item >= nitems) break;
-    const bool ok = solve_item(gsm, tid, barid, bar, ph, tbase, &tmq, &tmk, p, item / p.Nv, item % p.Nv);
-    __threadfence();                       // this thread's tile stores are visible device-wide
-    named_sync(barid, 128);
-    if (tid == 0) st_release(flags + item, ok ? 1 : -1);
-    if (!ok) break;
+  if (g < ngroups) {
+    // items are claimed one ahead (alternating broadcast slots), so that the next item's
+    // gate values and tiles load under the current one
+    int par = 0;
+    auto claim = [&]() {
+      if (tid == 0) item_slot[par] = atomicAdd(counter, 1);
+      named_sync(barid, 128);
+      const int v = item_slot[par];
+      par ^= 1;
+      return v;
+    };
+    SolveAhead ahead{false, false, 0.f};
+    int item = claim();
+    while (item < nitems) {
+      const int next = claim();
+      int c, h, nc = -1, nh = 0;
+      item_chunk(sp, p.Nv, item, c, h);
+      if (next < nitems) item_chunk(sp, p.Nv, next, nc, nh);
+      const bool ok = solve_item(gsm, tid, barid, bar, ph, tbase, &tmq, &tmk, p, c, h, ahead, nc, nh);
+      if (tid == 0) st_release(flags + (size_t)c * p.Nv + h, ok ? 1 : -1);   // tiles complete (see solve_item)
+      if (!ok) break;
+      if (next < nitems) solve_prefetch_tiles(gsm, tid, bar, &tmq, &tmk, p, ahead, nc, nh);
+      item = next;
+    }
   }
   tc_fence_before();
   __syncthreads();
   if (threadIdx.x < 32) tmem_dealloc(*tslot, 512);
+}
+
+// ---------------------------------------------------------------------------
+// kernel 4: the fix-up of a sequence split in two segments.  With S_mid the state
+// after the first segment (the state the second segment is entered with):
+//   o[t] += R[t] S_mid   for the second segment's tokens (R: the map scan's rows);
+//   S_T   = Bst + Phi S_mid.
+// Output CTAs (the first nout): one value head and a run of 128-token blocks.  Per
+// block D = R_blk S_mid on the tensor core (M = 128 tokens, N = Dv, K = Dk): R by TMA
+// (K-major, two buffers), S_mid converted once to bf16 in shared memory (MN-major);
+// thread t adds row t of D to its output row.  State CTAs: 16 rows of S_T of one
+// head each, in fp32 on CUDA cores.
+// ---------------------------------------------------------------------------
+constexpr int NT4 = 128;
+constexpr uint32_t K4_S = 0;                   // S_mid as bf16: two N blocks of 128 K rows x 128 B
+constexpr uint32_t K4_R = 32768;               // 2 x R block: two K chunks x 128 rows x 128 B
+constexpr uint32_t K4_BAR = K4_R + 2 * 32768;
+constexpr uint32_t K4_SMEM = K4_BAR + 64 + 1024;
+
+struct FixArgs {
+  const float* S_mid;
+  const float* Bst;
+  const float* Phi;
+  float* ST;              // [Nv][Dk][Dv], or null
+  void* o;                // [T, Nv, Dv]
+  int t1;                 // first token of the second segment
+  int T, Nv;
+  int nblk;               // 128-token blocks of the second segment
+  int bpc;                // blocks per output CTA
+  int cph;                // output CTAs per head
+  int* err;
+};
+
+template <typename Tout>
+__global__ void __launch_bounds__(NT4)
+chunk_fixup_kernel(const __grid_constant__ CUtensorMap tmr, FixArgs f) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int nout = f.cph * f.Nv;
+  if ((int)blockIdx.x >= nout) {
+    // ---- S_T = Bst + Phi S_mid: thread (row i, 16 columns from c0)
+    if (f.ST == nullptr) return;
+    const int id = blockIdx.x - nout;
+    const int h = id >> 3, i = (id & 7) * 16 + (tid >> 3), c0 = (tid & 7) * 16;
+    const size_t hs = (size_t)h * DK * DV;
+    float acc[16];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float4 b4 = __ldg(reinterpret_cast<const float4*>(f.Bst + hs + (size_t)i * DV + c0) + q);
+      acc[4 * q] = b4.x; acc[4 * q + 1] = b4.y; acc[4 * q + 2] = b4.z; acc[4 * q + 3] = b4.w;
+    }
+    const float* phi = f.Phi + hs + (size_t)i * DK;
+#pragma unroll 4
+    for (int j = 0; j < DK; ++j) {
+      const float a = __ldg(phi + j);
+      const float4* srow = reinterpret_cast<const float4*>(f.S_mid + hs + (size_t)j * DV + c0);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 s4 = __ldg(srow + q);
+        acc[4 * q] = fmaf(a, s4.x, acc[4 * q]);
+        acc[4 * q + 1] = fmaf(a, s4.y, acc[4 * q + 1]);
+        acc[4 * q + 2] = fmaf(a, s4.z, acc[4 * q + 2]);
+        acc[4 * q + 3] = fmaf(a, s4.w, acc[4 * q + 3]);
+      }
+    }
+    float4* dst = reinterpret_cast<float4*>(f.ST + hs + (size_t)i * DV + c0);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) dst[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+    return;
+  }
+  // ---- o[t] += R[t] S_mid over blocks [b0, b1) of head h
+  const int h = blockIdx.x / f.cph;
+  const int b0 = (blockIdx.x % f.cph) * f.bpc, b1 = min(f.nblk, b0 + f.bpc);
+  uint64_t* rbar = reinterpret_cast<uint64_t*>(sm + K4_BAR);      // [0], [1]: R buffers landed
+  uint64_t* mbar = rbar + 2;                                        // product complete
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + K4_BAR + 32);
+  if (tid == 0) {
+    mbar_init(&rbar[0], 1);
+    mbar_init(&rbar[1], 1);
+    mbar_init(mbar, 1);
+    fence_barrier_init();
+    prefetch_tmap(&tmr);
+  }
+  if (warp == 0) tmem_alloc(tslot, 128);
+  {   // S_mid of head h as the MN-major B operand: K row j = tid, N blocks of 64 columns
+    const float* src = f.S_mid + (size_t)h * DK * DV + (size_t)tid * DV;
+#pragma unroll
+    for (int nb = 0; nb < 2; ++nb) {
+      float v[64];
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        const float4 x = __ldg(reinterpret_cast<const float4*>(src + nb * 64) + q);
+        v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
+      }
+      st_row64(sm, K4_S + nb * 16384, tid, v);
+    }
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+  const uint32_t lane_base = tbase + ((uint32_t)(warp * 32) << 16);
+  const uint32_t sb = smem_u32(sm);
+  auto load_r = [&](int blk, int buf) {
+    uint8_t* dst = sm + K4_R + (uint32_t)buf * 32768u;
+    mbar_arrive_expect_tx(&rbar[buf], 32768);
+#pragma unroll
+    for (int kc = 0; kc < 2; ++kc)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf)
+        tma_load_2d(dst + kc * 16384 + hf * 8192, &tmr, &rbar[buf], h * DK + kc * 64, blk * 128 + hf * 64);
+  };
+  // thread 0 tracks the R loads issued and landed and the products issued, so that a
+  // failed wait still lets everything in flight land before the CTA exits
+  int issued = 0, landed = 0, mma_issued = 0;
+  if (tid == 0 && b0 < b1) {
+    load_r(b0, 0);
+    issued = 1;
+  }
+  bool ok = true;
+  for (int b = b0; b < b1; ++b) {
+    const int it = b - b0, buf = it & 1;
+    bool good = true;
+    if (tid == 0) {
+      // the other buffer's product completed before the last epilogue: it is free
+      if (b + 1 < b1) {
+        load_r(b + 1, buf ^ 1);
+        issued = it + 2;
+      }
+      good = mbar_wait(&rbar[buf], (it >> 1) & 1, WAIT_LIMIT);
+      if (good) {
+        landed = it + 1;
+        tc_fence_after();
+        const uint32_t id = idesc_bf16(128, 128, false, true);
+        const uint64_t a = sdesc_sw128(sb + K4_R + (uint32_t)buf * 32768u, 16, 1024);
+        const uint64_t bs = sdesc_sw128(sb + K4_S, 16384, 1024);
+#pragma unroll
+        for (int ks = 0; ks < DK / 16; ++ks)
+          mma_bf16(tbase, a + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4), bs + ks * 128, id, ks > 0 ? 1u : 0u);
+        mma_commit(mbar);
+        mma_issued = it + 1;
+      }
+    }
+    if (__syncthreads_or(!good)) { ok = false; break; }
+    good = mbar_wait(mbar, it & 1, WAIT_LIMIT);
+    if (__syncthreads_or(!good)) { ok = false; break; }
+    tc_fence_after();
+    const int t = f.t1 + b * 128 + tid;
+    float d[4][32];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) tmem_ld32(lane_base + q * 32, d[q]);
+    tmem_ld_wait();
+#pragma unroll
+    for (int q = 0; q < 4; ++q) tmem_ld_fence(d[q]);
+    if (t < f.T) {
+      Tout* orow = static_cast<Tout*>(f.o) + ((size_t)t * f.Nv + h) * DV;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 8) {
+          float x[8];
+          load8(orow + q * 32 + e, x);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) x[u] += d[q][e + u];
+          store8(orow + q * 32 + e, x);
+        }
+      }
+    }
+    tc_fence_before();
+    __syncthreads();          // D is read out before the next product overwrites it
+    tc_fence_after();
+  }
+  if (!ok && tid == 0) {
+    raise_error(f.err, kDevErrTimeout);
+    for (int k = landed; k < issued; ++k) mbar_wait(&rbar[k & 1], (k >> 1) & 1, WAIT_LIMIT);
+    if (mma_issued > 0) mbar_wait(mbar, (mma_issued - 1) & 1, WAIT_LIMIT);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tbase, 128);
 }
 
 // ---- host: tensor maps and launch
@@ -1230,9 +1598,38 @@ bool chunk_tc_supported(const ChunkArgs& p) {
 
 // Workspace: the tiles of every (chunk slot, value head), then one ready flag
 // per tile and the solve groups' item counter (used by the fused launch).
-size_t chunk_tc_workspace_bytes(int num_seqs, int total, int Nv) {
+// Then, for one sequence long enough to be split in two segments (kSplitMinChunks
+// chunks or more), the split's scratch: S_mid, Bst, Phi and the response rows R.
+namespace {
+constexpr int kSplitMinChunks = 32;
+
+struct SplitLayout {
+  int n, m;               // chunks, first chunk of the second segment
+  size_t off, bytes;      // byte offset of the scratch in the workspace, and its size
+};
+
+size_t tiles_and_flags_bytes(int num_seqs, int total, int Nv) {
   const size_t tiles = ((size_t)(total / CT) + (size_t)num_seqs) * (size_t)Nv;
   return tiles * TILE_T_BYTES + ((tiles + 1) * sizeof(int) + 255) / 256 * 256;
+}
+
+bool split_layout(int num_seqs, int total, int Nv, SplitLayout* L) {
+  const int n = (total + CT - 1) / CT;
+  if (num_seqs != 1 || n < kSplitMinChunks) return false;
+  L->n = n;
+  L->m = (n + 1) / 2;
+  L->off = tiles_and_flags_bytes(num_seqs, total, Nv);
+  const size_t st = (size_t)Nv * DK * DV * sizeof(float);
+  L->bytes = 3 * st + ((size_t)(total - L->m * CT) * Nv * DV * sizeof(bf16) + 255) / 256 * 256;
+  return true;
+}
+}  // namespace
+
+size_t chunk_tc_workspace_bytes(int num_seqs, int total, int Nv) {
+  SplitLayout L;
+  size_t bytes = tiles_and_flags_bytes(num_seqs, total, Nv);
+  if (split_layout(num_seqs, total, Nv, &L)) bytes += L.bytes;
+  return bytes;
 }
 
 namespace {
@@ -1268,6 +1665,11 @@ bool fused_device(int* sms) {
       ok = ok && cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)K3_SMEM) == cudaSuccess &&
            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, NT3, K3_SMEM) == cudaSuccess && nb >= 1;
     }
+    ok = ok &&
+         cudaFuncSetAttribute(reinterpret_cast<const void*>(chunk_fixup_kernel<bf16>),
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)K4_SMEM) == cudaSuccess &&
+         cudaFuncSetAttribute(reinterpret_cast<const void*>(chunk_fixup_kernel<float>),
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)K4_SMEM) == cudaSuccess;
     if (ok) {
       f.ok = true;
       f.sms = n;
@@ -1301,22 +1703,63 @@ cudaError_t launch_chunk_tc(const ChunkArgs& args, cudaStream_t s) {
   int sms = 0;
   if (p.num_seqs == 1 && fused_device(&sms) && sms > p.Nv) {
     // one sequence: solve and scan overlap in one cooperative launch
-    int nscan = p.Nv, nitems = slots * p.Nv;
-    int* flags = reinterpret_cast<int*>(static_cast<uint8_t*>(p.workspace) + (size_t)nitems * TILE_T_BYTES);
+    uint8_t* ws = static_cast<uint8_t*>(p.workspace);
+    const int n = (p.total + CT - 1) / CT;
+    int nitems = n * p.Nv;
+    int* flags = reinterpret_cast<int*>(ws + (size_t)slots * p.Nv * TILE_T_BYTES);
     cudaError_t e = cudaMemsetAsync(flags, 0, (size_t)(nitems + 1) * sizeof(int), s);
     if (e != cudaSuccess) return e;
     CUtensorMap mo = mk;                               // fp32 rows are stored directly
     if (p.out_bf16 && !make_map(&mo, p.o, p.total, p.Nv * DV)) return cudaErrorInvalidValue;
+    // A long sequence is split in two segments when the SMs hold three scans per head and
+    // at least two solve CTAs per head beside them (the two segments' scans take twice the
+    // solve's output per period; with fewer solve SMs the split runs slower than one chain:
+    // 264 vs 124 us at 32 heads, T = 4096, on 152 SMs), and the output is the plain o (the
+    // gated norm of the fused epilogue cannot be corrected afterwards).
+    SplitLayout L;
+    SplitArgs sp{1, n, n, nullptr, nullptr, nullptr, nullptr};
+    CUtensorMap mr = mk;
+    if (split_layout(1, p.total, p.Nv, &L) && p.z == nullptr && sms >= 5 * p.Nv) {
+      const size_t st = (size_t)p.Nv * DK * DV;
+      float* scr = reinterpret_cast<float*>(ws + L.off);
+      sp = SplitArgs{2, L.m, n, scr, scr + st, scr + 2 * st, reinterpret_cast<bf16*>(scr + 3 * st)};
+      if (!make_map(&mr, sp.R, p.total - L.m * CT, p.Nv * DV)) return cudaErrorInvalidValue;
+    }
+    int nscan = sp.nseg == 2 ? 3 * p.Nv : p.Nv;
     ChunkArgs pc = p;
     // Solve groups per CTA: the scans take Nv items per period (about 1.5 us), and one, two
     // or three groups per SM deliver an item per about 6, 8 or 10.6 us each; take the fewest
-    // that keep the solve about 1.3x ahead.
-    const double per_scan = (double)(sms - nscan) / (double)nscan;
+    // that keep the solve about 1.3x ahead (a split sequence's scans take two chunks' items
+    // per period: three groups).
+    const double per_scan = (double)(sms - nscan) / (double)(sp.nseg * p.Nv);
     int ngroups = per_scan >= 5.3 ? 1 : (per_scan >= 3.55 ? 2 : 3);
     if (p.no_solve) ngroups = 0;           // test hook: no flag is ever published
-    void* args[] = {&mq, &mk, &mv, &mo, &mz, &pc, &nscan, &nitems, &flags, &ngroups};
+    void* args[] = {&mq, &mk, &mv, &mo, &mz, &mr, &pc, &sp, &nscan, &nitems, &flags, &ngroups};
     const void* fn = fused_kernels()[(p.out_bf16 ? 0 : 2) + (p.z != nullptr ? 1 : 0)];
-    return cudaLaunchCooperativeKernel(fn, dim3(sms), dim3(NT3), args, K3_SMEM, s);
+    e = cudaLaunchCooperativeKernel(fn, dim3(sms), dim3(NT3), args, K3_SMEM, s);
+    if (e != cudaSuccess || sp.nseg == 1) return e;
+    // the second segment's outputs and the final state from S_mid
+    FixArgs f{};
+    f.S_mid = sp.S_mid;
+    f.Bst = sp.Bst;
+    f.Phi = sp.Phi;
+    f.ST = p.ST;
+    f.o = p.o;
+    f.t1 = sp.m * CT;
+    f.T = p.total;
+    f.Nv = p.Nv;
+    f.nblk = (p.total - f.t1 + 127) / 128;
+    const int target = 2 * sms;                        // output CTAs: about two per SM
+    const int cph = std::max(1, std::min(f.nblk, target / p.Nv));
+    f.bpc = (f.nblk + cph - 1) / cph;
+    f.cph = (f.nblk + f.bpc - 1) / f.bpc;
+    f.err = p.err;
+    const int grid = f.cph * p.Nv + (p.ST ? 8 * p.Nv : 0);
+    if (p.out_bf16)
+      chunk_fixup_kernel<bf16><<<grid, NT4, K4_SMEM, s>>>(mr, f);
+    else
+      chunk_fixup_kernel<float><<<grid, NT4, K4_SMEM, s>>>(mr, f);
+    return cudaGetLastError();
   }
   if (p.no_solve) return cudaErrorNotSupported;     // the test hook needs the one-sequence launch
   cudaError_t e = cudaFuncSetAttribute(chunk_solve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
