@@ -140,13 +140,96 @@ constexpr uint32_t S1_BAR = S1_VEC + 6 * 64 * 4;
 constexpr uint32_t S1_SMEM = S1_BAR + 64 + 1024;
 static_assert(S1_TR % 1024 == 0 && S1_AT % 1024 == 0, "tile alignment");
 
+// One warp's m16n8k8 product on the tensor core through mma.sync, tf32 operands
+// (10-bit mantissa, rounded to nearest) and fp32 accumulation: d += a b.
+// Fragments (g = lane / 4, t = lane % 4):  a = A[g][t], A[g+8][t], A[g][t+4], A[g+8][t+4];
+// b = B[t][g], B[t+4][g];  d = D[g][2t], D[g][2t+1], D[g+8][2t], D[g+8][2t+1].
+__device__ __forceinline__ uint32_t tf32_rn(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+               : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// One warp: T[R:R+16M][C+8w : C+8w+8] = -T[R:R+16M][R:R+16M] (A[R:R+16M][C:C+16M] T[C:C+16M][C+8w : ...])
+// for an M x M block (M = 1: 16 x 16, M = 2: 32 x 32) below the diagonal, w the warp's
+// 8-column tile.  The intermediate X (16M x 8) goes through the warp's own scratch XW
+// (16M x 8 floats) from accumulator to operand layout.
+template <int M>
+__device__ __forceinline__ void merge_tile(const float* AT, float* TR, float* XW, int R, int C, int w, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  const int n0 = C + 8 * w;
+  float x[M][4];
+#pragma unroll
+  for (int mt = 0; mt < M; ++mt) x[mt][0] = x[mt][1] = x[mt][2] = x[mt][3] = 0.f;
+#pragma unroll
+  for (int ks = 0; ks < 2 * M; ++ks) {             // X = A21 T11: K = 16 M
+    const int k = C + 8 * ks + t;
+    const uint32_t b0 = tf32_rn(TR[k * FS + n0 + g]), b1 = tf32_rn(TR[(k + 4) * FS + n0 + g]);
+#pragma unroll
+    for (int mt = 0; mt < M; ++mt) {
+      const int r = R + 16 * mt + g;                // A[r][k] = AT[k][r]
+      mma_tf32(x[mt], tf32_rn(AT[k * FS + r]), tf32_rn(AT[k * FS + r + 8]), tf32_rn(AT[(k + 4) * FS + r]),
+               tf32_rn(AT[(k + 4) * FS + r + 8]), b0, b1);
+    }
+  }
+#pragma unroll
+  for (int mt = 0; mt < M; ++mt) {
+    *reinterpret_cast<float2*>(XW + (16 * mt + g) * 8 + 2 * t) = make_float2(x[mt][0], x[mt][1]);
+    *reinterpret_cast<float2*>(XW + (16 * mt + g + 8) * 8 + 2 * t) = make_float2(x[mt][2], x[mt][3]);
+  }
+  __syncwarp();
+  float y[M][4];
+#pragma unroll
+  for (int mt = 0; mt < M; ++mt) y[mt][0] = y[mt][1] = y[mt][2] = y[mt][3] = 0.f;
+#pragma unroll
+  for (int ks = 0; ks < 2 * M; ++ks) {             // T21 = -T22 X: K = 16 M
+    const int k = 8 * ks + t;
+    const uint32_t b0 = tf32_rn(XW[k * 8 + g]), b1 = tf32_rn(XW[(k + 4) * 8 + g]);
+#pragma unroll
+    for (int mt = 0; mt < M; ++mt) {
+      const float* tr = TR + (R + 16 * mt + g) * FS + R + k;
+      mma_tf32(y[mt], tf32_rn(tr[0]), tf32_rn(tr[8 * FS]), tf32_rn(tr[4]), tf32_rn(tr[8 * FS + 4]), b0, b1);
+    }
+  }
+#pragma unroll
+  for (int mt = 0; mt < M; ++mt) {
+    *reinterpret_cast<float2*>(TR + (R + 16 * mt + g) * FS + n0 + 2 * t) = make_float2(-y[mt][0], -y[mt][1]);
+    *reinterpret_cast<float2*>(TR + (R + 16 * mt + g + 8) * FS + n0 + 2 * t) = make_float2(-y[mt][2], -y[mt][3]);
+  }
+}
+
+// Write 64 bf16 values (times sc) as swizzled row `row` of a 64-column block in global memory.
+__device__ __forceinline__ void st_row64_global(uint8_t* dst, uint32_t row, const float* v, float sc) {
+#pragma unroll
+  for (int ch = 0; ch < 8; ++ch) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __nv_bfloat162 h = __floats2bfloat162_rn(sc * v[ch * 8 + 2 * i], sc * v[ch * 8 + 2 * i + 1]);
+      w[i] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    const uint32_t off = row * 128u + ((((uint32_t)ch ^ (row & 7u)) & 7u) << 4);
+    *reinterpret_cast<uint4*>(dst + off) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
 // T = (I + A)^-1 for a 64 x 64 strictly lower A given transposed (AT[k][i] =
 // A[i][k], stride FS), by 128 threads into TR (row-major, stride FS; TR must
 // hold zeros above the diagonal blocks on entry).
-//   1. the four 16 x 16 diagonal blocks, one column per thread (64 threads);
-//   2. T[b+1][b] = -T[b+1][b+1] (A[b+1][b] T[b][b]) for the pairs (0,1), (2,3);
-//   3. T[32:64][0:32] = -T[32:64][32:64] (A[32:64][0:32] T[0:32][0:32]).
-// XS is fp32 scratch of 32 x 36.  The 128 threads synchronise on named barrier barid.
+//   1. the four 16 x 16 diagonal blocks, one column per thread (64 threads), fp32;
+//   2. T[b+1][b] = -T[b+1][b+1] (A[b+1][b] T[b][b]) for the pairs (0,1), (2,3): warp w
+//      takes pair w / 2, columns 8 (w % 2) .. + 8 of the block;
+//   3. T[32:64][0:32] = -T[32:64][32:64] (A[32:64][0:32] T[0:32][0:32]): warp w takes
+//      columns 8w .. 8w + 8.
+// The block products of 2 and 3 run on the tensor core (mma.sync, tf32 operands, fp32
+// accumulation); T is rounded to bf16 when it is used.  XS is fp32 scratch of 4 KB.
+// The 128 threads synchronise on named barrier barid.
 __device__ __forceinline__ void invert_unit_lower(const float* AT, float* TR, float* XS, int tid, uint32_t barid) {
   if (tid < 64) {
     const int b = (tid >> 4) * 16, c = tid & 15;
@@ -176,68 +259,10 @@ __device__ __forceinline__ void invert_unit_lower(const float* AT, float* TR, fl
     }
   }
   named_sync(barid, 128);
-  {   // 16 -> 32: pair pr = tid / 64, block rows R = 16 (2 pr + 1), columns C = 32 pr
-    const int pr = tid >> 6, u = tid & 63;
-    const int r0 = 2 * (u >> 3), c0 = 2 * (u & 7);
-    const int R = 16 * (2 * pr + 1), C = 32 * pr;
-    float* X = XS + pr * 16 * 20;
-    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);   // rows r0, r0 + 1
-#pragma unroll 4
-    for (int k = 0; k < 16; ++k) {
-      const float2 a = *reinterpret_cast<const float2*>(AT + (C + k) * FS + R + r0);
-      const float2 t = *reinterpret_cast<const float2*>(TR + (C + k) * FS + C + c0);
-      acc0 = __ffma2_rn(make_float2(a.x, a.x), t, acc0);
-      acc1 = __ffma2_rn(make_float2(a.y, a.y), t, acc1);
-    }
-    *reinterpret_cast<float2*>(X + r0 * 20 + c0) = acc0;
-    *reinterpret_cast<float2*>(X + (r0 + 1) * 20 + c0) = acc1;
-    named_sync(barid, 128);
-    acc0 = acc1 = make_float2(0.f, 0.f);
-#pragma unroll 4
-    for (int k = 0; k < 16; ++k) {
-      const float t0 = TR[(R + r0) * FS + R + k], t1 = TR[(R + r0 + 1) * FS + R + k];
-      const float2 y = *reinterpret_cast<const float2*>(X + k * 20 + c0);
-      acc0 = __ffma2_rn(make_float2(t0, t0), y, acc0);
-      acc1 = __ffma2_rn(make_float2(t1, t1), y, acc1);
-    }
-    *reinterpret_cast<float2*>(TR + (R + r0) * FS + C + c0) = make_float2(-acc0.x, -acc0.y);
-    *reinterpret_cast<float2*>(TR + (R + r0 + 1) * FS + C + c0) = make_float2(-acc1.x, -acc1.y);
-  }
+  const int w = tid >> 5, lane = tid & 31;
+  merge_tile<1>(AT, TR, XS + w * 256, 16 * (2 * (w >> 1) + 1), 32 * (w >> 1), w & 1, lane);
   named_sync(barid, 128);
-  {   // 32 -> 64: 2 x 4 outputs per thread
-    const int r0 = 2 * (tid >> 3), c0 = 4 * (tid & 7);
-    float2 acc[2][2] = {{make_float2(0.f, 0.f), make_float2(0.f, 0.f)}, {make_float2(0.f, 0.f), make_float2(0.f, 0.f)}};
-#pragma unroll 8
-    for (int k = 0; k < 32; ++k) {
-      const float2 a = *reinterpret_cast<const float2*>(AT + k * FS + 32 + r0);
-      const float4 t = *reinterpret_cast<const float4*>(TR + k * FS + c0);
-      const float2 tl = make_float2(t.x, t.y), th = make_float2(t.z, t.w);
-      acc[0][0] = __ffma2_rn(make_float2(a.x, a.x), tl, acc[0][0]);
-      acc[0][1] = __ffma2_rn(make_float2(a.x, a.x), th, acc[0][1]);
-      acc[1][0] = __ffma2_rn(make_float2(a.y, a.y), tl, acc[1][0]);
-      acc[1][1] = __ffma2_rn(make_float2(a.y, a.y), th, acc[1][1]);
-    }
-#pragma unroll
-    for (int a = 0; a < 2; ++a)
-      *reinterpret_cast<float4*>(XS + (r0 + a) * 36 + c0) = make_float4(acc[a][0].x, acc[a][0].y, acc[a][1].x, acc[a][1].y);
-    named_sync(barid, 128);
-#pragma unroll
-    for (int a = 0; a < 2; ++a) acc[a][0] = acc[a][1] = make_float2(0.f, 0.f);
-#pragma unroll 8
-    for (int k = 0; k < 32; ++k) {
-      const float t0 = TR[(32 + r0) * FS + 32 + k], t1 = TR[(32 + r0 + 1) * FS + 32 + k];
-      const float4 y = *reinterpret_cast<const float4*>(XS + k * 36 + c0);
-      const float2 yl = make_float2(y.x, y.y), yh = make_float2(y.z, y.w);
-      acc[0][0] = __ffma2_rn(make_float2(t0, t0), yl, acc[0][0]);
-      acc[0][1] = __ffma2_rn(make_float2(t0, t0), yh, acc[0][1]);
-      acc[1][0] = __ffma2_rn(make_float2(t1, t1), yl, acc[1][0]);
-      acc[1][1] = __ffma2_rn(make_float2(t1, t1), yh, acc[1][1]);
-    }
-#pragma unroll
-    for (int a = 0; a < 2; ++a)
-      *reinterpret_cast<float4*>(TR + (32 + r0 + a) * FS + c0) =
-          make_float4(-acc[a][0].x, -acc[a][0].y, -acc[a][1].x, -acc[a][1].y);
-  }
+  merge_tile<2>(AT, TR, XS + w * 256, 32, 0, w, lane);
   named_sync(barid, 128);
 }
 
@@ -282,17 +307,27 @@ struct SolveAhead {
   float gb;
 };
 
+__device__ __forceinline__ void st_release(int* f, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
+}
+
+// Claim the next work item: a relaxed atomic add issued where it stands in the program
+// (its result is read only after the current item, so its latency hides under it).
+__device__ __forceinline__ int claim_item(int* counter) {
+  int v;
+  asm volatile("atom.relaxed.gpu.global.add.s32 %0, [%1], 1;" : "=r"(v) : "l"(counter) : "memory");
+  return v;
+}
+
 // One (chunk slot, value head) by 128 threads (tid 0-127 of a group that
 // synchronises on named barrier barid).  sm is the group's 1024-aligned
 // shared memory (S1_BYTES), bar an initialised mbarrier whose next phase
 // parity is ph & 1 (ph advances by three), tbase 128 allocated tensor-memory
-// columns.  The item's tiles are built in shared memory and written to the
-// workspace by bulk copies of whole tiles (P staged in the T buffer, T diag(beta)
-// there too, diag(gamma) Q over the Q tiles and -W over the K tiles, so that the
-// 32 KB [-W | Q~] block leaves in one copy); thread 0 has waited for every copy to
-// complete when this returns.  `ahead` carries the loads of the next item
-// (nslot < 0: none) that this item issues: its gate values during the inverse,
-// and its Q, K tiles once this item's copies have left the QK buffer.
+// columns.  The tiles go to the workspace as direct 16-byte row stores; when this
+// returns every thread has fenced them (visible device-wide).  `ahead` carries the
+// loads this item issues for the next one (nslot < 0: none): its gate values, in
+// flight under this item's A and P rows, and its Q, K tiles, issued by thread 0 as
+// soon as this item's W product has completed (the last reader of the QK buffer).
 // Returns false, with the device error flag raised, on a timeout.
 __device__ bool solve_item(uint8_t* sm, int tid, uint32_t barid, uint64_t* bar, uint32_t& ph, uint32_t tbase,
                            const CUtensorMap* tmq, const CUtensorMap* tmk, const ChunkArgs& p, int slot, int h,
@@ -320,8 +355,12 @@ __device__ bool solve_item(uint8_t* sm, int tid, uint32_t barid, uint64_t* bar, 
   const uint32_t sb = smem_u32(sm);
 
   if (tid == 0 && !ahead.tiles) solve_load_tiles(sm, bar, tmq, tmk, p, c0, h);
-  // threads 0-63 hold g, threads 64-127 beta (loaded during the item before, else now)
+  ahead.tiles = false;
+  // threads 0-63 hold g, threads 64-127 beta (loaded during the item before, else now);
+  // the zeroing of T (which starts at zero above its diagonal blocks) runs meanwhile
   const float gb = ahead.gate ? ahead.gb : solve_gate(p, tid, c0, len, h);
+  for (int i = tid * 4; i < 64 * FS; i += 128 * 4)
+    *reinterpret_cast<float4*>(TR + i) = make_float4(0.f, 0.f, 0.f, 0.f);
   (tid < CT ? Gs : Bet)[tid & 63] = gb;
   named_sync(barid, 128);
   if (warp == 0) {
@@ -382,8 +421,7 @@ __device__ bool solve_item(uint8_t* sm, int tid, uint32_t barid, uint64_t* bar, 
         for (int r = 0; r < 64; r += 4)
           *reinterpret_cast<float4*>(AT + j * FS + r) = make_float4(v[r], v[r + 1], v[r + 2], v[r + 3]);
       } else {
-        // row r of P = M o Q K^T: (q_r . k_j) e^(G_r - G_j) for j <= r, the product taken from j = r
-        // down; staged as a swizzled bf16 row in the T buffer (zeroed again before the inverse)
+        // row r of P = M o Q K^T: (q_r . k_j) e^(G_r - G_j) for j <= r, the product taken from j = r down
         const int r = tid - CT;
         float cur = 1.f;
 #pragma unroll
@@ -401,10 +439,11 @@ __device__ bool solve_item(uint8_t* sm, int tid, uint32_t barid, uint64_t* bar, 
             v[j] = j <= r ? v[j] * cur : 0.f;
           }
         }
-        st_row64(sm, S1_TR, r, v);
+        st_row64_global(ws + WS_P, r, v, 1.f);
       }
     }
-    // diag(gamma) Q in place over the Q tiles (same swizzled rows), then dec and gamma_L
+    // diag(gamma) Q -> rows 64-127 of the two [-W; Q~] blocks (same swizzled rows as
+    // the TMA tiles), then dec and gamma_L
     {
       uint4 qu[8];
       float f[8];
@@ -426,31 +465,20 @@ __device__ bool solve_item(uint8_t* sm, int tid, uint32_t barid, uint64_t* bar, 
           __nv_bfloat162 y = __floats2bfloat162_rn(x.x * f[k], x.y * f[k]);
           w[j] = *reinterpret_cast<uint32_t*>(&y);
         }
-        *reinterpret_cast<uint4*>(sm + S1_QK + 8192 + off) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(ws + WS_QW + 8192 + off) = make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
     if (tid < CT) reinterpret_cast<float*>(ws + WS_VEC)[tid] = Dec[tid];
     if (tid == 0) reinterpret_cast<float*>(ws + WS_VEC)[CT] = Gam[CT - 1];
-    fence_proxy_async_smem();        // P is read by the copy engine next
     tc_fence_before();
-    named_sync(barid, 128);
-    if (tid == 0) {
-      bulk_store(ws + WS_P, sm + S1_TR, 8192);
-      bulk_commit_group();
-      bulk_wait_read<0>();           // the T buffer is free again
-    }
-    named_sync(barid, 128);
-    for (int i = tid * 4; i < 64 * FS; i += 128 * 4)   // T starts at zero above its diagonal blocks
-      *reinterpret_cast<float4*>(TR + i) = make_float4(0.f, 0.f, 0.f, 0.f);
     named_sync(barid, 128);
     invert_unit_lower(AT, TR, XS, tid, barid);
     // A^T is dead: its space becomes the [T diag(beta gamma); T diag(beta gamma)] operand (the
-    // rows twice, so that all four warps take a share of W out of tensor memory); T diag(beta)
-    // is staged over T
+    // rows twice, so that all four warps take a share of W out of tensor memory)
     uint8_t* tbg = sm + S1_AT;
     {
-      // thread (r, ch) = (tid / 8 + 16 k, tid % 8): every read of T, beta and beta gamma,
-      // then a barrier, then the stores
+      // thread (r, ch) = (tid / 8 + 16 k, tid % 8): every read of T, beta and beta gamma
+      // before the first store (the stores go over the dead A^T)
       const int ch = tid & 7;
       float4 t0[4], t1[4];
 #pragma unroll
@@ -465,7 +493,6 @@ __device__ bool solve_item(uint8_t* sm, int tid, uint32_t barid, uint64_t* bar, 
       const float4 bg1 = *reinterpret_cast<const float4*>(BG + ch * 8 + 4);
       const float be[8] = {be0.x, be0.y, be0.z, be0.w, be1.x, be1.y, be1.z, be1.w};
       const float bgv[8] = {bg0.x, bg0.y, bg0.z, bg0.w, bg1.x, bg1.y, bg1.z, bg1.w};
-      named_sync(barid, 128);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int r = (tid >> 3) + 16 * k;
@@ -479,7 +506,7 @@ __device__ bool solve_item(uint8_t* sm, int tid, uint32_t barid, uint64_t* bar, 
           wb[i] = *reinterpret_cast<uint32_t*>(&hb);
         }
         const uint32_t sw = r * 128u + ((((uint32_t)ch ^ (uint32_t)(r & 7)) & 7u) << 4);
-        *reinterpret_cast<uint4*>(sm + S1_TR + sw) = make_uint4(wa[0], wa[1], wa[2], wa[3]);
+        *reinterpret_cast<uint4*>(ws + WS_TB + sw) = make_uint4(wa[0], wa[1], wa[2], wa[3]);
         *reinterpret_cast<uint4*>(tbg + sw) = make_uint4(wb[0], wb[1], wb[2], wb[3]);
         *reinterpret_cast<uint4*>(tbg + 8192 + sw) = make_uint4(wb[0], wb[1], wb[2], wb[3]);
       }
@@ -489,8 +516,6 @@ __device__ bool solve_item(uint8_t* sm, int tid, uint32_t barid, uint64_t* bar, 
     named_sync(barid, 128);
     tc_fence_after();
     if (tid == 0) {
-      bulk_store(ws + WS_TB, sm + S1_TR, 8192);
-      bulk_commit_group();
       // W = T diag(beta gamma) K, in rows 0-63 and again in rows 64-127 of the 128 x 128 result
       const uint32_t id = idesc_bf16(128, 128, false, true);
       const uint64_t a = sdesc_sw128(sb + S1_AT, 16, 1024);
@@ -502,57 +527,39 @@ __device__ bool solve_item(uint8_t* sm, int tid, uint32_t barid, uint64_t* bar, 
     ok = mbar_wait(bar, ph & 1u, WAIT_LIMIT);
     if (!named_sync_or(barid, 128, !ok)) {
       tc_fence_after();
-      {   // -W over the K tiles: warps 0-1 columns 0-63 of rows 0-63, warps 2-3 columns 64-127 of the copy
+      // the W product was the QK buffer's last reader: the next item's tiles may land there
+      if (tid == 0 && nused) solve_load_tiles(sm, bar, tmq, tmk, p, nc0, nh);
+      ahead.tiles = nused;
+      {   // warps 0-1: columns 0-63 of rows 0-63; warps 2-3: columns 64-127 of the copy
         const int half = tid >> 6;
         float v[64];
         tm_ld64(lane_base + half * 64, v);
-#pragma unroll
-        for (int i = 0; i < 64; ++i) v[i] = -v[i];
-        st_row64(sm, S1_QK + half * 16384, tid & 63, v);
-      }
-      fence_proxy_async_smem();
-      named_sync(barid, 128);
-      if (tid == 0) {
-        bulk_store(ws + WS_QW, sm + S1_QK, 32768);   // [-W | Q~ | -W | Q~]
-        bulk_commit_group();
+        st_row64_global(ws + WS_QW + half * 16384, tid & 63, v, -1.f);
       }
       done = true;
     }
   }
   ph += 1;
   if (!done && tid == 0) raise_error(p.err, kDevErrTimeout);
-  if (tid == 0) {
-    bulk_wait_all();                 // every copy of this item complete (its writes performed)
-    fence_proxy_async_global();
-  }
-  __threadfence();                   // this thread's direct stores (dec, gamma_L) likewise
+  __threadfence();                   // this thread's tile stores are visible device-wide
   // the next item may reuse this shared and tensor memory
   tc_fence_before();
   named_sync(barid, 128);
   tc_fence_after();
-  ahead.tiles = false;
   return done;
 }
 
-// After the item's flag is published: thread 0 issues the next item's tile loads into
-// the (now free) QK buffer.
-__device__ __forceinline__ void solve_prefetch_tiles(uint8_t* sm, int tid, uint64_t* bar, const CUtensorMap* tmq,
-                                                     const CUtensorMap* tmk, const ChunkArgs& p, SolveAhead& ahead,
-                                                     int nslot, int nh) {
-  int nc0 = 0, nlen = 0;
-  if (nslot >= 0 && slot_chunk(p, nslot, nc0, nlen)) {
-    if (tid == 0) solve_load_tiles(sm, bar, tmq, tmk, p, nc0, nh);
-    ahead.tiles = true;
-  }
-}
-
+// Packed batches: persistent CTAs (three per SM) claim (chunk slot, value head) items
+// in slot order from an atomic counter, one ahead, so that the next item's gate
+// values and tiles load under the current one.
 __global__ void __launch_bounds__(128, 3)
 chunk_solve_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                   ChunkArgs p) {
+                   ChunkArgs p, int nitems, int* counter) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + S1_BAR);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S1_BAR + 16);
+  volatile int* item_slot = reinterpret_cast<volatile int*>(sm + S1_BAR + 32);   // two slots
   const int tid = threadIdx.x;
   if (tid == 0) {
     mbar_init(bar, 1);
@@ -563,8 +570,27 @@ chunk_solve_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
   __syncthreads();
   tc_fence_after();
   uint32_t ph = 0;
+  // items claimed two ahead (see the one-sequence launch)
+  if (tid == 0) {
+    item_slot[0] = atomicAdd(counter, 1);
+    item_slot[1] = atomicAdd(counter, 1);
+  }
+  __syncthreads();
+  int item = item_slot[0], next = item_slot[1];
   SolveAhead ahead{false, false, 0.f};
-  solve_item(sm, tid, 1, bar, ph, *tslot, &tmq, &tmk, p, blockIdx.x, blockIdx.y, ahead, -1, 0);
+  int par = 0;
+  while (item < nitems) {
+    const int after = tid == 0 && next < nitems ? claim_item(counter) : nitems;
+    const int nslot = next < nitems ? next / p.Nv : -1, nh = next < nitems ? next % p.Nv : 0;
+    if (!solve_item(sm, tid, 1, bar, ph, *tslot, &tmq, &tmk, p, item / p.Nv, item % p.Nv, ahead, nslot, nh)) break;
+    if (tid == 0) item_slot[par] = after;
+    __syncthreads();
+    item = next;
+    next = item_slot[par];
+    par ^= 1;
+  }
+  tc_fence_before();
+  __syncthreads();
   if ((tid >> 5) == 0) tmem_dealloc(*tslot, 128);
 }
 
@@ -1270,10 +1296,6 @@ constexpr uint32_t S1_GROUP = (S1_BAR + 64 + 1023) & ~1023u;     // one solve gr
 constexpr uint32_t K3_SMEM = (3 * S1_GROUP + 1024) > K2_SMEM ? (3 * S1_GROUP + 1024) : K2_SMEM;
 static_assert(K3_SMEM <= 232448, "shared memory budget");
 
-__device__ __forceinline__ void st_release(int* f, int v) {
-  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
-}
-
 // A sequence split in two segments (nseg = 2): chunks [0, m) and [m, n).  Scratch in
 // the workspace: the first segment's final state S_mid, the second's final state from
 // zero Bst and its transition map Phi ([Nv][Dk][Dv] fp32 each), and the map scan's
@@ -1361,28 +1383,31 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
   int* counter = flags + nitems;
   uint32_t ph = 0;
   if (g < ngroups) {
-    // items are claimed one ahead (alternating broadcast slots), so that the next item's
-    // gate values and tiles load under the current one
-    int par = 0;
-    auto claim = [&]() {
-      if (tid == 0) item_slot[par] = atomicAdd(counter, 1);
-      named_sync(barid, 128);
-      const int v = item_slot[par];
-      par ^= 1;
-      return v;
-    };
+    // Items are claimed two ahead: the next item's gate values and tiles load under the
+    // current one, and the claim of the one after (a global atomic) is in flight meanwhile.
+    if (tid == 0) {
+      item_slot[0] = atomicAdd(counter, 1);
+      item_slot[1] = atomicAdd(counter, 1);
+    }
+    named_sync(barid, 128);
+    int item = item_slot[0], next = item_slot[1];
     SolveAhead ahead{false, false, 0.f};
-    int item = claim();
+    int par = 0;
     while (item < nitems) {
-      const int next = claim();
+      const int after = tid == 0 && next < nitems ? claim_item(counter) : nitems;   // read after the item
       int c, h, nc = -1, nh = 0;
       item_chunk(sp, p.Nv, item, c, h);
       if (next < nitems) item_chunk(sp, p.Nv, next, nc, nh);
       const bool ok = solve_item(gsm, tid, barid, bar, ph, tbase, &tmq, &tmk, p, c, h, ahead, nc, nh);
-      if (tid == 0) st_release(flags + (size_t)c * p.Nv + h, ok ? 1 : -1);   // tiles complete (see solve_item)
+      if (tid == 0) {
+        st_release(flags + (size_t)c * p.Nv + h, ok ? 1 : -1);   // tiles visible (see solve_item)
+        item_slot[par] = after;
+      }
       if (!ok) break;
-      if (next < nitems) solve_prefetch_tiles(gsm, tid, bar, &tmq, &tmk, p, ahead, nc, nh);
+      named_sync(barid, 128);
       item = next;
+      next = item_slot[par];
+      par ^= 1;
     }
   }
   tc_fence_before();
@@ -1727,12 +1752,12 @@ cudaError_t launch_chunk_tc(const ChunkArgs& args, cudaStream_t s) {
     }
     int nscan = sp.nseg == 2 ? 3 * p.Nv : p.Nv;
     ChunkArgs pc = p;
-    // Solve groups per CTA: the scans take Nv items per period (about 1.5 us), and one, two
-    // or three groups per SM deliver an item per about 6, 8 or 10.6 us each; take the fewest
-    // that keep the solve about 1.3x ahead (a split sequence's scans take two chunks' items
-    // per period: three groups).
+    // Solve groups per CTA: the scans take Nv items per period (about 1.5 us); one group
+    // per SM delivers an item per about 6 us, three groups one per about 12 us each.  Take
+    // one group where the solve SMs outnumber the scans' demand that much, else three (clock
+    // stamps at 32 heads on 152 SMs: with two groups the scans waited on the solve).
     const double per_scan = (double)(sms - nscan) / (double)(sp.nseg * p.Nv);
-    int ngroups = per_scan >= 5.3 ? 1 : (per_scan >= 3.55 ? 2 : 3);
+    int ngroups = per_scan >= 5.3 ? 1 : 3;
     if (p.no_solve) ngroups = 0;           // test hook: no flag is ever published
     void* args[] = {&mq, &mk, &mv, &mo, &mz, &mr, &pc, &sp, &nscan, &nitems, &flags, &ngroups};
     const void* fn = fused_kernels()[(p.out_bf16 ? 0 : 2) + (p.z != nullptr ? 1 : 0)];
@@ -1765,8 +1790,13 @@ cudaError_t launch_chunk_tc(const ChunkArgs& args, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(chunk_solve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)S1_SMEM);
   if (e != cudaSuccess) return e;
-  dim3 g1(slots, p.Nv);
-  chunk_solve_kernel<<<g1, 128, S1_SMEM, s>>>(mq, mk, p);
+  // the item counter sits in the workspace's flag area
+  const int nitems = slots * p.Nv;
+  int* counter = reinterpret_cast<int*>(static_cast<uint8_t*>(p.workspace) + (size_t)nitems * TILE_T_BYTES);
+  e = cudaMemsetAsync(counter, 0, sizeof(int), s);
+  if (e != cudaSuccess) return e;
+  const int nsm = num_sms();
+  chunk_solve_kernel<<<std::min(nitems, 3 * nsm), 128, S1_SMEM, s>>>(mq, mk, p, nitems, counter);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (!p.out_bf16) return launch_scan<float>(mk, mv, mk, mz, p, s);   // fp32 rows are stored directly
