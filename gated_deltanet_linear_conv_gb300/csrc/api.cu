@@ -163,6 +163,34 @@ int gdn_conv_gating(const gdn_dims* dims, const int32_t* cu_seqlens, const void*
   return GDN_OK;
 }
 
+int gdn_conv_state_steps(const gdn_dims* dims, const int32_t* cu_seqlens, const void* mixed_qkv, int in_dtype,
+                         const void* conv_state_in, void* step_states, void* stream) {
+  const char* fn = "gdn_conv_state_steps";
+  int st = check_dims(fn, dims, cu_seqlens);
+  if (st != GDN_OK) return st;
+  if (!valid_dtype(in_dtype)) return fail(GDN_ERR_INVALID_ARG, "%s: bad dtype", fn);
+  OPTIONAL_PTR(conv_state_in);
+  if (dims->total_tokens > 0) {
+    REQUIRE_PTR(mixed_qkv);
+    REQUIRE_PTR(step_states);
+  }
+  int* flag = nullptr;
+  st = get_flag(&flag);
+  if (st != GDN_OK) return st;
+  gdn::ConvGatingArgs p{};
+  p.x = mixed_qkv;
+  p.state_in = conv_state_in;
+  p.cu = cu_seqlens;
+  p.num_seqs = dims->num_seqs;
+  p.total = dims->total_tokens;
+  p.C = 2 * dims->num_k_heads * dims->head_k_dim + dims->num_v_heads * dims->head_v_dim;
+  p.in_bf16 = in_dtype == GDN_BF16;
+  p.err = flag;
+  cudaError_t e = gdn::launch_conv_state_steps(p, step_states, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  return GDN_OK;
+}
+
 int gdn_gating(int64_t rows, int32_t num_v_heads, const void* a, const void* b, int in_dtype,
                const float* A_log, const float* dt_bias, float* g, float* beta, void* stream) {
   const char* fn = "gdn_gating";
@@ -313,7 +341,7 @@ int gdn_chunk_prefill_static(const gdn_dims* dims, const int32_t* cu_seqlens, co
   if (st != GDN_OK) return st;
   if (!gdn::chunk_tc_supported(p))
     return fail(GDN_ERR_UNSUPPORTED, "%s: needs bf16 q/k/v and 128-wide heads", fn);
-  const size_t need = gdn::chunk_tc_workspace_bytes(dims->num_seqs, dims->total_tokens, dims->num_v_heads);
+  const size_t need = gdn::chunk_tc_workspace_bytes(dims->num_seqs, dims->total_tokens, dims->num_v_heads, false);
   if (need > gdn::kStaticScratchBytes)
     return fail(GDN_ERR_INVALID_ARG,
                 "%s: this problem needs %zu bytes of scratch, more than the library's fixed %zu bytes; "
@@ -324,6 +352,7 @@ int gdn_chunk_prefill_static(const gdn_dims* dims, const int32_t* cu_seqlens, co
   p.scale = scale;
   p.workspace = scratch;
   p.workspace_bytes = gdn::kStaticScratchBytes;
+  p.no_split = 1;                 // the layout checked above
   e = gdn::launch_chunk_tc(p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, fn);
   return GDN_OK;

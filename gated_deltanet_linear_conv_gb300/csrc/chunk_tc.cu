@@ -266,6 +266,36 @@ __device__ __forceinline__ void invert_unit_lower(const float* AT, float* TR, fl
   named_sync(barid, 128);
 }
 
+// The scan's waits are bounded in time: each gives up after limit_ns of device
+// time (%globaltimer) since it started, or at once when another role of the CTA
+// aborted.  A poll cap far above any limit in use ends the loop even if the timer
+// were not to advance.
+struct WaitCtl {
+  volatile int* abort;
+  uint64_t limit_ns;
+};
+constexpr uint32_t POLL_CAP = 1u << 28;
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait (thread 0 of a solve group) until a chunk's flag reached `need`: its
+// tiles were published and every scan that reads them released them.
+__device__ __forceinline__ bool wait_count(const int* f, int need, uint64_t limit_ns) {
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 0; i < POLL_CAP; ++i) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+    if (v >= need) return true;
+    if (v < 0 || global_ns() - t0 > limit_ns) break;
+    __nanosleep(64);
+  }
+  return false;
+}
+
 // Token range of chunk slot `slot`: false when the slot holds no chunk (past the end
 // of its sequence, or a sequence whose bounds are inconsistent: the scan reports that).
 __device__ __forceinline__ bool slot_chunk(const ChunkArgs& p, int slot, int& c0, int& len) {
@@ -323,15 +353,16 @@ __device__ __forceinline__ int claim_item(int* counter) {
 // synchronises on named barrier barid).  sm is the group's 1024-aligned
 // shared memory (S1_BYTES), bar an initialised mbarrier whose next phase
 // parity is ph & 1 (ph advances by three), tbase 128 allocated tensor-memory
-// columns.  The tiles go to the workspace as direct 16-byte row stores; when this
-// returns every thread has fenced them (visible device-wide).  `ahead` carries the
+// columns.  The tiles go to workspace tile `tile` (of the item's head) as direct
+// 16-byte row stores, once `rel` (if given) reached rel_need; when this returns every
+// thread has fenced them (visible device-wide).  `ahead` carries the
 // loads this item issues for the next one (nslot < 0: none): its gate values, in
 // flight under this item's A and P rows, and its Q, K tiles, issued by thread 0 as
 // soon as this item's W product has completed (the last reader of the QK buffer).
 // Returns false, with the device error flag raised, on a timeout.
 __device__ bool solve_item(uint8_t* sm, int tid, uint32_t barid, uint64_t* bar, uint32_t& ph, uint32_t tbase,
                            const CUtensorMap* tmq, const CUtensorMap* tmk, const ChunkArgs& p, int slot, int h,
-                           SolveAhead& ahead, int nslot, int nh) {
+                           SolveAhead& ahead, int nslot, int nh, size_t tile, const int* rel, int rel_need) {
   float* AT = reinterpret_cast<float*>(sm + S1_AT);
   float* TR = reinterpret_cast<float*>(sm + S1_TR);
   float* XS = reinterpret_cast<float*>(sm + S1_XS);
@@ -350,7 +381,7 @@ __device__ bool solve_item(uint8_t* sm, int tid, uint32_t barid, uint64_t* bar, 
     ahead.gate = false;
     return true;
   }
-  uint8_t* ws = static_cast<uint8_t*>(p.workspace) + ((size_t)slot * p.Nv + h) * TILE_T_BYTES;
+  uint8_t* ws = static_cast<uint8_t*>(p.workspace) + (tile * p.Nv + h) * TILE_T_BYTES;
   const uint32_t lane_base = tbase + ((uint32_t)(warp * 32) << 16);
   const uint32_t sb = smem_u32(sm);
 
@@ -388,6 +419,8 @@ __device__ bool solve_item(uint8_t* sm, int tid, uint32_t barid, uint64_t* bar, 
   // the next item's gate value, in flight under this item's work
   ahead.gate = nused;
   if (nused) ahead.gb = solve_gate(p, tid, nc0, nlen, nh);
+  // a ring position is written only once the chunk that used it before is released
+  if (tid == 0 && rel != nullptr && ok && !wait_count(rel, rel_need, p.wait_ns)) ok = false;
   bool done = false;
   if (!named_sync_or(barid, 128, !ok)) {
     tc_fence_after();
@@ -582,7 +615,9 @@ chunk_solve_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
   while (item < nitems) {
     const int after = tid == 0 && next < nitems ? claim_item(counter) : nitems;
     const int nslot = next < nitems ? next / p.Nv : -1, nh = next < nitems ? next % p.Nv : 0;
-    if (!solve_item(sm, tid, 1, bar, ph, *tslot, &tmq, &tmk, p, item / p.Nv, item % p.Nv, ahead, nslot, nh)) break;
+    if (!solve_item(sm, tid, 1, bar, ph, *tslot, &tmq, &tmk, p, item / p.Nv, item % p.Nv, ahead, nslot, nh,
+                    (size_t)(item / p.Nv), nullptr, 0))
+      break;
     if (tid == 0) item_slot[par] = after;
     __syncthreads();
     item = next;
@@ -643,22 +678,6 @@ struct ScanBars {
   int abort;
 };
 static_assert(sizeof(ScanBars) <= 256, "scan barriers fit their slot");
-
-// The scan's waits are bounded in time: each gives up after limit_ns of device
-// time (%globaltimer) since it started, or at once when another role of the CTA
-// aborted.  A poll cap far above any limit in use ends the loop even if the timer
-// were not to advance.
-struct WaitCtl {
-  volatile int* abort;
-  uint64_t limit_ns;
-};
-constexpr uint32_t POLL_CAP = 1u << 28;
-
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
 
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const WaitCtl& w) {
   if (mbar_test_wait(bar, parity)) return true;      // already complete: no suspension
@@ -748,6 +767,9 @@ struct ScanSeg {
   bool out_bf16;             // the rows are bf16 whatever Tout is
   const CUtensorMap* tmo;    // bf16 map over `out` (used for bf16 rows of whole chunks)
   int row_off;               // token t is output row t - row_off
+  int tile0, ring;           // workspace tiles: chunk c of the segment at position tile0 + c % ring
+                             // (ring 0: one tile per chunk slot, at the sequence's slot + c)
+  bool release;              // add one to a chunk's flag once its tiles are no longer needed
 };
 
 // The scan of one (sequence s, value head h) by the CTA's warps 0-8 (more
@@ -779,7 +801,11 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
   }
   const int n = (eos - bos + CT - 1) / CT;
   const uint8_t* wsb = static_cast<const uint8_t*>(p.workspace);
-  auto ws_tile = [&](int c) { return wsb + ((size_t)(slot0 + c) * p.Nv + h) * TILE_T_BYTES; };
+  int* flags_rw = const_cast<int*>(flags);
+  auto ws_tile = [&](int c) {
+    const size_t t = sg.ring ? (size_t)(sg.tile0 + c % sg.ring) : (size_t)(slot0 + c);
+    return wsb + (t * p.Nv + h) * TILE_T_BYTES;
+  };
 
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
@@ -863,6 +889,14 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
         if (!ok) break;
         if (c >= 2) ok = wait_bar(&B->ob[c & 1], ((c - 2) >> 1) & 1, wc);           // stage free
         if (!ok) break;
+        if (sg.release && c >= 2) {
+          // chunk c - 2's tiles have been consumed (its stage and v buffers are free again: the
+          // copies that read them completed before their products ran), so the solve of a later
+          // chunk may overwrite them; a relaxed add keeps the loader from waiting on the fence
+          // a release would need
+          int* rel = flags_rw + (size_t)(slot0 + c - 2) * p.Nv + h;
+          asm volatile("red.relaxed.gpu.global.add.s32 [%0], 1;" ::"l"(rel) : "memory");
+        }
         issue_stage(c);
         st_issued = c + 1;
       }
@@ -1265,6 +1299,9 @@ __device__ __forceinline__ ScanSeg whole_seq(const ChunkArgs& p, int h, int s, c
   sg.out_bf16 = false;
   sg.tmo = tmo;
   sg.row_off = 0;
+  sg.tile0 = 0;
+  sg.ring = 0;
+  sg.release = false;
   return sg;
 }
 
@@ -1302,6 +1339,7 @@ static_assert(K3_SMEM <= 232448, "shared memory budget");
 // response rows R (bf16 [tokens - 64 m, Nv, Dk]).
 struct SplitArgs {
   int nseg, m, n;
+  int ring;               // tile positions per segment and head
   float* S_mid;
   float* Bst;
   float* Phi;
@@ -1335,12 +1373,45 @@ __global__ void __launch_bounds__(NT3, 1)
 chunk_fused_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo,
                    const __grid_constant__ CUtensorMap tmz, const __grid_constant__ CUtensorMap tmr, ChunkArgs p,
-                   SplitArgs sp, int nscan, int nitems, int* flags, int ngroups) {
+                   SplitArgs sp, int nscan, int nitems, int skip, int* flags, int ngroups) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   if ((int)blockIdx.x < nscan) {
     const int role = blockIdx.x / p.Nv, h = blockIdx.x % p.Nv;
+    if (skip > 0 && role < 2) {
+      // The first chunk of this CTA's segment is solved here, by warps 0-3 in the shared
+      // and tensor memory the scan has not taken yet: alone on its SM the item is ready
+      // well before a solve group sharing an SM with others would deliver it.  The solve
+      // groups start after the segments' first chunks.
+      const int c = role == 0 ? 0 : sp.m;
+      uint64_t* bar = reinterpret_cast<uint64_t*>(sm + S1_BAR);
+      uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S1_BAR + 16);
+      const int tid = threadIdx.x;
+      if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_barrier_init();
+      }
+      if (tid < 32) tmem_alloc_keep(tslot, 128);   // the scan allocates (and relinquishes) next
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
+      if (tid < 128) {
+        SolveAhead ahead{false, false, 0.f};
+        uint32_t ph = 0;
+        const bool ok = solve_item(sm, tid, 1, bar, ph, *tslot, &tmq, &tmk, p, c, h, ahead, -1, 0,
+                                   (size_t)(role * sp.ring), nullptr, 0);
+        if (tid == 0) st_release(flags + (size_t)c * p.Nv + h, ok ? 1 : -1);
+      }
+      tc_fence_before();
+      __syncthreads();
+      if (tid < 32) tmem_dealloc(*tslot, 128);
+      if (tid == 0) mbar_inval(bar);
+      __syncthreads();
+    }
     ScanSeg sg = whole_seq(p, h, 0, &tmo);
+    sg.ring = sp.ring;
+    sg.tile0 = role == 0 ? 0 : sp.ring;            // the second segment's ring follows the first's
+    sg.release = true;
     if (sp.nseg == 2) {
       const size_t hs = (size_t)h * DK * DV;
       if (role == 0) {                       // first segment: the caller's initial state
@@ -1381,6 +1452,7 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
   tc_fence_after();
   const uint32_t tbase = *tslot + 128u * (uint32_t)g;
   int* counter = flags + nitems;
+  nitems -= skip;                        // items claimed here: those after the self-solved chunks
   uint32_t ph = 0;
   if (g < ngroups) {
     // Items are claimed two ahead: the next item's gate values and tiles load under the
@@ -1396,9 +1468,13 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
     while (item < nitems) {
       const int after = tid == 0 && next < nitems ? claim_item(counter) : nitems;   // read after the item
       int c, h, nc = -1, nh = 0;
-      item_chunk(sp, p.Nv, item, c, h);
-      if (next < nitems) item_chunk(sp, p.Nv, next, nc, nh);
-      const bool ok = solve_item(gsm, tid, barid, bar, ph, tbase, &tmq, &tmk, p, c, h, ahead, nc, nh);
+      item_chunk(sp, p.Nv, item + skip, c, h);
+      if (next < nitems) item_chunk(sp, p.Nv, next + skip, nc, nh);
+      // the chunk's ring position, and the chunk that used it before (same segment)
+      const int seg = sp.nseg == 2 && c >= sp.m ? 1 : 0, cl = c - seg * sp.m;
+      const int* rel = cl >= sp.ring ? flags + (size_t)(c - sp.ring) * p.Nv + h : nullptr;
+      const bool ok = solve_item(gsm, tid, barid, bar, ph, tbase, &tmq, &tmk, p, c, h, ahead, nc, nh,
+                                 (size_t)(seg * sp.ring + cl % sp.ring), rel, seg ? 3 : 2);
       if (tid == 0) {
         st_release(flags + (size_t)c * p.Nv + h, ok ? 1 : -1);   // tiles visible (see solve_item)
         item_slot[par] = after;
@@ -1621,42 +1697,6 @@ bool chunk_tc_supported(const ChunkArgs& p) {
   return p.Dk == DK && p.Dv == DV && p.in_bf16 && tmap_encoder() != nullptr;
 }
 
-// Workspace: the tiles of every (chunk slot, value head), then one ready flag
-// per tile and the solve groups' item counter (used by the fused launch).
-// Then, for one sequence long enough to be split in two segments (kSplitMinChunks
-// chunks or more), the split's scratch: S_mid, Bst, Phi and the response rows R.
-namespace {
-constexpr int kSplitMinChunks = 32;
-
-struct SplitLayout {
-  int n, m;               // chunks, first chunk of the second segment
-  size_t off, bytes;      // byte offset of the scratch in the workspace, and its size
-};
-
-size_t tiles_and_flags_bytes(int num_seqs, int total, int Nv) {
-  const size_t tiles = ((size_t)(total / CT) + (size_t)num_seqs) * (size_t)Nv;
-  return tiles * TILE_T_BYTES + ((tiles + 1) * sizeof(int) + 255) / 256 * 256;
-}
-
-bool split_layout(int num_seqs, int total, int Nv, SplitLayout* L) {
-  const int n = (total + CT - 1) / CT;
-  if (num_seqs != 1 || n < kSplitMinChunks) return false;
-  L->n = n;
-  L->m = (n + 1) / 2;
-  L->off = tiles_and_flags_bytes(num_seqs, total, Nv);
-  const size_t st = (size_t)Nv * DK * DV * sizeof(float);
-  L->bytes = 3 * st + ((size_t)(total - L->m * CT) * Nv * DV * sizeof(bf16) + 255) / 256 * 256;
-  return true;
-}
-}  // namespace
-
-size_t chunk_tc_workspace_bytes(int num_seqs, int total, int Nv) {
-  SplitLayout L;
-  size_t bytes = tiles_and_flags_bytes(num_seqs, total, Nv);
-  if (split_layout(num_seqs, total, Nv, &L)) bytes += L.bytes;
-  return bytes;
-}
-
 namespace {
 // Per device: can one fused CTA stay resident on every SM (cooperative launch)?
 struct FusedDevice {
@@ -1706,6 +1746,73 @@ bool fused_device(int* sms) {
 }
 }  // namespace
 
+// ---- workspace plan
+// One sequence on a device that holds the cooperative launch: the solve tiles go
+// through a ring of kRing positions per segment and head (a solve item waits until
+// the chunk that last used its position has been released by every scan that reads
+// it), then one flag per (chunk, value head) -- 1 once the tiles are out, plus one per
+// consumer that released them -- and the solve's item counter; then, for a sequence
+// split in two segments (kSplitMinChunks chunks or more, and the SMs to hold the extra
+// scans), the split's scratch: S_mid, Bst, Phi and the response rows R.  The size does
+// not grow with the sequence beyond the flags (4 bytes per chunk and head) and R.
+// Packed batches: the tiles of every (chunk slot, value head) and the item counter.
+namespace {
+constexpr int kSplitMinChunks = 32;
+constexpr int kRing = 16;
+
+struct ChunkPlan {
+  bool fused;               // the one-sequence cooperative launch
+  int nseg, n, m;           // segments; chunks; first chunk of the second segment (n: none)
+  int ring;                 // tile positions per segment (0: one per chunk slot)
+  size_t tiles, nflags;
+  size_t flags_off, split_off, split_bytes, bytes;
+};
+
+ChunkPlan plan_chunk(int num_seqs, int total, int Nv, bool fused, bool split_ok) {
+  ChunkPlan L{};
+  L.n = (total + CT - 1) / CT;
+  L.fused = fused && num_seqs == 1;
+  if (L.fused) {
+    L.nseg = split_ok && L.n >= kSplitMinChunks ? 2 : 1;
+    L.m = L.nseg == 2 ? (L.n + 1) / 2 : L.n;
+    L.ring = std::max(1, std::min(kRing, L.m));          // the first segment is the longer one
+    L.tiles = (size_t)L.nseg * L.ring * Nv;
+    L.nflags = (size_t)L.n * Nv + 1;
+  } else {
+    L.nseg = 1;
+    L.m = L.n;
+    L.ring = 0;
+    L.tiles = ((size_t)(total / CT) + (size_t)num_seqs) * Nv;
+    L.nflags = 1;
+  }
+  L.flags_off = L.tiles * TILE_T_BYTES;
+  L.split_off = L.flags_off + (L.nflags * sizeof(int) + 255) / 256 * 256;
+  if (L.nseg == 2) {
+    const size_t st = (size_t)Nv * DK * DV * sizeof(float);
+    L.split_bytes = 3 * st + ((size_t)(total - L.m * CT) * Nv * DV * sizeof(bf16) + 255) / 256 * 256;
+  }
+  L.bytes = L.split_off + L.split_bytes;
+  return L;
+}
+
+// The plan a call takes on the current device.  A sequence is split when the SMs hold
+// three scans per head and at least two solve CTAs per head beside them (the two
+// segments' scans take twice the solve's output per period; with fewer solve SMs the
+// split runs slower than one chain: 264 vs 124 us at 32 heads, T = 4096, on 152 SMs),
+// and the output is the plain o (the gated norm of the fused epilogue cannot be
+// corrected afterwards).
+ChunkPlan device_plan(int num_seqs, int total, int Nv, bool allow_split, int* sms_out) {
+  int sms = 0;
+  const bool fused = num_seqs == 1 && fused_device(&sms) && sms > Nv;
+  if (sms_out) *sms_out = sms;
+  return plan_chunk(num_seqs, total, Nv, fused, allow_split && sms >= 5 * Nv);
+}
+}  // namespace
+
+size_t chunk_tc_workspace_bytes(int num_seqs, int total, int Nv, bool allow_split) {
+  return device_plan(num_seqs, total, Nv, allow_split, nullptr).bytes;
+}
+
 cudaError_t launch_chunk_tc(const ChunkArgs& args, cudaStream_t s) {
   ChunkArgs p = args;
   if (p.wait_ns == 0) p.wait_ns = kDefaultWaitNs;
@@ -1726,28 +1833,22 @@ cudaError_t launch_chunk_tc(const ChunkArgs& args, cudaStream_t s) {
   if (p.z != nullptr && !make_map(&mz, p.z, p.total, p.Nv * DV)) return cudaErrorInvalidValue;
   const int slots = p.total / CT + p.num_seqs;
   int sms = 0;
-  if (p.num_seqs == 1 && fused_device(&sms) && sms > p.Nv) {
+  const ChunkPlan L = device_plan(p.num_seqs, p.total, p.Nv, !p.no_split && p.z == nullptr, &sms);
+  if (L.fused) {
     // one sequence: solve and scan overlap in one cooperative launch
     uint8_t* ws = static_cast<uint8_t*>(p.workspace);
-    const int n = (p.total + CT - 1) / CT;
-    int nitems = n * p.Nv;
-    int* flags = reinterpret_cast<int*>(ws + (size_t)slots * p.Nv * TILE_T_BYTES);
-    cudaError_t e = cudaMemsetAsync(flags, 0, (size_t)(nitems + 1) * sizeof(int), s);
+    int nitems = L.n * p.Nv;
+    int* flags = reinterpret_cast<int*>(ws + L.flags_off);
+    cudaError_t e = cudaMemsetAsync(flags, 0, L.nflags * sizeof(int), s);
     if (e != cudaSuccess) return e;
     CUtensorMap mo = mk;                               // fp32 rows are stored directly
     if (p.out_bf16 && !make_map(&mo, p.o, p.total, p.Nv * DV)) return cudaErrorInvalidValue;
-    // A long sequence is split in two segments when the SMs hold three scans per head and
-    // at least two solve CTAs per head beside them (the two segments' scans take twice the
-    // solve's output per period; with fewer solve SMs the split runs slower than one chain:
-    // 264 vs 124 us at 32 heads, T = 4096, on 152 SMs), and the output is the plain o (the
-    // gated norm of the fused epilogue cannot be corrected afterwards).
-    SplitLayout L;
-    SplitArgs sp{1, n, n, nullptr, nullptr, nullptr, nullptr};
+    SplitArgs sp{1, L.n, L.n, L.ring, nullptr, nullptr, nullptr, nullptr};
     CUtensorMap mr = mk;
-    if (split_layout(1, p.total, p.Nv, &L) && p.z == nullptr && sms >= 5 * p.Nv) {
+    if (L.nseg == 2) {
       const size_t st = (size_t)p.Nv * DK * DV;
-      float* scr = reinterpret_cast<float*>(ws + L.off);
-      sp = SplitArgs{2, L.m, n, scr, scr + st, scr + 2 * st, reinterpret_cast<bf16*>(scr + 3 * st)};
+      float* scr = reinterpret_cast<float*>(ws + L.split_off);
+      sp = SplitArgs{2, L.m, L.n, L.ring, scr, scr + st, scr + 2 * st, reinterpret_cast<bf16*>(scr + 3 * st)};
       if (!make_map(&mr, sp.R, p.total - L.m * CT, p.Nv * DV)) return cudaErrorInvalidValue;
     }
     int nscan = sp.nseg == 2 ? 3 * p.Nv : p.Nv;
@@ -1759,7 +1860,9 @@ cudaError_t launch_chunk_tc(const ChunkArgs& args, cudaStream_t s) {
     const double per_scan = (double)(sms - nscan) / (double)(sp.nseg * p.Nv);
     int ngroups = per_scan >= 5.3 ? 1 : 3;
     if (p.no_solve) ngroups = 0;           // test hook: no flag is ever published
-    void* args[] = {&mq, &mk, &mv, &mo, &mz, &mr, &pc, &sp, &nscan, &nitems, &flags, &ngroups};
+    // the scan CTAs of the first and of the second segment solve their first chunk themselves
+    int skip = p.no_solve ? 0 : sp.nseg * p.Nv;
+    void* args[] = {&mq, &mk, &mv, &mo, &mz, &mr, &pc, &sp, &nscan, &nitems, &skip, &flags, &ngroups};
     const void* fn = fused_kernels()[(p.out_bf16 ? 0 : 2) + (p.z != nullptr ? 1 : 0)];
     e = cudaLaunchCooperativeKernel(fn, dim3(sms), dim3(NT3), args, K3_SMEM, s);
     if (e != cudaSuccess || sp.nseg == 1) return e;
@@ -1792,7 +1895,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs& args, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   // the item counter sits in the workspace's flag area
   const int nitems = slots * p.Nv;
-  int* counter = reinterpret_cast<int*>(static_cast<uint8_t*>(p.workspace) + (size_t)nitems * TILE_T_BYTES);
+  int* counter = reinterpret_cast<int*>(static_cast<uint8_t*>(p.workspace) + L.flags_off);
   e = cudaMemsetAsync(counter, 0, sizeof(int), s);
   if (e != cudaSuccess) return e;
   const int nsm = num_sms();

@@ -563,6 +563,49 @@ cudaError_t launch_typed(const ConvGatingArgs& p, cudaStream_t s) {
 
 }  // namespace
 
+// ---------------------------------------------------------------------------
+// conv state after every token (the rollback points of a draft + verify step):
+// step_states[t] = the last three raw inputs up to and including token t of its
+// sequence, oldest first, with the sequence's state in before its first token.
+// One thread per (token, channel).
+// ---------------------------------------------------------------------------
+namespace {
+template <typename Tin>
+__global__ void conv_state_steps_kernel(ConvGatingArgs p, Tin* steps) {
+  const int t = blockIdx.y;
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= p.C) return;
+  const int s = find_seq(p.cu, p.num_seqs, p.total, t);
+  int bos, eos;
+  if (!seq_bounds(p.cu, p.num_seqs, p.total, s, bos, eos) || t < bos || t >= eos) {
+    if (c == 0) raise_error(p.err, kDevErrSeqlens);
+    return;
+  }
+  const int i = t - bos;
+  const Tin* x = static_cast<const Tin*>(p.x);
+  const Tin* sin = static_cast<const Tin*>(p.state_in);
+  Tin out[3];
+#pragma unroll
+  for (int j = 0; j < 3; ++j) {
+    const int q = i + 1 + j;                  // index into [state in (3) ; the sequence's inputs]
+    out[j] = q >= 3 ? x[(size_t)(bos + q - 3) * p.C + c]
+                    : (sin ? sin[((size_t)s * p.C + c) * 3 + q] : from_f32<Tin>(0.f));
+  }
+#pragma unroll
+  for (int j = 0; j < 3; ++j) steps[((size_t)t * p.C + c) * 3 + j] = out[j];
+}
+}  // namespace
+
+cudaError_t launch_conv_state_steps(const ConvGatingArgs& p, void* steps, cudaStream_t s) {
+  if (p.total == 0) return cudaSuccess;
+  dim3 grid((p.C + 255) / 256, p.total);
+  if (p.in_bf16)
+    conv_state_steps_kernel<bf16><<<grid, 256, 0, s>>>(p, static_cast<bf16*>(steps));
+  else
+    conv_state_steps_kernel<float><<<grid, 256, 0, s>>>(p, static_cast<float*>(steps));
+  return cudaGetLastError();
+}
+
 cudaError_t launch_conv_gating(const ConvGatingArgs& p, cudaStream_t s) {
   if (p.in_bf16) {
     return p.out_bf16 ? launch_typed<bf16, bf16>(p, s) : launch_typed<bf16, float>(p, s);

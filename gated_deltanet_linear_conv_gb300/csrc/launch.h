@@ -30,6 +30,8 @@ struct ConvGatingArgs {
   int* err;
 };
 cudaError_t launch_conv_gating(const ConvGatingArgs& p, cudaStream_t s);
+// The conv state after every token ([tokens, C, 3], the input element type).
+cudaError_t launch_conv_state_steps(const ConvGatingArgs& p, void* steps, cudaStream_t s);
 
 struct GatingArgs {
   const void* a; const void* b; const float* A_log; const float* dt_bias;
@@ -86,13 +88,16 @@ struct ChunkArgs {
   // bound of each wait of the scan on a flag or barrier, in ns of device time (0: the default)
   unsigned long long wait_ns;
   int no_solve;                                  // test hook: the one-sequence launch runs no solve
+  int no_split;                                  // never split a long sequence (smaller workspace)
 };
 constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
 // Portable fp32 CUDA-core implementation of the chunk form.
 cudaError_t launch_chunk_simt(const ChunkArgs& p, cudaStream_t s);
 // tcgen05 tensor-core implementation (bf16 q/k/v, Dk = Dv = 128).
 bool chunk_tc_supported(const ChunkArgs& p);
-size_t chunk_tc_workspace_bytes(int num_seqs, int total, int Nv);
+// Workspace bytes of a call on the current device (allow_split: a long single sequence may
+// run split in two segments, which needs extra scratch).
+size_t chunk_tc_workspace_bytes(int num_seqs, int total, int Nv, bool allow_split = true);
 cudaError_t launch_chunk_tc(const ChunkArgs& p, cudaStream_t s);
 // Fixed-size device scratch owned by the library (see gdn_chunk_prefill_static).
 constexpr size_t kStaticScratchBytes = (size_t)32 << 20;

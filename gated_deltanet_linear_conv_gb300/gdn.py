@@ -20,6 +20,7 @@ GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_CUDA, GDN_ERR_DEVICE =
 GDN_BF16, GDN_F32 = 0, 1
 
 EXPORTS = ('gdn_version', 'gdn_last_error_string', 'gdn_check_device_error', 'gdn_conv_gating',
+           'gdn_conv_state_steps',
            'gdn_gating', 'gdn_chunk_prefill_workspace_size', 'gdn_chunk_prefill',
            'gdn_chunk_prefill_fp32', 'gdn_chunk_prefill_static', 'gdn_chunk_prefill_gated_norm',
            'gdn_recurrent_decode', 'gdn_recurrent_decode_steps',
@@ -47,6 +48,7 @@ _SIGS = {
     'gdn_conv_gating': ([_DIMS, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _F, _F,
                          _P, _P, _P, _I, _P, _P, _P], _I),
     'gdn_gating': ([_I64, ctypes.c_int32, _P, _P, _I, _P, _P, _P, _P, _P], _I),
+    'gdn_conv_state_steps': ([_DIMS, _P, _P, _I, _P, _P, _P], _I),
     'gdn_chunk_prefill_workspace_size': ([_DIMS, ctypes.POINTER(_SZ)], _I),
     'gdn_chunk_prefill': ([_DIMS, _P, _P, _P, _P, _I, _P, _P, _F, _P, _P, _P, _I, _P, _SZ, _P], _I),
     'gdn_chunk_prefill_fp32': ([_DIMS, _P, _P, _P, _P, _I, _P, _P, _F, _P, _P, _P, _I, _P], _I),
@@ -153,6 +155,22 @@ def conv_gating(mixed_qkv, conv_w, a, b, A_log, dt_bias, Nk, Nv, Dk, Dv, cu_seql
                                _ptr(v), _dt(q), _ptr(g), _ptr(beta), _stream())
     _check(st, 'gdn_conv_gating')
     return q, k, v, g, beta
+
+
+def conv_state_steps(mixed_qkv, Nk, Nv, Dk, Dv, conv_state_in=None, cu_seqlens=None, num_seqs=1, out=None):
+    """gdn_conv_state_steps: the conv state after every token, [tokens, C, 3]."""
+    T, C = mixed_qkv.shape
+    if cu_seqlens is not None:
+        num_seqs = cu_seqlens.numel() - 1
+    if out is None:
+        out = torch.empty(T, C, 3, dtype=mixed_qkv.dtype, device=mixed_qkv.device)
+    if conv_state_in is not None and conv_state_in.dtype != mixed_qkv.dtype:
+        raise ValueError('conv_state_in shares the dtype of mixed_qkv')
+    d = _dims(num_seqs, T, Nk, Nv, Dk, Dv)
+    st = lib().gdn_conv_state_steps(ctypes.byref(d), _ptr(cu_seqlens), _ptr(mixed_qkv), _dt(mixed_qkv),
+                                    _ptr(conv_state_in), _ptr(out), _stream())
+    _check(st, 'gdn_conv_state_steps')
+    return out
 
 
 def gating(a, b, A_log, dt_bias, out=None):

@@ -140,6 +140,23 @@ int gdn_conv_gating(const gdn_dims* dims, const int32_t* cu_seqlens,
                     float* g, float* beta, void* stream);
 
 /* ------------------------------------------------------------------------
+ * gdn_conv_state_steps -- the conv state after every token: the rollback
+ * points of a multi-token (draft + verify) decode step, beside the recurrent
+ * states of gdn_recurrent_decode_steps; a caller that accepts the first j + 1
+ * tokens of a sequence keeps step_states[bos + j] as its conv state.  With
+ * xpad = [conv_state_in (3 oldest-first inputs, or zeros) ; x] of a sequence
+ * ([QDA] "Cache": the conv cache keeps the latest raw inputs), token i of it
+ * gets step_states[bos + i] = xpad[i + 1 .. i + 3] (oldest first).  The last
+ * token's entry equals the conv_state_out of gdn_conv_gating.
+ *   mixed_qkv      [tokens, C]          in_dtype
+ *   conv_state_in  [N, C, 3] in_dtype, or NULL (zeros); the state the tokens
+ *                  follow -- read it before an in-place update of it
+ *   step_states    [tokens, C, 3]       in_dtype, written
+ * ------------------------------------------------------------------------ */
+int gdn_conv_state_steps(const gdn_dims* dims, const int32_t* cu_seqlens, const void* mixed_qkv, int in_dtype,
+                         const void* conv_state_in, void* step_states, void* stream);
+
+/* ------------------------------------------------------------------------
  * gdn_gating -- step a3 alone, for callers that already hold q, k, v:
  *   beta[t, h] = sigmoid(b[t, h]);  g[t, h] = -exp(A_log[h]) * softplus(a[t, h] + dt_bias[h])
  *   a, b [rows, Nv] in_dtype; A_log, dt_bias [Nv] float32; g, beta [rows, Nv] float32.
@@ -161,12 +178,22 @@ int gdn_gating(int64_t rows, int32_t num_v_heads, const void* a, const void* b, 
  * fp32 accumulation and state); fp32 inputs and 64-wide heads run the fp32
  * CUDA-core kernel of gdn_chunk_prefill_fp32.
  *
- * Launches: on the tensor-core path, a memset of the workspace's ready flags
- * and then, for one sequence, a single cooperative launch (one CTA per SM;
- * the scan of each head overlaps the solve of later chunks), or, for packed
- * batches, a solve kernel and a scan kernel.  The workspace holds the
- * per-(chunk, head) solve tiles and those flags; one workspace must not be
- * shared by calls that can run at the same time.
+ * Launches: on the tensor-core path, a memset of the workspace's flags and
+ * then, for one sequence, a single cooperative launch (one CTA per SM; the
+ * scan of each head overlaps the solve of later chunks), or, for packed
+ * batches, a solve kernel and a scan kernel.  One long sequence (32 chunks or
+ * more) runs split in two segments when the device holds three scans per head
+ * and two solve CTAs per head beside them (with Nv = 32 that needs 160 SMs):
+ * the second segment is scanned from a zero state and its transition map beside
+ * the first, and a fix-up kernel adds the first segment's final state's share
+ * to its outputs and to the final state.
+ * The workspace of one sequence holds a ring of 16 solve-tile positions per
+ * head (and segment), one flag per (chunk, head), and the split's scratch when
+ * it splits: it grows by 4 bytes per chunk and head (plus, split, 128 bytes per
+ * token and head), not by the 49,664-byte tile of every chunk.  Packed batches
+ * keep one tile per (chunk, head).  The size is for the current device (its SM
+ * count decides the split).  One workspace must not be shared by calls that
+ * can run at the same time.
  *
  *   q, k           [tokens, Nk, Dk]     in_dtype
  *   v              [tokens, Nv, Dv]     in_dtype
@@ -238,10 +265,13 @@ int gdn_chunk_prefill_fp32(const gdn_dims* dims, const int32_t* cu_seqlens,
  * allocates or frees.
  *   - Supported inputs: bf16 q/k/v with Dk = Dv = 128 (else
  *     GDN_ERR_UNSUPPORTED).
- *   - Size limit: the workspace that gdn_chunk_prefill_workspace_size()
- *     reports for these dims must be at most 32 MiB (for 32 value heads and
- *     one sequence, about 1,280 tokens); larger problems return
- *     GDN_ERR_INVALID_ARG and should use gdn_chunk_prefill.
+ *   - Size limit: the workspace of these dims, laid out without the split of a
+ *     long sequence, must be at most 32 MiB.  One sequence of any length up to
+ *     about 4 million tokens fits (its solve tiles go through a fixed ring; at
+ *     32 value heads the ring takes 25.4 MB), but it never runs split.  Packed
+ *     batches keep a tile per (chunk, head): at 32 value heads, about 1,200
+ *     tokens in all.  Larger problems return GDN_ERR_INVALID_ARG and should use
+ *     gdn_chunk_prefill.
  *   - The first call on a device looks up the scratch array's device address
  *     (once per device, with that device current); make that first call before
  *     any stream capture.

@@ -420,3 +420,57 @@ def test_chunk_prefill_one_long_sequence(T, odt, state):
         assert_close(np64(S), rS, TOL_BF16)
     else:
         assert S is None
+
+
+# ------------------------------------------------------------------ draft + verify decode, both states
+
+def test_verify_decode_rolls_back_conv_and_recurrent_state():
+    """A multi-token (1 + 3 tokens) decode step of the mixer core with the rollback
+    points of both caches: the conv state after every token (gdn_conv_state_steps)
+    against the oracle's state after each prefix, bit for bit, and the recurrent
+    state after every token (gdn_recurrent_decode_steps).  Rolling sequence 1 back to
+    its second token and replaying its last two tokens from the two kept states
+    reproduces the first pass."""
+    shape = SHAPES[0]
+    lengths = [4, 4, 4]
+    inp = I.make_mixer_inputs(77, lengths, shape, dtype=torch.bfloat16, conv_state_std=1.0, S0_std=0.05)
+    sh = inp.shape
+    cu = inp.cu_seqlens()
+    cu_l = cu.tolist()
+    x, w = cuda(inp.mixed_qkv), cuda(inp.conv_w)
+    cs_in = cuda(inp.conv_state)
+    conv_steps = gdn.conv_state_steps(x, sh.Nk, sh.Nv, sh.Dk, sh.Dv, conv_state_in=cs_in, cu_seqlens=cuda(cu))
+    cs_out = torch.empty_like(cs_in)
+    q, k, v, g, beta = gdn.conv_gating(x, w, cuda(inp.a), cuda(inp.b), cuda(inp.A_log), cuda(inp.dt_bias),
+                                       sh.Nk, sh.Nv, sh.Dk, sh.Dv, cu_seqlens=cuda(cu), conv_state_in=cs_in,
+                                       conv_state_out=cs_out, out_dtype=torch.float32)
+    S = cuda(inp.S0.clone())
+    rec_steps = torch.empty(sum(lengths), sh.Nv, sh.Dk, sh.Dv, device='cuda')
+    o = gdn.recurrent_decode(q, k, v, g, beta, S, 1.0, cu_seqlens=cuda(cu), out_dtype=torch.float32,
+                             step_states=rec_steps)
+    torch.cuda.synchronize()
+    gdn.check_device_error()
+    # every step's conv state against the oracle's state after that prefix (raw copies: exact)
+    xs = np64(inp.mixed_qkv)
+    for s in range(len(lengths)):
+        for j in range(lengths[s]):
+            _, st = O.causal_conv1d(xs[cu_l[s]:cu_l[s] + j + 1], np64(inp.conv_w), None, np64(inp.conv_state[s]))
+            np.testing.assert_array_equal(np64(conv_steps[cu_l[s] + j]), st)
+        assert torch.equal(conv_steps[cu_l[s + 1] - 1], cs_out[s])       # the last step is the new state
+    ref = O.mixer_prefill(xs, np64(inp.conv_w), np64(inp.a), np64(inp.b), np64(inp.A_log), np64(inp.dt_bias),
+                          np64(inp.z), np64(inp.norm_w), sh.Nk, sh.Nv, sh.Dk, sh.Dv, cu_seqlens=cu.numpy(),
+                          conv_state=np64(inp.conv_state), initial_state=np64(inp.S0))
+    assert_close(np64(o), ref['o'], TOL_F32)
+    # roll sequence 1 back to its second token (keep both states there) and replay tokens 2-3
+    b0 = cu_l[1]
+    tail = slice(b0 + 2, b0 + 4)
+    cs1 = conv_steps[b0 + 1].unsqueeze(0).contiguous()
+    S1 = rec_steps[b0 + 1].unsqueeze(0).clone()
+    q2, k2, v2, g2, beta2 = gdn.conv_gating(cuda(inp.mixed_qkv[tail].contiguous()), w, cuda(inp.a[tail].contiguous()),
+                                            cuda(inp.b[tail].contiguous()), cuda(inp.A_log), cuda(inp.dt_bias),
+                                            sh.Nk, sh.Nv, sh.Dk, sh.Dv, num_seqs=1, conv_state_in=cs1,
+                                            out_dtype=torch.float32)
+    o2 = gdn.recurrent_decode(q2, k2, v2, g2, beta2, S1, 1.0, num_seqs=1, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    torch.testing.assert_close(o2, o[tail], rtol=1e-5, atol=1e-6)
+    torch.testing.assert_close(S1[0], S[1], rtol=1e-5, atol=1e-6)

@@ -79,9 +79,29 @@ def test_static_scratch_one_sequence_twice():
     gdn.check_device_error()
 
 
+def test_static_scratch_long_single_sequence():
+    """One sequence's solve tiles go through a fixed ring, so the fixed scratch holds a
+    sequence far longer than its tiles would need one by one (8192 tokens, 32 heads)."""
+    shape = I.MixerShape(16, 32, 128, 128)
+    T = 8192
+    c = I.make_core_inputs(95, [T], shape, dtype=torch.bfloat16, S0_std=0.05)
+    g, beta = O.gating(np64(c.a), np64(c.b), np64(c.A_log), np64(c.dt_bias))
+    gt, bt = torch.tensor(g, dtype=torch.float32).cuda(), torch.tensor(beta, dtype=torch.float32).cuda()
+    q, k, v, S0 = c.q.cuda(), c.k.cuda(), c.v.cuda(), c.S0.cuda()
+    o_ref, S_ref = gdn.chunk_prefill(q, k, v, gt, bt, 1.0, initial_state=S0, out_dtype=torch.float32)
+    o = torch.empty_like(o_ref)
+    ST = torch.empty_like(S_ref)
+    _static_call(q, k, v, gt, bt, 1.0, S0, ST, o, None, 1)
+    torch.cuda.synchronize()
+    assert_close(np64(o), np64(o_ref), TOL_BF16)
+    assert_close(np64(ST), np64(S_ref), TOL_BF16)
+    gdn.check_device_error()
+
+
 def test_static_scratch_rejects_too_large():
-    T, Nk, Nv, D = 131072, 16, 32, 128
-    d = gdn.gdn_dims(1, T, Nk, Nv, D, D)
+    # a packed batch keeps one tile per (chunk, head): 4 x 32768 tokens at 32 heads is far past it
+    T, N, Nk, Nv, D = 131072, 4, 16, 32, 128
+    d = gdn.gdn_dims(N, T, Nk, Nv, D, D)
     x = torch.empty(16, dtype=torch.bfloat16, device='cuda')      # never read: rejected before launch
     f = torch.empty(16, device='cuda')
     st = gdn.lib().gdn_chunk_prefill_static(
