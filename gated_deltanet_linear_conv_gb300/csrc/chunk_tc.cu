@@ -787,6 +787,7 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int dv = (warp & 3) * 32 + lane;        // this thread's tensor-memory lane
+
   const int hk = h / (p.Nv / p.Nk);
   int bos, eos;
   if (!seq_bounds(p.cu, p.num_seqs, p.total, s, bos, eos)) {
@@ -953,14 +954,18 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
     // ============================== STATE ==============================
     const bool leader = tid == 32;
     {
-      // S^T <- initial state (S0 is [dk][dv]: thread dv reads a column), or the identity
+      // S^T <- initial state (S0 is [dk][dv]: thread dv reads a column), or the identity;
+      // every load is issued before the first store (one memory round trip, not four)
       const float* src = sg.S0 ? sg.S0 + dv : nullptr;
+      float s0v[DK];
+#pragma unroll
+      for (int i = 0; i < DK; ++i)
+        s0v[i] = sg.identity ? (i == dv ? 1.f : 0.f) : (src ? __ldg(src + (size_t)i * DV) : 0.f);
 #pragma unroll
       for (int c0 = 0; c0 < DK; c0 += 32) {
         float v[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          v[i] = sg.identity ? (c0 + i == dv ? 1.f : 0.f) : (src ? __ldg(src + (size_t)(c0 + i) * DV) : 0.f);
+        for (int i = 0; i < 32; ++i) v[i] = s0v[c0 + i];
         tmem_st32(lane_base + TM_S + c0, v);
       }
       tmem_st_wait();
