@@ -335,6 +335,7 @@ struct SolveAhead {
   bool tiles;    // its Q, K tiles were issued into the QK buffer (on the group's mbarrier)
   bool gate;     // gb holds this thread's gate value of it
   float gb;
+  int slot, c0, len;   // its chunk slot and token range (slot -1: not known yet)
 };
 
 __device__ __forceinline__ void st_release(int* f, int v) {
@@ -354,8 +355,8 @@ __device__ __forceinline__ int claim_item(int* counter) {
 // shared memory (S1_BYTES), bar an initialised mbarrier whose next phase
 // parity is ph & 1 (ph advances by three), tbase 128 allocated tensor-memory
 // columns.  The tiles go to workspace tile `tile` (of the item's head) as direct
-// 16-byte row stores, once `rel` (if given) reached rel_need; when this returns every
-// thread has fenced them (visible device-wide).  `ahead` carries the
+// 16-byte stores, once `rel` (if given) reached rel_need; when this returns, thread 0
+// has fenced them for the group after a barrier (its release of a flag publishes them).  `ahead` carries the
 // loads this item issues for the next one (nslot < 0: none): its gate values, in
 // flight under this item's A and P rows, and its Q, K tiles, issued by thread 0 as
 // soon as this item's W product has completed (the last reader of the QK buffer).
@@ -374,9 +375,12 @@ __device__ bool solve_item(uint8_t* sm, int tid, uint32_t barid, uint64_t* bar, 
   float* Alp = Dec + CT;                 // e^(G_t - G_(t-1))
   const int warp = tid >> 5, lane = tid & 31;
   int c0 = 0, len = 0;
-  const bool used = slot_chunk(p, slot, c0, len);
+  const bool used = ahead.slot == slot ? (c0 = ahead.c0, len = ahead.len, true) : slot_chunk(p, slot, c0, len);
   int nc0 = 0, nlen = 0;
   const bool nused = nslot >= 0 && slot_chunk(p, nslot, nc0, nlen);
+  ahead.slot = nused ? nslot : -1;     // (the next item reuses its range)
+  ahead.c0 = nc0;
+  ahead.len = nlen;
   if (!used) {                // nothing to solve (tiles are only ever prefetched for used slots)
     ahead.gate = false;
     return true;
@@ -560,25 +564,39 @@ __device__ bool solve_item(uint8_t* sm, int tid, uint32_t barid, uint64_t* bar, 
     ok = mbar_wait(bar, ph & 1u, WAIT_LIMIT);
     if (!named_sync_or(barid, 128, !ok)) {
       tc_fence_after();
-      // the W product was the QK buffer's last reader: the next item's tiles may land there
-      if (tid == 0 && nused) solve_load_tiles(sm, bar, tmq, tmk, p, nc0, nh);
-      ahead.tiles = nused;
-      {   // warps 0-1: columns 0-63 of rows 0-63; warps 2-3: columns 64-127 of the copy
+      {   // -W, swizzled, over the K tiles (the W product has read them): warps 0-1 columns
+          // 0-63 of rows 0-63, warps 2-3 columns 64-127 of the copy
         const int half = tid >> 6;
         float v[64];
         tm_ld64(lane_base + half * 64, v);
-        st_row64_global(ws + WS_QW + half * 16384, tid & 63, v, -1.f);
+#pragma unroll
+        for (int i = 0; i < 64; ++i) v[i] = -v[i];
+        st_row64(sm, S1_QK + half * 16384, tid & 63, v);
       }
+      named_sync(barid, 128);
+      // ... and out to the workspace in 512-byte runs per warp instruction (the row per
+      // thread above would touch 32 lines per instruction)
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int i = tid + 128 * k;                  // 16-byte chunk of the two 8 KB boxes
+        const uint32_t off = (uint32_t)(i >> 9) * 16384u + (uint32_t)(i & 511) * 16u;
+        *reinterpret_cast<uint4*>(ws + WS_QW + off) = *reinterpret_cast<const uint4*>(sm + S1_QK + off);
+      }
+      named_sync(barid, 128);
+      // the QK buffer is free: the next item's tiles may land there
+      if (tid == 0 && nused) solve_load_tiles(sm, bar, tmq, tmk, p, nc0, nh);
+      ahead.tiles = nused;
       done = true;
     }
   }
   ph += 1;
   if (!done && tid == 0) raise_error(p.err, kDevErrTimeout);
-  __threadfence();                   // this thread's tile stores are visible device-wide
-  // the next item may reuse this shared and tensor memory
+  // the next item may reuse this shared and tensor memory; thread 0 then fences for the
+  // group (the barrier orders every thread's tile stores before its fence and flag)
   tc_fence_before();
   named_sync(barid, 128);
   tc_fence_after();
+  if (tid == 0) __threadfence();
   return done;
 }
 
@@ -610,7 +628,7 @@ chunk_solve_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
   }
   __syncthreads();
   int item = item_slot[0], next = item_slot[1];
-  SolveAhead ahead{false, false, 0.f};
+  SolveAhead ahead{false, false, 0.f, -1, 0, 0};
   int par = 0;
   while (item < nitems) {
     const int after = tid == 0 && next < nitems ? claim_item(counter) : nitems;
@@ -1401,7 +1419,7 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
       __syncthreads();
       tc_fence_after();
       if (tid < 128) {
-        SolveAhead ahead{false, false, 0.f};
+        SolveAhead ahead{false, false, 0.f, -1, 0, 0};
         uint32_t ph = 0;
         const bool ok = solve_item(sm, tid, 1, bar, ph, *tslot, &tmq, &tmk, p, c, h, ahead, -1, 0,
                                    (size_t)(role * sp.ring), nullptr, 0);
@@ -1468,7 +1486,7 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
     }
     named_sync(barid, 128);
     int item = item_slot[0], next = item_slot[1];
-    SolveAhead ahead{false, false, 0.f};
+    SolveAhead ahead{false, false, 0.f, -1, 0, 0};
     int par = 0;
     while (item < nitems) {
       const int after = tid == 0 && next < nitems ? claim_item(counter) : nitems;   // read after the item
