@@ -1328,14 +1328,39 @@ __device__ __forceinline__ ScanSeg whole_seq(const ChunkArgs& p, int h, int s, c
   return sg;
 }
 
+// Packed batches: CTA i scans value head i % Nv of the sequence of length rank i / Nv
+// (longest first, ties by index): CTAs start in index order, so the long chains start
+// first and the short ones fill in behind them.
 template <typename Tout, bool NORM>
 __global__ void __launch_bounds__(NT2, 1)
 chunk_scan_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   const __grid_constant__ CUtensorMap tmo, const __grid_constant__ CUtensorMap tmz, ChunkArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const ScanSeg sg = whole_seq(p, blockIdx.x, blockIdx.y, &tmo);
-  scan_body<Tout, NORM>(sm, &tmk, &tmv, sg, &tmz, p, blockIdx.x, blockIdx.y, nullptr);
+  const int h = blockIdx.x % p.Nv, rank = blockIdx.x / p.Nv;
+  volatile int* pick = reinterpret_cast<volatile int*>(sm + K2_BAR + 248);   // before the barriers' set-up
+  if (threadIdx.x == 0) *pick = rank;                // (equal lengths: the identity)
+  __syncthreads();
+  if (p.cu != nullptr) {
+    auto len = [&](int q) {
+      const int a = __ldg(p.cu + q), b = __ldg(p.cu + q + 1);
+      return b > a ? b - a : 0;
+    };
+    for (int q = threadIdx.x; q < p.num_seqs; q += blockDim.x) {
+      const int lq = len(q);
+      int r = 0;
+      for (int o = 0; o < p.num_seqs; ++o) {
+        const int lo = len(o);
+        r += lo > lq || (lo == lq && o < q);
+      }
+      if (r == rank) *pick = q;
+    }
+  }
+  __syncthreads();
+  const int s = *pick;
+  __syncthreads();
+  const ScanSeg sg = whole_seq(p, h, s, &tmo);
+  scan_body<Tout, NORM>(sm, &tmk, &tmv, sg, &tmz, p, h, s, nullptr);
 }
 
 // ---------------------------------------------------------------------------
@@ -1709,7 +1734,7 @@ cudaError_t launch_scan(const CUtensorMap& mk, const CUtensorMap& mv, const CUte
   const auto fn = p.z != nullptr ? chunk_scan_kernel<Tout, true> : chunk_scan_kernel<Tout, false>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)K2_SMEM);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.Nv, p.num_seqs);
+  dim3 grid(p.Nv * p.num_seqs);
   fn<<<grid, NT2, K2_SMEM, s>>>(mk, mv, mo, mz, p);
   return cudaGetLastError();
 }
