@@ -267,9 +267,11 @@ __device__ __forceinline__ void invert_unit_lower(const float* AT, float* TR, fl
 }
 
 // The scan's waits are bounded in time: each gives up after limit_ns of device
-// time (%globaltimer) since it started, or at once when another role of the CTA
-// aborted.  A poll cap far above any limit in use ends the loop even if the timer
-// were not to advance.
+// time (%globaltimer), or at once when another role of the CTA aborted.  An mbarrier
+// wait takes its start time on entry; a flag poll reads the timer only every 64th
+// poll, the first such read being its start.  A poll cap far above any limit in use
+// ends the loop even if the timer were not to advance.  (The mbarrier wait has no
+// separate test_wait fast path: the smaller inlined loop measured faster.)
 struct WaitCtl {
   volatile int* abort;
   uint64_t limit_ns;
@@ -692,13 +694,14 @@ struct ScanBars {
   uint64_t gh;       // state update complete
   uint64_t zb[2];    // z tile of a chunk landed in its output buffer (gated norm)
   uint64_t ub[2];    // U^T of a chunk in tensor memory as bf16 and its S^T update issued
+  uint64_t s0f;      // the initial state landed in shared memory (bulk copies)
+  uint64_t s0c;      // the state role has moved it into tensor memory (128 arrivals)
   uint32_t tslot;
   int abort;
 };
 static_assert(sizeof(ScanBars) <= 256, "scan barriers fit their slot");
 
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const WaitCtl& w) {
-  if (mbar_test_wait(bar, parity)) return true;      // already complete: no suspension
   const uint64_t t0 = global_ns();
   for (uint32_t i = 1; i < POLL_CAP; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -751,7 +754,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // Bounded wait until the solve of one (chunk slot, value head) published
 // its workspace tiles (1), or reported a failure (-1).
 __device__ __forceinline__ bool wait_flag(const int* f, const WaitCtl& w) {
-  const uint64_t t0 = global_ns();
+  uint64_t t0 = 0;
   for (uint32_t i = 0; i < POLL_CAP; ++i) {
     int v;
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
@@ -759,7 +762,12 @@ __device__ __forceinline__ bool wait_flag(const int* f, const WaitCtl& w) {
       asm volatile("fence.proxy.async.global;" ::: "memory");   // the tiles are read by the copy engine
       return true;
     }
-    if (v < 0 || *w.abort || global_ns() - t0 > w.limit_ns) break;
+    if (v < 0 || *w.abort) break;
+    if ((i & 63u) == 63u) {
+      const uint64_t now = global_ns();
+      if (t0 == 0) t0 = now;
+      else if (now - t0 > w.limit_ns) break;
+    }
     __nanosleep(100);
   }
   *w.abort = 1;
@@ -839,6 +847,8 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
     mbar_init(&B->gh, 1);
     mbar_init(&B->zb[0], 1);
     mbar_init(&B->zb[1], 1);
+    mbar_init(&B->s0f, 1);
+    mbar_init(&B->s0c, 128);
     B->abort = 0;
     fence_barrier_init();
     prefetch_tmap(tmk);
@@ -857,6 +867,21 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
   const uint32_t tbase = B->tslot;
   const uint32_t lane_base = tbase + ((uint32_t)((warp & 3) * 32) << 16);
   const uint32_t sb = smem_u32(sm);
+
+  // The initial state arrives by four 16 KB bulk copies issued before any role starts (a
+  // thread's 128 dependent-free column loads from global memory took about 10 us at the
+  // start of a launch): rows 32q .. 32q + 31 into the second stage buffer (q < 3) and into
+  // the head of the second v buffer (q = 3).  Both are first written by the loads of chunk
+  // 1, which wait until the state role has moved the state into tensor memory (s0c).  (The
+  // host requires every pointer to be 16-byte aligned, as the copies do.)
+  const bool s0_bulk = sg.S0 != nullptr && !sg.identity;
+  auto s0_part = [&](int q) -> uint8_t* {
+    return sm + (q < 3 ? K2_ST + STAGE_BYTES + (uint32_t)q * 16384u : K2_VT + 32768u);
+  };
+  if (tid == 0 && s0_bulk) {
+    mbar_arrive_expect_tx(&B->s0f, 65536);
+    for (int q = 0; q < 4; ++q) bulk_load(s0_part(q), sg.S0 + (size_t)q * 32 * DV, 16384, &B->s0f);
+  }
 
   // loads of a chunk: v tiles and T diag(beta) (for [U~^T | 0]), and the stage
   auto issue_vt = [&](int c) {
@@ -900,7 +925,9 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
         // period before the stage buffer does
         ok = wait_flag(flags + (size_t)(slot0 + c) * p.Nv + h, wc);
         if (!sg.zero_v) {
-          if (ok && c >= 2) ok = wait_bar(&B->ready[c & 1], ((c - 2) >> 1) & 1, wc);   // v tiles free
+          // v tiles free (for c = 1: the state's copy in that buffer was read)
+          if (ok && (c >= 2 || (c == 1 && s0_bulk)))
+            ok = c >= 2 ? wait_bar(&B->ready[c & 1], ((c - 2) >> 1) & 1, wc) : wait_bar(&B->s0c, 0, wc);
           if (!ok) break;
           issue_vt(c);
           vt_issued = c + 1;
@@ -916,7 +943,7 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
           int* rel = flags_rw + (size_t)(slot0 + c - 2) * p.Nv + h;
           asm volatile("red.relaxed.gpu.global.add.s32 [%0], 1;" ::"l"(rel) : "memory");
         }
-        issue_stage(c);
+        issue_stage(c);        // (for c = 1 after the v tiles' wait for the state's copy above)
         st_issued = c + 1;
       }
       if (!ok) {     // let the copies in flight land (the waits are bounded)
@@ -939,8 +966,14 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
     // ============================== PREP ==============================
     if (lane == 0) {
       int issued = 0, committed = 0, c = 0;
-      if (self_load)
-        while (issued < n && issued < 2 && issue_vt(issued)) ++issued;
+      if (self_load && n > 0) {
+        issue_vt(0);
+        issued = 1;
+        if (n > 1 && (!s0_bulk || wait_bar(&B->s0c, 0, wc))) {
+          issue_vt(1);
+          issued = 2;
+        }
+      }
       bool ok = true;
       for (; c < n; ++c) {
         const int b = c & 1;
@@ -971,20 +1004,29 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
   } else if (warp <= 4) {
     // ============================== STATE ==============================
     const bool leader = tid == 32;
-    {
-      // S^T <- initial state (S0 is [dk][dv]: thread dv reads a column), or the identity;
-      // every load is issued before the first store (one memory round trip, not four)
-      const float* src = sg.S0 ? sg.S0 + dv : nullptr;
-      float s0v[DK];
-#pragma unroll
-      for (int i = 0; i < DK; ++i)
-        s0v[i] = sg.identity ? (i == dv ? 1.f : 0.f) : (src ? __ldg(src + (size_t)i * DV) : 0.f);
-#pragma unroll
-      for (int c0 = 0; c0 < DK; c0 += 32) {
+    bool s0ok = true;
+    if (s0_bulk) {
+      // S^T <- the initial state from its shared-memory copy (S0 is [dk][dv]: thread dv
+      // reads a column, conflict-free), 32 columns of tensor memory at a time
+      s0ok = wait_bar(&B->s0f, 0, wc);
+#pragma unroll 1
+      for (int q = 0; q < 4; ++q) {
+        const float* src = reinterpret_cast<const float*>(s0_part(q)) + dv;
         float v[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = s0v[c0 + i];
-        tmem_st32(lane_base + TM_S + c0, v);
+        for (int i = 0; i < 32; ++i) v[i] = src[i * DV];
+        tmem_st32(lane_base + TM_S + q * 32, v);
+      }
+      tmem_st_wait();
+      mbar_arrive(&B->s0c);
+    } else {
+      // ... or the identity, or zeros
+#pragma unroll 1
+      for (int q = 0; q < 4; ++q) {
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = sg.identity && q * 32 + i == dv ? 1.f : 0.f;
+        tmem_st32(lane_base + TM_S + q * 32, v);
       }
       tmem_st_wait();
     }
@@ -993,14 +1035,16 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
     int c = 0;
     // ok carries each thread's waits of the chunk before (its S^T update, and this chunk's
     // stage and [U~^T | 0] product) into the barrier that precedes this chunk's first product
-    bool ok = n == 0 || wait_bar2(&B->stl[0], 0, &B->ready[0], 0, wc);
+    bool ok = s0ok && (n == 0 || wait_bar2(&B->stl[0], 0, &B->ready[0], 0, wc));
     for (; c < n; ++c) {
       const int b = c & 1;
       const uint32_t st = K2_ST + (uint32_t)b * STAGE_BYTES;
       const float* vec = reinterpret_cast<const float*>(sm + st + SG_VEC);   // dec[0..63], gamma_L
       tc_fence_after();
-      // E_S: bf16 copy of S^T (the A operand); only this sits before the product
-#pragma unroll
+      // E_S: bf16 copy of S^T (the A operand); only this sits before the product.  (This
+      // loop and the rescale below are not unrolled: the scan's roles share one SM's
+      // instruction caches, and the smaller loop body measured faster.)
+#pragma unroll 1
       for (int half = 0; half < 2; ++half) {
         float x[32], y[32], pk[32];
         tmem_ld32(lane_base + TM_S + half * 64, x);
@@ -1034,7 +1078,7 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
       // S^T update below reads this)
       {
         const float gl = vec[CT];
-#pragma unroll
+#pragma unroll 1
         for (int half = 0; half < 2; ++half) {
           float x[32], y[32];
           tmem_ld32(lane_base + TM_S + half * 64, x);
@@ -1103,6 +1147,7 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
     tc_fence_after();
     if (fail) {
       if (leader) {
+        if (s0_bulk) mbar_wait(&B->s0f, 0, WAIT_LIMIT);       // the state's copies have landed
         if (fg_issued > 0) mbar_wait(&B->fg, (fg_issued - 1) & 1, WAIT_LIMIT);
         if (gh_issued > 0) mbar_wait(&B->gh, (gh_issued - 1) & 1, WAIT_LIMIT);
         if (ob_issued > 0) mbar_wait(&B->ob[(ob_issued - 1) & 1], ((ob_issued - 1) >> 1) & 1, WAIT_LIMIT);
@@ -1126,8 +1171,14 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
     constexpr bool kBf16Out = sizeof(Tout) == 2;
     const bool rows_bf16 = kBf16Out || sg.out_bf16;
     int issued = 0;
-    if (leader && self_load)
-      while (issued < n && issued < 2 && issue_stage(issued)) ++issued;
+    if (leader && self_load && n > 0) {
+      issue_stage(0);
+      issued = 1;
+      if (n > 1 && (!s0_bulk || wait_bar(&B->s0c, 0, wc))) {
+        issue_stage(1);
+        issued = 2;
+      }
+    }
     // Gated RMSNorm in the epilogue (when z is given): y = o / sqrt(mean_dv o^2 + eps) * w * silu(z);
     // the mean over a row is a sum over this warpgroup's 128 lanes.  The z tile of a chunk
     // arrives by TMA in the output buffer its y tile is later written over, one chunk ahead.
