@@ -340,8 +340,11 @@ struct SolveAhead {
   int slot, c0, len;   // its chunk slot and token range (slot -1: not known yet)
 };
 
-__device__ __forceinline__ void st_release(int* f, int v) {
-  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
+// A flag store after solve_item's closing fence: the fence (acq_rel, gpu scope, by the
+// storing thread after a barrier of the whole group) and this strong relaxed store form a
+// release of every tile store of the group (a release store would fence a second time).
+__device__ __forceinline__ void st_flag(int* f, int v) {
+  asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
 }
 
 // Claim the next work item: a relaxed atomic add issued where it stands in the program
@@ -358,7 +361,7 @@ __device__ __forceinline__ int claim_item(int* counter) {
 // parity is ph & 1 (ph advances by three), tbase 128 allocated tensor-memory
 // columns.  The tiles go to workspace tile `tile` (of the item's head) as direct
 // 16-byte stores, once `rel` (if given) reached rel_need; when this returns, thread 0
-// has fenced them for the group after a barrier (its release of a flag publishes them).  `ahead` carries the
+// has fenced them for the group after a barrier (a relaxed flag store of its then publishes them).  `ahead` carries the
 // loads this item issues for the next one (nslot < 0: none): its gate values, in
 // flight under this item's A and P rows, and its Q, K tiles, issued by thread 0 as
 // soon as this item's W product has completed (the last reader of the QK buffer).
@@ -598,7 +601,7 @@ __device__ bool solve_item(uint8_t* sm, int tid, uint32_t barid, uint64_t* bar, 
   tc_fence_before();
   named_sync(barid, 128);
   tc_fence_after();
-  if (tid == 0) __threadfence();
+  if (tid == 0) asm volatile("fence.acq_rel.gpu;" ::: "memory");
   return done;
 }
 
@@ -1499,7 +1502,7 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
         uint32_t ph = 0;
         const bool ok = solve_item(sm, tid, 1, bar, ph, *tslot, &tmq, &tmk, p, c, h, ahead, -1, 0,
                                    (size_t)(role * sp.ring), nullptr, 0);
-        if (tid == 0) st_release(flags + (size_t)c * p.Nv + h, ok ? 1 : -1);
+        if (tid == 0) st_flag(flags + (size_t)c * p.Nv + h, ok ? 1 : -1);
       }
       tc_fence_before();
       __syncthreads();
@@ -1575,7 +1578,7 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
       const bool ok = solve_item(gsm, tid, barid, bar, ph, tbase, &tmq, &tmk, p, c, h, ahead, nc, nh,
                                  (size_t)(seg * sp.ring + cl % sp.ring), rel, seg ? 3 : 2);
       if (tid == 0) {
-        st_release(flags + (size_t)c * p.Nv + h, ok ? 1 : -1);   // tiles visible (see solve_item)
+        st_flag(flags + (size_t)c * p.Nv + h, ok ? 1 : -1);   // tiles visible (see solve_item)
         item_slot[par] = after;
       }
       if (!ok) break;
