@@ -612,7 +612,7 @@ __global__ void __launch_bounds__(128, 3)
 chunk_solve_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                    ChunkArgs p, int nitems, int* counter) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sm = tc::smem_aligned<1024>(smem_raw);
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + S1_BAR);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S1_BAR + 16);
   volatile int* item_slot = reinterpret_cast<volatile int*>(sm + S1_BAR + 32);   // two slots
@@ -1284,7 +1284,6 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
         Tout* yrow = o + ((size_t)(c0 + r) * p.Nv + h) * DV + bx * 64;
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch) {
-          const uint32_t off = rowoff + ((((uint32_t)ch ^ (uint32_t)r) & 7u) << 4);
           const uint32_t xw[4] = {xu[ch].x, xu[ch].y, xu[ch].z, xu[ch].w};
           const uint32_t zw[4] = {zu[ch].x, zu[ch].y, zu[ch].z, zu[ch].w};
           float y[8];
@@ -1390,7 +1389,7 @@ __global__ void __launch_bounds__(NT2, 1)
 chunk_scan_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   const __grid_constant__ CUtensorMap tmo, const __grid_constant__ CUtensorMap tmz, ChunkArgs p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sm = tc::smem_aligned<1024>(smem_raw);
   const int h = blockIdx.x % p.Nv, rank = blockIdx.x / p.Nv;
   volatile int* pick = reinterpret_cast<volatile int*>(sm + K2_BAR + 248);   // before the barriers' set-up
   if (threadIdx.x == 0) *pick = rank;                // (equal lengths: the identity)
@@ -1477,7 +1476,7 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
                    const __grid_constant__ CUtensorMap tmz, const __grid_constant__ CUtensorMap tmr, ChunkArgs p,
                    SplitArgs sp, int nscan, int nitems, int skip, int* flags, int ngroups) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sm = tc::smem_aligned<1024>(smem_raw);
   if ((int)blockIdx.x < nscan) {
     const int role = blockIdx.x / p.Nv, h = blockIdx.x % p.Nv;
     if (skip > 0 && role < 2) {
@@ -1628,7 +1627,7 @@ template <typename Tout>
 __global__ void __launch_bounds__(NT4)
 chunk_fixup_kernel(const __grid_constant__ CUtensorMap tmr, FixArgs f) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sm = tc::smem_aligned<1024>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5;
   const int nout = f.cph * f.Nv;
   if ((int)blockIdx.x >= nout) {

@@ -207,24 +207,32 @@ conv_gating_kernel(ConvGatingArgs p) {
   }
 }
 
-// Tiled variant for bf16 inputs with C a multiple of 1024 and q/k regions of
-// whole 256-channel strips.  A persistent CTA walks tiles of [3 + 16 tokens] x
-// [1024 channels] of mixed_qkv, staged in shared memory by four TMA box loads
-// (the rows before the first token, including negative token indices, arrive
-// as zeros) with the next tile's loads in flight while the current one is
-// computed.  Warp w walks 256-channel strip w % 4 (8 channels per lane,
-// 16-byte reads) down tokens 8 (w / 4) .. + 7 of the tile with a four-row
-// register ring; the loop is unrolled so the ring never moves.  Channel pairs
-// go through the packed fp32x2 FMA (each lane holds an even/odd channel pair
-// as one float2), which rounds each half as the scalar FMA does.  Tokens in
-// the first 3 positions of a sequence are recomputed with their conv state
-// afterwards.  The gates, which depend on the token and head only, are
-// computed after the tile loop by the CTAs that ran one tile fewer.
+// Tiled variant for bf16 inputs with C a multiple of 1024, q/k regions of whole
+// 256-channel strips and Dk 64 or 128.  A persistent CTA walks tiles of [3 + 16
+// tokens] x [1024 channels] of mixed_qkv, staged in shared memory by four TMA box
+// loads (the rows before the first token, including negative token indices,
+// arrive as zeros) together with the block's weights, with the next tile's loads
+// in flight while the current one is computed.  The channel block of a CTA's
+// tiles rotates from round to round, so that the q and k blocks (with their L2
+// norms) are spread over all CTAs.  Warp w walks 256-channel strip w % 4 (8
+// channels per lane, 16-byte reads) down tokens 8 (w / 4) .. + 7 of the tile with
+// a four-row register ring; the loop is unrolled so the ring never moves.
+// Channel pairs go through the packed fp32x2 FMA (each lane holds an even/odd
+// channel pair as one float2), which rounds each half as the scalar FMA does.
+// Tokens in the first 3 positions of a sequence (but for a first sequence without
+// a conv state in, whose zero left context the TMA fill supplies) are recomputed
+// with their conv state afterwards.  The gates, which depend on the token and
+// head only, are computed by all CTAs while their first tile is in flight.
 constexpr int TT = 16;                         // tokens per tile
 constexpr int TROWS = TT + 3;
 constexpr int RPW = TT / 2;                    // tokens per warp
 constexpr uint32_t STRIP_BYTES = TROWS * 512;  // 256 bf16 channels per row
-constexpr uint32_t TILE_BYTES = 4 * STRIP_BYTES;
+constexpr uint32_t W_OFF = 4 * STRIP_BYTES;    // the block's conv weights [1024][4] bf16
+constexpr uint32_t W_BYTES = 1024 * 4 * 2;
+constexpr uint32_t B_OFF = W_OFF + W_BYTES;    // its bias [1024] bf16 (when there is one)
+constexpr uint32_t B_BYTES = 1024 * 2;
+constexpr uint32_t TILE_BYTES = B_OFF + B_BYTES;
+static_assert(W_OFF % 16 == 0 && B_OFF % 16 == 0 && TILE_BYTES % 128 == 0, "bulk copy alignment");
 constexpr uint32_t TILE_SMEM = 2 * TILE_BYTES + 64 + 128;
 
 __device__ __forceinline__ float tanh_approx(float x) {
@@ -238,20 +246,21 @@ __device__ __forceinline__ float tanh_approx(float x) {
 // most about 2^-11 |h|: within half a bf16 ulp of the result for x >= -2; for
 // more negative x silu is near zero and the error, still far below the bf16
 // rounding of O(1) values, is no longer small relative to the result.
-template <typename Tout> __device__ __forceinline__ float silu_out(float x);
-template <> __device__ __forceinline__ float silu_out<bf16>(float x) {
-  const float h = 0.5f * x;
-  return fmaf(h, tanh_approx(h), h);
-}
-template <> __device__ __forceinline__ float silu_out<float>(float x) { return silu_fast(x); }
-template <typename Tout> __device__ __forceinline__ float2 silu_out2(float2 x);
-template <> __device__ __forceinline__ float2 silu_out2<bf16>(float2 x) {
-  const float2 h = __fmul2_rn(x, make_float2(0.5f, 0.5f));
+// For bf16 outputs the tiled kernel computes the halved pre-activation h directly (its
+// weights and bias scaled by 1/2, which is exact), so silu is h + h tanh(h) with no
+// multiply before the tanh; for fp32 outputs the pre-activation is the plain one.
+template <typename Tout> __device__ __forceinline__ float silu_pre(float v);
+template <> __device__ __forceinline__ float silu_pre<bf16>(float h) { return fmaf(h, tanh_approx(h), h); }
+template <> __device__ __forceinline__ float silu_pre<float>(float x) { return silu_fast(x); }
+template <typename Tout> __device__ __forceinline__ float2 silu_pre2(float2 v);
+template <> __device__ __forceinline__ float2 silu_pre2<bf16>(float2 h) {
   return __ffma2_rn(h, make_float2(tanh_approx(h.x), tanh_approx(h.y)), h);
 }
-template <> __device__ __forceinline__ float2 silu_out2<float>(float2 x) {
+template <> __device__ __forceinline__ float2 silu_pre2<float>(float2 x) {
   return make_float2(silu_fast(x.x), silu_fast(x.y));
 }
+template <typename Tout> constexpr float kPreScale = 1.0f;
+template <> constexpr float kPreScale<bf16> = 0.5f;
 
 __device__ __forceinline__ float2 bf2_to_f2(uint32_t w) {
   return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
@@ -268,12 +277,16 @@ template <typename T> __device__ __forceinline__ void store8x2(T* p, const float
   const float f[8] = {y[0].x, y[0].y, y[1].x, y[1].y, y[2].x, y[2].y, y[3].x, y[3].y};
   store8(p, f);
 }
-// L2-normalise (times qs) a head split over `lanes_per_head` lanes of 8 channels
-__device__ __forceinline__ void l2norm8x2(float2 (&y)[4], int lanes_per_head, float eps, float qs) {
+// L2-normalise (times qs) a head split over LPH lanes of 8 channels (a shuffle tree of
+// fixed depth: no loop control between its steps)
+template <int LPH>
+__device__ __forceinline__ void l2norm8x2(float2 (&y)[4], float eps, float qs) {
   float2 ss2 = __fmul2_rn(y[0], y[0]);
 #pragma unroll
   for (int i = 1; i < 4; ++i) ss2 = __ffma2_rn(y[i], y[i], ss2);
-  const float ss = group_sum(ss2.x + ss2.y, lanes_per_head);
+  float ss = ss2.x + ss2.y;
+#pragma unroll
+  for (int off = LPH / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
   const float inv = rsqrtf(ss + eps) * qs;
 #pragma unroll
   for (int i = 0; i < 4; ++i) y[i] = __fmul2_rn(y[i], make_float2(inv, inv));
@@ -301,25 +314,34 @@ __device__ __forceinline__ void gates_range(const ConvGatingArgs& p, int64_t fir
   }
 }
 
-template <typename Tout>
+// LPH: lanes per q/k head (Dk / 8); BIAS: whether the conv has a bias.
+template <typename Tout, int LPH, bool BIAS>
 __global__ void __launch_bounds__(256, 2)
 conv_gating_tile_kernel(const __grid_constant__ CUtensorMap tmx, ConvGatingArgs p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  uint8_t* sm = tc::smem_aligned<128>(smem_raw);
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + 2 * TILE_BYTES);   // one per buffer
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int sid = warp & 3, half = warp >> 2;
   const int nct = p.C / 1024;
   const int ntiles = ((p.total + TT - 1) / TT) * nct;
   const int kd = p.Nk * p.Dk;
-  const int lanes_per_head = p.Dk / 8;
   const bf16* st_in = static_cast<const bf16*>(p.state_in);
-  const bf16* xg = static_cast<const bf16*>(p.x);
+  // Tile L covers tokens TT (L / nct) .. and channel block (L + L / nct) % nct: over the
+  // rounds of a persistent CTA (L advancing by the grid size) the block rotates, so that
+  // the q and k blocks (with their L2 norms) are spread over all CTAs.
+  auto tile_ct = [&](int tile) { return (tile + tile / nct) % nct; };
   auto issue = [&](int tile, int buf) {
-    const int t0 = (tile / nct) * TT, ct = tile % nct;
-    tc::mbar_arrive_expect_tx(&bar[buf], TILE_BYTES);
+    const int t0 = (tile / nct) * TT, ct = tile_ct(tile);
+    tc::mbar_arrive_expect_tx(&bar[buf], W_OFF + W_BYTES + (BIAS ? B_BYTES : 0));
     for (int i = 0; i < 4; ++i)
       tc::tma_load_2d(sm + buf * TILE_BYTES + i * STRIP_BYTES, &tmx, &bar[buf], ct * 1024 + i * 256, t0 - 3);
+    // the block's weights (and bias) come with its rows: the block changes from tile to tile
+    tc::bulk_load(sm + buf * TILE_BYTES + W_OFF, static_cast<const uint8_t*>(p.w) + (size_t)ct * W_BYTES, W_BYTES,
+                  &bar[buf]);
+    if (BIAS)
+      tc::bulk_load(sm + buf * TILE_BYTES + B_OFF, static_cast<const uint8_t*>(p.bias) + (size_t)ct * B_BYTES,
+                    B_BYTES, &bar[buf]);
   };
   if (threadIdx.x == 0) {
     tc::mbar_init(&bar[0], 1);
@@ -342,37 +364,21 @@ conv_gating_tile_kernel(const __grid_constant__ CUtensorMap tmx, ConvGatingArgs 
       }
     }
   }
+  // The gates, which depend on the token and head only, while the first tile is in flight
+  // (their loads are small beside it)
+  gates_range(p, (int64_t)blockIdx.x * blockDim.x + threadIdx.x, (int64_t)gridDim.x * blockDim.x);
   __syncthreads();
   float2 wt[4][4], bias[4];                          // [channel pair][tap]
-  int wct = -1;                                      // channel block the weights belong to
   int k = 0;
   for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k) {
     const int buf = k & 1;
-    const int tt = tile / nct, ct = tile % nct;
+    const int tt = tile / nct, ct = tile_ct(tile);
     const int t0 = tt * TT, t_end = min(t0 + TT, p.total);
     // the other buffer was released by the barrier that ended the previous tile
     if (threadIdx.x == 0 && tile + (int)gridDim.x < ntiles) issue(tile + gridDim.x, buf ^ 1);
     const int strip0 = ct * 1024 + sid * 256;         // first channel of the warp's strip
     const int c0 = strip0 + lane * 8;
     const int region = strip0 < kd ? 0 : (strip0 < 2 * kd ? 1 : 2);
-    if (ct != wct) {
-      wct = ct;
-      float w8[8][4], b8[8];
-#pragma unroll
-      for (int c = 0; c < 8; ++c) load4(static_cast<const bf16*>(p.w) + (size_t)(c0 + c) * 4, w8[c]);
-      if (p.bias) {
-        load8(static_cast<const bf16*>(p.bias) + c0, b8);
-      } else {
-#pragma unroll
-        for (int c = 0; c < 8; ++c) b8[c] = 0.f;
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        bias[q] = make_float2(b8[2 * q], b8[2 * q + 1]);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) wt[q][j] = make_float2(w8[2 * q][j], w8[2 * q + 1][j]);
-      }
-    }
     const bool ok = tc::mbar_wait(&bar[buf], (uint32_t)(k >> 1) & 1u, 1u << 24);
     if (!__syncthreads_and(ok ? 1 : 0)) {
       if (threadIdx.x == 0) {
@@ -382,6 +388,27 @@ conv_gating_tile_kernel(const __grid_constant__ CUtensorMap tmx, ConvGatingArgs 
         if (tile + (int)gridDim.x < ntiles) tc::mbar_wait(&bar[buf ^ 1], (uint32_t)((k + 1) >> 1) & 1u, 1u << 24);
       }
       return;
+    }
+    {   // this lane's 8 channels: weights [channel][tap] (64 contiguous bytes) and bias
+      const uint8_t* wsm = sm + buf * TILE_BYTES + W_OFF + (uint32_t)(sid * 256 + lane * 8) * 8u;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {             // 16 bytes: channels 2q, 2q + 1, four taps each
+        const uint4 u = *reinterpret_cast<const uint4*>(wsm + 16 * q);
+        const float2 e01 = bf2_to_f2(u.x), e23 = bf2_to_f2(u.y), o01 = bf2_to_f2(u.z), o23 = bf2_to_f2(u.w);
+        const float2 k2 = make_float2(kPreScale<Tout>, kPreScale<Tout>);
+        wt[q][0] = __fmul2_rn(make_float2(e01.x, o01.x), k2);
+        wt[q][1] = __fmul2_rn(make_float2(e01.y, o01.y), k2);
+        wt[q][2] = __fmul2_rn(make_float2(e23.x, o23.x), k2);
+        wt[q][3] = __fmul2_rn(make_float2(e23.y, o23.y), k2);
+      }
+      if (BIAS) {
+        lds8x2(sm + buf * TILE_BYTES + B_OFF + (uint32_t)(sid * 256 + lane * 8) * 2u, bias);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) bias[q] = __fmul2_rn(bias[q], make_float2(kPreScale<Tout>, kPreScale<Tout>));
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) bias[q] = make_float2(0.f, 0.f);
+      }
     }
     Tout* dst;
     size_t row_stride;
@@ -400,40 +427,67 @@ conv_gating_tile_kernel(const __grid_constant__ CUtensorMap tmx, ConvGatingArgs 
     float2 ring[4][4];
 #pragma unroll
     for (int j = 0; j < 3; ++j) lds8x2(rows + j * 512, ring[j]);
-#pragma unroll
-    for (int r = 0; r < RPW; ++r) {
+    // one output row (the ring index is static once the loop is unrolled)
+    auto row_out = [&](int r, Tout* d) {
       float2(&cur)[4] = ring[(r + 3) & 3];
       lds8x2(rows + (r + 3) * 512, cur);
-      if (t0 + r0 + r < t_end) {
-        const float2(&x0)[4] = ring[r & 3];
-        const float2(&x1)[4] = ring[(r + 1) & 3];
-        const float2(&x2)[4] = ring[(r + 2) & 3];
-        float2 y[4];
+      const float2(&x0)[4] = ring[r & 3];
+      const float2(&x1)[4] = ring[(r + 1) & 3];
+      const float2(&x2)[4] = ring[(r + 2) & 3];
+      float2 y[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          float2 acc = __ffma2_rn(wt[q][0], x0[q], bias[q]);
-          acc = __ffma2_rn(wt[q][1], x1[q], acc);
-          acc = __ffma2_rn(wt[q][2], x2[q], acc);
-          y[q] = silu_out2<Tout>(__ffma2_rn(wt[q][3], cur[q], acc));
-        }
-        if (region < 2) l2norm8x2(y, lanes_per_head, p.l2_eps, qs);
-        store8x2(dst, y);
+      for (int q = 0; q < 4; ++q) {
+        float2 acc = BIAS ? __ffma2_rn(wt[q][0], x0[q], bias[q]) : __fmul2_rn(wt[q][0], x0[q]);
+        acc = __ffma2_rn(wt[q][1], x1[q], acc);
+        acc = __ffma2_rn(wt[q][2], x2[q], acc);
+        y[q] = silu_pre2<Tout>(__ffma2_rn(wt[q][3], cur[q], acc));
       }
-      dst += row_stride;
+      if (region < 2) l2norm8x2<LPH>(y, p.l2_eps, qs);
+      store8x2(d, y);
+    };
+    if (t_end - (t0 + r0) >= RPW) {          // every row of this warp is a token
+#pragma unroll
+      for (int r = 0; r < RPW; ++r) row_out(r, dst + (size_t)r * row_stride);
+    } else {
+#pragma unroll
+      for (int r = 0; r < RPW; ++r) {
+        if (t0 + r0 + r < t_end) {
+          row_out(r, dst + (size_t)r * row_stride);
+        } else {                             // (keeps the ring in step)
+          lds8x2(rows + (r + 3) * 512, ring[(r + 3) & 3]);
+        }
+      }
     }
     // tokens of this warp in the first 3 positions of a sequence: redo with the conv state
-    // (a single sequence starts at token 0 only)
+    // (zeros without one) in place of the previous sequence's rows; the x rows of the
+    // sequence itself are staged in the tile (row t - t0 + 3 holds token t).  A sequence
+    // that starts at token 0 with no state in needs nothing: the rows before token 0 were
+    // staged as zeros.
     const int ta = t0 + r0, tb = min(t0 + r0 + RPW, t_end);
-    if (p.num_seqs > 1 || ta < 3) {
+    if (p.num_seqs > 1 || (ta < 3 && st_in != nullptr)) {
+      const uint8_t* srow0 = sm + buf * TILE_BYTES + sid * STRIP_BYTES + lane * 16;
+      auto lds8f = [&](int row, float (&f)[8]) {
+        float2 pr[4];
+        lds8x2(srow0 + row * 512, pr);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          f[2 * i] = pr[i].x;
+          f[2 * i + 1] = pr[i].y;
+        }
+      };
       const int seq0 = find_seq(p.cu, p.num_seqs, p.total, max(ta - 3, 0));
       for (int sq = seq0; sq < p.num_seqs; ++sq) {
-        const int st = seq_start(p.cu, p.num_seqs, p.total, sq);
+        int st, en;
+        if (!seq_bounds(p.cu, p.num_seqs, p.total, sq, st, en)) {
+          if (lane == 0) raise_error(p.err, kDevErrSeqlens);
+          break;
+        }
         if (st >= tb) break;
-        for (int t = max(st, ta); t < min(st + 3, tb); ++t) {
-          const int seq = find_seq(p.cu, p.num_seqs, p.total, t);
-          const int pos = t - seq_start(p.cu, p.num_seqs, p.total, seq);
+        if (st == 0 && st_in == nullptr) continue;
+        for (int t = max(st, ta); t < min(min(st + 3, en), tb); ++t) {     // tokens of sequence sq only
+          const int pos = t - st;
           float cur[8], y8[8];
-          load8(xg + (size_t)t * p.C + c0, cur);
+          lds8f(t - t0 + 3, cur);
 #pragma unroll
           for (int c = 0; c < 8; ++c)
             y8[c] = fmaf((c & 1) ? wt[c >> 1][3].y : wt[c >> 1][3].x, cur[c], (c & 1) ? bias[c >> 1].y : bias[c >> 1].x);
@@ -444,17 +498,17 @@ conv_gating_tile_kernel(const __grid_constant__ CUtensorMap tmx, ConvGatingArgs 
             if (si < 3) {
 #pragma unroll
               for (int c = 0; c < 8; ++c)
-                xv[c] = (st_in != nullptr && si >= 0) ? __bfloat162float(st_in[((size_t)seq * p.C + c0 + c) * 3 + si]) : 0.f;
+                xv[c] = st_in != nullptr ? __bfloat162float(st_in[((size_t)sq * p.C + c0 + c) * 3 + si]) : 0.f;
             } else {
-              load8(xg + (size_t)(t - 3 + j) * p.C + c0, xv);
+              lds8f(t - t0 + j, xv);
             }
 #pragma unroll
             for (int c = 0; c < 8; ++c) y8[c] = fmaf((c & 1) ? wt[c >> 1][j].y : wt[c >> 1][j].x, xv[c], y8[c]);
           }
           float2 y[4];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) y[q] = make_float2(silu_out<Tout>(y8[2 * q]), silu_out<Tout>(y8[2 * q + 1]));
-          if (region < 2) l2norm8x2(y, lanes_per_head, p.l2_eps, qs);
+          for (int q = 0; q < 4; ++q) y[q] = make_float2(silu_pre<Tout>(y8[2 * q]), silu_pre<Tout>(y8[2 * q + 1]));
+          if (region < 2) l2norm8x2<LPH>(y, p.l2_eps, qs);
           store8x2(dst0 + (size_t)t * row_stride, y);
         }
       }
@@ -483,14 +537,6 @@ conv_gating_tile_kernel(const __grid_constant__ CUtensorMap tmx, ConvGatingArgs 
       }
     }
     __syncthreads();     // the tile is read; the next TMA may overwrite it
-  }
-  // The gates, which depend on the token and head only, are left to the CTAs that ran one
-  // tile fewer (they would idle while the others finish), or to all CTAs when the tiles
-  // divide evenly.
-  const int fewer_from = ntiles % (int)gridDim.x;
-  if ((int)blockIdx.x >= fewer_from) {
-    const int64_t nctas = (int64_t)gridDim.x - fewer_from;
-    gates_range(p, ((int64_t)blockIdx.x - fewer_from) * blockDim.x + threadIdx.x, nctas * blockDim.x);
   }
 }
 
@@ -529,16 +575,19 @@ template <typename Tin, typename Tout>
 cudaError_t launch_typed(const ConvGatingArgs& p, cudaStream_t s) {
   bool tiled = false;
   const int kd = p.Nk * p.Dk;
-  if (std::is_same<Tin, bf16>::value && p.C % 1024 == 0 && kd % 256 == 0 && p.total > 0) {
+  if (std::is_same<Tin, bf16>::value && p.C % 1024 == 0 && kd % 256 == 0 && p.total > 0 &&
+      (p.Dk == 64 || p.Dk == 128)) {
     CUtensorMap m;
     if (make_tmap_2d(&m, p.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.total, p.C, 256, TROWS,
                      CU_TENSOR_MAP_SWIZZLE_NONE)) {
-      cudaError_t e = cudaFuncSetAttribute(conv_gating_tile_kernel<Tout>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TILE_SMEM);
+      const bool bias = p.bias != nullptr;
+      auto fn = p.Dk == 128 ? (bias ? conv_gating_tile_kernel<Tout, 16, true> : conv_gating_tile_kernel<Tout, 16, false>)
+                            : (bias ? conv_gating_tile_kernel<Tout, 8, true> : conv_gating_tile_kernel<Tout, 8, false>);
+      cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TILE_SMEM);
       if (e != cudaSuccess) return e;
       const int ntiles = ((p.total + TT - 1) / TT) * (p.C / 1024);
       const int blocks = std::min(ntiles, num_sms() * 2);
-      conv_gating_tile_kernel<Tout><<<blocks, 256, TILE_SMEM, s>>>(m, p);
+      fn<<<blocks, 256, TILE_SMEM, s>>>(m, p);
       e = cudaGetLastError();
       if (e != cudaSuccess) return e;
       tiled = true;

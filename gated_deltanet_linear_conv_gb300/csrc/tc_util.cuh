@@ -23,6 +23,14 @@ namespace tc {
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
+// The dynamic shared-memory array advanced to the next multiple of ALIGN bytes, by an
+// offset into the array: the pointer keeps its shared-memory provenance (a round trip
+// through an integer would not), so accesses through it compile to shared loads and
+// stores that the compiler knows cannot alias global memory.
+template <uint32_t ALIGN>
+__device__ __forceinline__ uint8_t* smem_aligned(uint8_t* raw) {
+  return raw + ((ALIGN - (smem_u32(raw) & (ALIGN - 1u))) & (ALIGN - 1u));
+}
 
 // Byte offset of element (row, e) (e < 64 two-byte elements) inside a
 // 128-byte-swizzled region whose rows are 128 bytes apart.
