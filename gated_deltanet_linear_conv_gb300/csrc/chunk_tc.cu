@@ -1422,9 +1422,9 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
 // three independent 128-thread solve groups (own shared memory slice, 128
 // tensor-memory columns, named barrier) that claim (chunk slot, value head)
 // items in chunk order and publish a ready flag per item.  Groups on one SM
-// slow each other down (an item takes about 1.7x as long with three as with
+// slow each other down (an item takes about 2.5x as long with three as with
 // one), so `ngroups` of them claim items: enough for the solve to stay ahead
-// of the scans, and no more, which shortens the wait for the first chunk.  A scan CTA awaits a chunk's
+// of the scans, and no more.  A scan CTA awaits a chunk's
 // flag before loading its tiles, so the solve of later chunks overlaps the
 // scan of earlier ones.  All CTAs are resident at once (cooperative launch
 // with one CTA per SM), so these waits always end; each is bounded anyway.
@@ -1558,16 +1558,24 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
   if (g < ngroups) {
     // Items are claimed two ahead: the next item's gate values and tiles load under the
     // current one, and the claim of the one after (a global atomic) is in flight meanwhile.
+    // The first two items of every group are fixed: group i (numbered group-major over the
+    // CTAs, so that consecutive items go to different SMs) takes items i and G + i, G the
+    // number of groups; the counter hands out the items after 2G.  (With two atomic claims
+    // per group at the start, an item of an early chunk could become some group's second
+    // item and wait for its first.)
+    const int nsolve = (int)gridDim.x - nscan;
+    const int G = ngroups * nsolve;
     if (tid == 0) {
-      item_slot[0] = atomicAdd(counter, 1);
-      item_slot[1] = atomicAdd(counter, 1);
+      const int gi = g * nsolve + ((int)blockIdx.x - nscan);
+      item_slot[0] = gi;
+      item_slot[1] = G + gi;
     }
     named_sync(barid, 128);
     int item = item_slot[0], next = item_slot[1];
     SolveAhead ahead{false, false, 0.f, -1, 0, 0};
     int par = 0;
     while (item < nitems) {
-      const int after = tid == 0 && next < nitems ? claim_item(counter) : nitems;   // read after the item
+      const int after = tid == 0 && next < nitems ? 2 * G + claim_item(counter) : nitems;   // read after the item
       int c, h, nc = -1, nh = 0;
       item_chunk(sp, p.Nv, item + skip, c, h);
       if (next < nitems) item_chunk(sp, p.Nv, next + skip, nc, nh);
@@ -1954,12 +1962,14 @@ cudaError_t launch_chunk_tc(const ChunkArgs& args, cudaStream_t s) {
     }
     int nscan = sp.nseg == 2 ? 3 * p.Nv : p.Nv;
     ChunkArgs pc = p;
-    // Solve groups per CTA: the scans take Nv items per period (about 1.5 us); one group
-    // per SM delivers an item per about 6 us, three groups one per about 12 us each.  Take
-    // one group where the solve SMs outnumber the scans' demand that much, else three (clock
-    // stamps at 32 heads on 152 SMs: with two groups the scans waited on the solve).
+    // Solve groups per CTA: the scans take Nv items per period (about 1.6 us); one group
+    // per SM delivers an item per about 6.5 us, two groups one per about 11 us each, three
+    // one per about 16 us each.  Take one group where the solve SMs outnumber the scans'
+    // demand that much, else two (at 32 heads on 152 SMs two measured 1-2 % faster than
+    // three on long sequences, the same at 4096 tokens: the third group adds little
+    // throughput and every item's latency grows).
     const double per_scan = (double)(sms - nscan) / (double)(sp.nseg * p.Nv);
-    int ngroups = per_scan >= 5.3 ? 1 : 3;
+    int ngroups = per_scan >= 5.3 ? 1 : 2;
     if (p.no_solve) ngroups = 0;           // test hook: no flag is ever published
     // the scan CTAs of the first and of the second segment solve their first chunk themselves
     int skip = p.no_solve ? 0 : sp.nseg * p.Nv;
