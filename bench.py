@@ -17,7 +17,7 @@ the public API with the inputs copied in from pinned host memory and y read back
 every step; the copies of step i+1 run on a copy stream under step i's compute
 (two device buffer sets), as a pipelined caller would run them.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-cpu-baseline] [--headline-only]
 
 --impl reference times the fp64 CPU oracle (the reference arm of this
 project) on a bounded sample of the same workload.  Under torchrun (N > 1)
@@ -547,7 +547,7 @@ def run_ours(args):
     torch.cuda.empty_cache()
     extra = {}
     extra_launches = 0
-    for key, name in (('varlen', 'varlen_16seq'), ('long_context', 'prefill_t131072')):
+    for key, name in (() if args.headline_only else (('varlen', 'varlen_16seq'), ('long_context', 'prefill_t131072'))):
         res, winp, nl = time_prefill_workload(name, args.steps, args.warmup, barrier, max_over_ranks, tc_peak)
         res['tokens_per_s'] = whole_job_rate(res['tokens'], ws, res['us_per_step'] * 1e-3)
         extra[key] = (res, winp)
@@ -634,6 +634,9 @@ def main():
     ap.add_argument('--warmup', type=int, default=5)
     ap.add_argument('--impl', default='ours', choices=['ours', 'reference'])
     ap.add_argument('--no-cpu-baseline', action='store_true')
+    ap.add_argument('--headline-only', action='store_true',
+                    help='time only prefill_t4096 and decode_b256 (no varlen / long-context lines): '
+                         'a small device footprint for profiler captures')
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == 'ours':
         print('note: warmup raised to 3', file=sys.stderr)
