@@ -701,6 +701,7 @@ struct ScanBars {
   uint64_t s0c;      // the state role has moved it into tensor memory (128 arrivals)
   uint32_t tslot;
   int abort;
+  int odone;         // side norm: chunks whose o stores have landed (the output role counts)
 };
 static_assert(sizeof(ScanBars) <= 256, "scan barriers fit their slot");
 
@@ -801,8 +802,72 @@ struct ScanSeg {
   bool release;              // add one to a chunk's flag once its tiles are no longer needed
 };
 
-// The scan of one (sequence s, value head h) by the CTA's warps 0-8 (more
-// warps may be present; they only join the final barrier).  sm is 1024-aligned
+__device__ __forceinline__ void unpack8(const uint4 (&u)[1], float (&f)[8]) {   // 8 bf16
+  const uint32_t w[4] = {u[0].x, u[0].y, u[0].z, u[0].w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+    f[2 * i] = a.x;
+    f[2 * i + 1] = a.y;
+  }
+}
+__device__ __forceinline__ void unpack8(const uint4 (&u)[2], float (&f)[8]) {   // 8 fp32
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    f[4 * j] = __uint_as_float(u[j].x);
+    f[4 * j + 1] = __uint_as_float(u[j].y);
+    f[4 * j + 2] = __uint_as_float(u[j].z);
+    f[4 * j + 3] = __uint_as_float(u[j].w);
+  }
+}
+
+// The gated RMSNorm of rows c0 .. c0 + len - 1 (len <= NB * NT / 16) of value head h, in
+// place: y = o / sqrt(mean_dv o^2 + eps) * w * silu(z), o being the stored output row.  NT
+// threads: thread (r, l) = (tid / 16, tid % 16) takes elements 8l .. 8l + 7 of rows
+// r, r + NT/16, ...; every load is issued before the first use (one round trip; o is read
+// from L2, where the scan's stores landed), and a row's sum of squares is a shuffle over
+// its 16 lanes (one half-warp).
+template <typename Tout, int NT, int NB>
+__device__ __forceinline__ void norm_rows(const ChunkArgs& p, int c0, int len, int h, int tid, const float (&w)[8]) {
+  constexpr int NR = sizeof(Tout) == 2 ? 1 : 2;      // 16-byte pieces of 8 output elements
+  constexpr int RS = NT / 16;                         // rows per step
+  const int l = tid & 15, r0 = tid >> 4;
+  const unsigned half = (tid & 16) ? 0xffff0000u : 0x0000ffffu;
+  uint4 ou[NB][NR], zu[NB];
+#pragma unroll
+  for (int i = 0; i < NB; ++i) {
+    if (r0 + RS * i < len) {
+      const size_t off = ((size_t)(c0 + r0 + RS * i) * p.Nv + h) * DV + 8 * l;
+      const uint4* op = reinterpret_cast<const uint4*>(static_cast<const Tout*>(p.o) + off);
+#pragma unroll
+      for (int j = 0; j < NR; ++j) ou[i][j] = __ldcg(op + j);
+      zu[i] = __ldg(reinterpret_cast<const uint4*>(static_cast<const bf16*>(p.z) + off));
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < NB; ++i) {
+    if (r0 + RS * i < len) {                           // (the same for the 16 lanes of a row)
+      float x[8], z[8];
+      unpack8(ou[i], x);
+      const uint4 zz[1] = {zu[i]};
+      unpack8(zz, z);
+      float ss = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+#pragma unroll
+      for (int m = 8; m > 0; m >>= 1) ss += __shfl_xor_sync(half, ss, m);
+      const float inv = rsqrtf(ss * (1.0f / DV) + p.norm_eps);
+      float y[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) y[e] = x[e] * inv * w[e] * silu_out<Tout>(z[e]);
+      store8(static_cast<Tout*>(p.o) + ((size_t)(c0 + r0 + RS * i) * p.Nv + h) * DV + 8 * l, y);
+    }
+  }
+}
+
+// The scan of one (sequence s, value head h) by the CTA's warps 0-9 (with the side
+// norm of the one-sequence launch, warp 10 publishes the output blocks; other warps
+// only join the final barrier).  sm is 1024-aligned
 // shared memory of K2 bytes.  With `flags`, every chunk's workspace tiles are
 // awaited before they are loaded (the solve runs concurrently in other CTAs).
 template <typename Tout, bool NORM>
@@ -853,6 +918,7 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
     mbar_init(&B->s0f, 1);
     mbar_init(&B->s0c, 128);
     B->abort = 0;
+    B->odone = 0;
     fence_barrier_init();
     prefetch_tmap(tmk);
     prefetch_tmap(tmv);
@@ -1167,6 +1233,32 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
         for (int i = 0; i < 32; ++i) dst[(size_t)(c0 + i) * DV] = v[i];
       }
     }
+  } else if (warp == 10 && p.side_norm && flags != nullptr) {
+    // ============================== PUBLISHER ==============================
+    // Side norm: publish each chunk's o block (a flag per (chunk, head)) once the output role
+    // counts its stores as landed.  The gpu-scope fence this needs costs the thread that runs
+    // it a memory round trip; here it holds up no other role (on the output role it cost the
+    // chain about 30 us per 4096 tokens).  One fence covers every block counted since the last.
+    if (lane == 0) {
+      int* oflags = flags_rw + (size_t)((p.total + CT - 1) / CT) * p.Nv + 2;
+      uint64_t t0 = global_ns();                 // time of the last progress
+      int done = 0;
+      for (uint32_t i = 0; done < n && i < POLL_CAP; ++i) {
+        int avail;
+        asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(avail) : "r"(smem_u32(&B->odone)) : "memory");
+        if (avail > done) {
+          fence_proxy_async_global();
+          asm volatile("fence.acq_rel.gpu;" ::: "memory");
+          for (; done < avail; ++done) st_flag(oflags + (size_t)(slot0 + done) * p.Nv + h, 1);
+          t0 = global_ns();
+          continue;
+        }
+        // no progress within the wait bound: the scan failed (its own waits report it) or
+        // stalled; the norm groups' bounded waits then end the call
+        if (*abort || global_ns() - t0 > wc.limit_ns) break;
+        __nanosleep(200);
+      }
+    }
   } else if (warp <= 8) {
     // ============================== OUT ==============================
     const bool leader = tid == 160;
@@ -1205,6 +1297,18 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
       named_sync(3, 128);
     }
     const int ot = tid - 160;                     // thread within OUT
+    // Side norm (one-sequence launch with z): each chunk's o block is published with a flag
+    // once its stores have landed -- a TMA-stored chunk when the next chunk's store has been
+    // issued (one store group may stay in flight), a chunk of plain stores at once -- so that
+    // spare solve groups can normalise it in place.
+    const bool pub_o = p.side_norm && flags != nullptr;
+    auto count_done = [&](int v) {               // (release at CTA scope: the publisher reads it)
+      asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&B->odone)), "r"(v) : "memory");
+    };
+    // The TMA stores of o (and every wait on them) belong to a thread of another warp than
+    // the leader, which issues the O products: a leader waiting on a store would hold back
+    // the next O product, and with it the next chunk's E_U.
+    const bool storer = tid == 192;
     for (; c < n; ++c) {
       const int b = c & 1;
       const int c0 = bos + c * CT, len = min(CT, eos - c0);
@@ -1229,7 +1333,7 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
       float v[64];
       tm_ld64(lane_base + TM_ACC + b * 128 + 64, v);   // lane dv holds O[0..63][dv]
       const bool use_tma = rows_bf16 && len == CT;
-      if (leader) {
+      if (storer) {
         // the stores that read the buffers have left them (with the norm, the other
         // buffer holds this chunk's o rows next)
         if (!norm && use_tma) bulk_wait_read<1>();
@@ -1326,7 +1430,7 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
         }
         fence_proxy_async_smem();
         named_sync(3, 128);
-        if (leader) {
+        if (storer) {
           tma_store_2d(tmo, os, h * DV, c0 - sg.row_off);
           tma_store_2d(tmo, os + 8192, h * DV + 64, c0 - sg.row_off);
           bulk_commit_group();
@@ -1338,20 +1442,40 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
           for (int r = 0; r < CT; ++r)
             if (r < len) dst[(size_t)r * p.Nv * DV] = __float2bfloat16_rn(p.scale * v[r]);
         } else {
+          // (for the side norm, o is normalised as a bf16 o would be stored, whatever the
+          // output type: fp32 rows carry bf16-rounded values)
           Tout* dst = o + ((size_t)(c0 - sg.row_off) * p.Nv + h) * DV + dv;
 #pragma unroll
-          for (int r = 0; r < CT; ++r)
-            if (r < len) dst[(size_t)r * p.Nv * DV] = from_f32<Tout>(p.scale * v[r]);
+          for (int r = 0; r < CT; ++r) {
+            const float x = p.scale * v[r];
+            if (r < len) dst[(size_t)r * p.Nv * DV] = from_f32<Tout>(pub_o ? __bfloat162float(__float2bfloat16_rn(x)) : x);
+          }
+        }
+      }
+      if (pub_o) {
+        if (use_tma) {
+          // chunks up to c - 1 have landed once at most this chunk's store group is pending
+          if (storer && c >= 1) {
+            bulk_wait_group<1>();
+            count_done(c);
+          }
+        } else {
+          named_sync(3, 128);                      // every OUT thread's plain stores are issued
+          if (storer) {
+            bulk_wait_all();
+            count_done(c + 1);
+          }
         }
       }
     }
-    if (leader) {
-      if (fail) {
-        for (int k = c; k < issued; ++k) mbar_wait(&B->stl[k & 1], (k >> 1) & 1, WAIT_LIMIT);
-        for (int k = c; k < zissued; ++k) mbar_wait(&B->zb[k & 1], (k >> 1) & 1, WAIT_LIMIT);
-        if (g2_issued > 0) mbar_wait(&B->ob[(g2_issued - 1) & 1], ((g2_issued - 1) >> 1) & 1, WAIT_LIMIT);
-      }
+    if (storer) {
       bulk_wait_all();
+      if (pub_o && !fail) count_done(n);
+    }
+    if (leader && fail) {
+      for (int k = c; k < issued; ++k) mbar_wait(&B->stl[k & 1], (k >> 1) & 1, WAIT_LIMIT);
+      for (int k = c; k < zissued; ++k) mbar_wait(&B->zb[k & 1], (k >> 1) & 1, WAIT_LIMIT);
+      if (g2_issued > 0) mbar_wait(&B->ob[(g2_issued - 1) & 1], ((g2_issued - 1) >> 1) & 1, WAIT_LIMIT);
     }
   }
 
@@ -1553,6 +1677,7 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
   tc_fence_after();
   const uint32_t tbase = *tslot + 128u * (uint32_t)g;
   int* counter = flags + nitems;
+  const int ntotal = nitems;             // (chunk, value head) items of the call
   nitems -= skip;                        // items claimed here: those after the self-solved chunks
   uint32_t ph = 0;
   if (g < ngroups) {
@@ -1593,6 +1718,32 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
       item = next;
       next = item_slot[par];
       par ^= 1;
+    }
+  } else if (p.side_norm && g == 2) {
+    // The side norm: the third group of every solve CTA applies the gated RMSNorm to the
+    // output blocks in chunk order, each once the scan has published it (its o rows sit in
+    // the output buffer), claiming blocks from a counter of their own.  A block that is not
+    // published within the wait bound (a failed scan) ends the group with the device error.
+    int* ncount = flags + ntotal + 1;
+    const int* oflags = flags + ntotal + 2;
+    float w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = p.norm_w[8 * (tid & 15) + i];
+    for (;;) {
+      if (tid == 0) {
+        int it = atomicAdd(ncount, 1);
+        if (it < ntotal && !wait_count(oflags + it, 1, p.wait_ns)) {
+          raise_error(p.err, kDevErrTimeout);
+          it = -1;
+        }
+        item_slot[0] = it;
+      }
+      named_sync(barid, 128);
+      const int it = item_slot[0];
+      named_sync(barid, 128);              // (the slot is written again next round)
+      if (it < 0 || it >= ntotal) break;
+      const int c0 = (it / p.Nv) * CT;
+      norm_rows<Tout, 128, 8>(p, c0, min(CT, p.total - c0), it % p.Nv, tid, w);
     }
   }
   tc_fence_before();
@@ -1886,7 +2037,9 @@ ChunkPlan plan_chunk(int num_seqs, int total, int Nv, bool fused, bool split_ok)
     L.m = L.nseg == 2 ? (L.n + 1) / 2 : L.n;
     L.ring = std::max(1, std::min(kRing, L.m));          // the first segment is the longer one
     L.tiles = (size_t)L.nseg * L.ring * Nv;
-    L.nflags = (size_t)L.n * Nv + 1;
+    // per (chunk, head): the ready / release count; the item counter; the side norm's block
+    // counter; per (chunk, head): the side norm's o-ready flag
+    L.nflags = 2 * (size_t)L.n * Nv + 2;
   } else {
     L.nseg = 1;
     L.m = L.n;
@@ -1962,6 +2115,9 @@ cudaError_t launch_chunk_tc(const ChunkArgs& args, cudaStream_t s) {
     }
     int nscan = sp.nseg == 2 ? 3 * p.Nv : p.Nv;
     ChunkArgs pc = p;
+    // With z, the scan stores o and the third group of every solve CTA applies the norm to
+    // each published block in place (the norm in the scan's epilogue would pace the chain)
+    pc.side_norm = p.z != nullptr ? 1 : 0;
     // Solve groups per CTA: the scans take Nv items per period (about 1.6 us); one group
     // per SM delivers an item per about 6.5 us, two groups one per about 11 us each, three
     // one per about 16 us each.  Take one group where the solve SMs outnumber the scans'
@@ -1974,7 +2130,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs& args, cudaStream_t s) {
     // the scan CTAs of the first and of the second segment solve their first chunk themselves
     int skip = p.no_solve ? 0 : sp.nseg * p.Nv;
     void* args[] = {&mq, &mk, &mv, &mo, &mz, &mr, &pc, &sp, &nscan, &nitems, &skip, &flags, &ngroups};
-    const void* fn = fused_kernels()[(p.out_bf16 ? 0 : 2) + (p.z != nullptr ? 1 : 0)];
+    const void* fn = fused_kernels()[p.out_bf16 ? 0 : 2];
     e = cudaLaunchCooperativeKernel(fn, dim3(sms), dim3(NT3), args, K3_SMEM, s);
     if (e != cudaSuccess || sp.nseg == 1) return e;
     // the second segment's outputs and the final state from S_mid

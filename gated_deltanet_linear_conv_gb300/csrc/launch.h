@@ -89,6 +89,9 @@ struct ChunkArgs {
   unsigned long long wait_ns;
   int no_solve;                                  // test hook: the one-sequence launch runs no solve
   int no_split;                                  // never split a long sequence (smaller workspace)
+  // one-sequence launch with z: the scan writes o into o's buffer and spare solve groups apply
+  // the gated norm in place, block by block (set by the launcher, not by callers)
+  int side_norm;
 };
 constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
 // Portable fp32 CUDA-core implementation of the chunk form.

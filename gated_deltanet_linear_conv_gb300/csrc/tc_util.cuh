@@ -141,6 +141,11 @@ __device__ __forceinline__ void bulk_wait_read() {
 }
 // Wait until every bulk group of this thread has completed its writes.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Wait until at most N of this thread's bulk groups have not completed their writes.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group() {
+  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
 // Named barrier over `count` threads (a warp-multiple) with id 1..15.
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
