@@ -220,13 +220,16 @@ int gdn_chunk_prefill(const gdn_dims* dims, const int32_t* cu_seqlens,
  * gated delta rule of gdn_chunk_prefill followed by the gated RMSNorm of
  * gdn_gated_rmsnorm on each (token, value head) row of its output
  * ([RFC] 2.2 ops 4 and 6; [QDA] forward listing: core output, then
- * self.norm(core_output, z)).  The core output o is never stored; it is
- * rounded to bf16 (as a stored bf16 o would be) and normalised:
+ * self.norm(core_output, z)).  The core output o is rounded to bf16 (as a
+ * stored bf16 o would be) and normalised:
  *   y[t, h] = o[t, h] / sqrt(mean(o[t, h]^2) + norm_eps) * norm_w * silu(z[t, h])
- * For bf16 y the gate norm_w * silu(z) is evaluated in bf16x2 arithmetic (the
- * tanh form of gdn_conv_gating at bf16 precision); fp32 y keeps fp32 throughout.
- * On one GB300 this call is slower than gdn_chunk_prefill + gdn_gated_rmsnorm
- * (the norm epilogue paces the sequential scan); it saves the o round trip.
+ * One sequence (the cooperative launch): the scan stores o into y and spare
+ * solve groups normalise each 64-token block in place once it has landed, beside
+ * the scan of later chunks (on one GB300, 129.5 us against 118.8 + 18.9 us for
+ * gdn_chunk_prefill + gdn_gated_rmsnorm at 4096 tokens, 32 heads).  Packed
+ * batches apply the norm in the scan's output epilogue (o is never stored; for
+ * bf16 y the gate norm_w * silu(z) is evaluated in bf16x2 arithmetic), which is
+ * slower than the two separate calls.  fp32 y keeps fp32 arithmetic.
  * Arguments as gdn_chunk_prefill, with o replaced by
  *   z              [tokens, Nv, Dv]     bf16 (else GDN_ERR_UNSUPPORTED)
  *   norm_w         [Dv]                 float32
@@ -267,7 +270,7 @@ int gdn_chunk_prefill_fp32(const gdn_dims* dims, const int32_t* cu_seqlens,
  *     GDN_ERR_UNSUPPORTED).
  *   - Size limit: the workspace of these dims, laid out without the split of a
  *     long sequence, must be at most 32 MiB.  One sequence of any length up to
- *     about 4 million tokens fits (its solve tiles go through a fixed ring; at
+ *     about 2 million tokens fits (its solve tiles go through a fixed ring; at
  *     32 value heads the ring takes 25.4 MB), but it never runs split.  Packed
  *     batches keep a tile per (chunk, head): at 32 value heads, about 1,200
  *     tokens in all.  Larger problems return GDN_ERR_INVALID_ARG and should use
