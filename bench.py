@@ -14,8 +14,9 @@ lengths ~ U[512, 8192]) and on the long one (T=131072) under "varlen" and
 the oracle's tokens/s on a bounded sample).  Every device time is the median of
 --steps timed replays.  "e2e" is the same prefill step through
 the public API with the inputs copied in from pinned host memory and y read back
-every step; the copies of step i+1 run on a copy stream under step i's compute
-(two device buffer sets), as a pipelined caller would run them.
+every step; the copies of step i+1 run on two copy streams under step i's compute
+and the read-backs on a third (two device buffer sets), as a pipelined caller would
+run them.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-cpu-baseline] [--headline-only]
 
@@ -489,27 +490,41 @@ def run_ours(args):
     h2d = sum(t.numel() * t.element_size() for t in (hx, ha, hb, hz))
     d2h = hy.numel() * hy.element_size()
 
-    # Two sets of device inputs and outputs: step i's host->device copies run on a copy stream
-    # while step i-1 computes, and step i's device->host read follows its compute there.  The
-    # copy stream's order is H2D(0), H2D(1), D2H(0), H2D(2), D2H(1), ...; every step still
-    # moves its own inputs and result inside the timed region.
+    # Two sets of device inputs and outputs.  Step i's host->device copies run on three copy
+    # streams (each half of mixed_qkv on one; z, a and b on the third: about 34 MB each; one
+    # copy stream moved about 120 GB/s) while step i-1 computes, and step i's device->host
+    # read runs on a fourth stream after its compute, so that the two directions overlap.  A copy into set j waits for the compute that last read
+    # set j; a compute into set j waits for the read-back of set j's previous result.  Every
+    # step still moves its own inputs and result inside the timed region.
     sets = [(x, a, b, z, bufs['y'])]
     sets.append(tuple(torch.empty_like(t) for t in sets[0]))
     hys = [hy, torch.empty_like(hy).pin_memory()]
-    copy_stream = torch.cuda.Stream()
-    h2d_done = [torch.cuda.Event(), torch.cuda.Event()]
+    h2d_streams = [torch.cuda.Stream() for _ in range(3)]
+    d2h_stream = torch.cuda.Stream()
+    h2d_done = [[torch.cuda.Event() for _ in range(3)] for _ in range(2)]
     comp_done = [torch.cuda.Event(), torch.cuda.Event()]
-    d2h_done = torch.cuda.Event()
+    d2h_done = [torch.cuda.Event(), torch.cuda.Event()]
+    half = T // 2
+    # per copy stream: (device tensor of the set, host tensor) pairs, as slices
+    pieces = [lambda st: ((st[0][:half], hx[:half]),),
+              lambda st: ((st[0][half:], hx[half:]),),
+              lambda st: ((st[3], hz), (st[1], ha), (st[2], hb))]
 
-    def e2e_h2d(j):
-        with torch.cuda.stream(copy_stream):
-            for dst, src in zip(sets[j][:4], (hx, ha, hb, hz)):
-                dst.copy_(src, non_blocking=True)
-            h2d_done[j].record(copy_stream)
+    def e2e_h2d(j, first):
+        for k, (cs, piece) in enumerate(zip(h2d_streams, pieces)):
+            with torch.cuda.stream(cs):
+                if not first:
+                    cs.wait_event(comp_done[j])
+                for dst, src in piece(sets[j]):
+                    dst.copy_(src, non_blocking=True)
+                h2d_done[j][k].record(cs)
 
-    def e2e_compute(j):
+    def e2e_compute(j, first):
         xj, aj, bj, zj, yj = sets[j]
-        stream.wait_event(h2d_done[j])
+        for ev in h2d_done[j]:
+            stream.wait_event(ev)
+        if not first:
+            stream.wait_event(d2h_done[j])
         gdn.conv_gating(xj, w, aj, bj, A_log, dt_bias, sh.Nk, sh.Nv, sh.Dk, sh.Dv, num_seqs=1,
                         conv_state_out=conv_state_out,
                         out=(bufs['q'], bufs['k'], bufs['v'], bufs['g'], bufs['beta']))
@@ -518,21 +533,22 @@ def run_ours(args):
         comp_done[j].record(stream)
 
     def e2e_d2h(j):
-        with torch.cuda.stream(copy_stream):
-            copy_stream.wait_event(comp_done[j])
+        with torch.cuda.stream(d2h_stream):
+            d2h_stream.wait_event(comp_done[j])
             hys[j].copy_(sets[j][4], non_blocking=True)
-            d2h_done.record(copy_stream)
+            d2h_done[j].record(d2h_stream)
 
     def e2e_steps(n, start=None):
-        if start is not None:          # the first copy starts inside the timed region
-            copy_stream.wait_event(start)
-        e2e_h2d(0)
+        if start is not None:          # the first copies start inside the timed region
+            for cs in h2d_streams:
+                cs.wait_event(start)
+        e2e_h2d(0, True)
         for i in range(n):
-            e2e_compute(i & 1)
+            e2e_compute(i & 1, i < 2)
             if i + 1 < n:
-                e2e_h2d((i + 1) & 1)
+                e2e_h2d((i + 1) & 1, i + 1 < 2)
             e2e_d2h(i & 1)
-        stream.wait_event(d2h_done)
+        stream.wait_event(d2h_done[(n - 1) & 1])     # (the read-backs run in order on one stream)
 
     e2e_steps(args.warmup)
     barrier()
@@ -602,7 +618,7 @@ def run_ours(args):
             'chunk_prefill': {'us': us_chunk, 'TFLOP/s': tflops, 'frac_tc': tflops / tc_peak},
             'gated_rmsnorm': {'us': us_norm, 'GB/s': nb / (us_norm * 1e-6) / 1e9,
                               'frac_hbm': nb / (us_norm * 1e-6) / 1e9 / hbm_peak, 'bytes': nb},
-            'chunk_prefill_gated_norm': {'us': us_fused, 'note': 'one call: chunk prefill with the norm in its epilogue'}},
+            'chunk_prefill_gated_norm': {'us': us_fused, 'note': 'one call: chunk prefill and the gated norm (for one sequence the norm runs beside the scan)'}},
         'decode': {'workload': 'decode_b256', 'kernel': 'gdn_decode_fused', 'steps': dsteps,
                    'us_per_step': ms_dec * 1e3, 'tokens_per_s': whole_job_rate(B, ws, ms_dec),
                    'us_per_step_spread': {'min': min(t_dec) * 1e3, 'median': ms_dec * 1e3,
