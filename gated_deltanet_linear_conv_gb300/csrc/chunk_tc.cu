@@ -368,7 +368,8 @@ __device__ __forceinline__ int claim_item(int* counter) {
 // Returns false, with the device error flag raised, on a timeout.
 __device__ bool solve_item(uint8_t* sm, int tid, uint32_t barid, uint64_t* bar, uint32_t& ph, uint32_t tbase,
                            const CUtensorMap* tmq, const CUtensorMap* tmk, const ChunkArgs& p, int slot, int h,
-                           SolveAhead& ahead, int nslot, int nh, size_t tile, const int* rel, int rel_need) {
+                           SolveAhead& ahead, int nslot, int nh, size_t tile, const int* rel, int rel_need,
+                           bool publish = true) {
   float* AT = reinterpret_cast<float*>(sm + S1_AT);
   float* TR = reinterpret_cast<float*>(sm + S1_TR);
   float* XS = reinterpret_cast<float*>(sm + S1_XS);
@@ -597,11 +598,12 @@ __device__ bool solve_item(uint8_t* sm, int tid, uint32_t barid, uint64_t* bar, 
   ph += 1;
   if (!done && tid == 0) raise_error(p.err, kDevErrTimeout);
   // the next item may reuse this shared and tensor memory; thread 0 then fences for the
-  // group (the barrier orders every thread's tile stores before its fence and flag)
+  // group (the barrier orders every thread's tile stores before its fence and flag) when a
+  // flag publishes the tile (`publish`; the packed path's scans run in a later launch)
   tc_fence_before();
   named_sync(barid, 128);
   tc_fence_after();
-  if (tid == 0) asm volatile("fence.acq_rel.gpu;" ::: "memory");
+  if (publish && tid == 0) asm volatile("fence.acq_rel.gpu;" ::: "memory");
   return done;
 }
 
@@ -639,7 +641,7 @@ chunk_solve_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
     const int after = tid == 0 && next < nitems ? claim_item(counter) : nitems;
     const int nslot = next < nitems ? next / p.Nv : -1, nh = next < nitems ? next % p.Nv : 0;
     if (!solve_item(sm, tid, 1, bar, ph, *tslot, &tmq, &tmk, p, item / p.Nv, item % p.Nv, ahead, nslot, nh,
-                    (size_t)(item / p.Nv), nullptr, 0))
+                    (size_t)(item / p.Nv), nullptr, 0, false))
       break;
     if (tid == 0) item_slot[par] = after;
     __syncthreads();
