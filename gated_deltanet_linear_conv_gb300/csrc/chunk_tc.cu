@@ -1550,10 +1550,12 @@ chunk_scan_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
 // items in chunk order and publish a ready flag per item.  Groups on one SM
 // slow each other down (an item takes about 2.5x as long with three as with
 // one), so `ngroups` of them claim items: enough for the solve to stay ahead
-// of the scans, and no more.  A scan CTA awaits a chunk's
-// flag before loading its tiles, so the solve of later chunks overlaps the
-// scan of earlier ones.  All CTAs are resident at once (cooperative launch
-// with one CTA per SM), so these waits always end; each is bounded anyway.
+// of the scans, and no more.  With z (the gated norm), the third group of every
+// solve CTA normalises the published output blocks instead (the side norm).  A
+// scan CTA awaits a chunk's flag before loading its tiles, so the solve of later
+// chunks overlaps the scan of earlier ones.  All CTAs are resident at once
+// (cooperative launch with one CTA per SM), so these waits always end; each is
+// bounded anyway.
 // ---------------------------------------------------------------------------
 constexpr int NT3 = 384;
 constexpr uint32_t S1_GROUP = (S1_BAR + 64 + 1023) & ~1023u;     // one solve group's shared memory
@@ -2062,9 +2064,9 @@ ChunkPlan plan_chunk(int num_seqs, int total, int Nv, bool fused, bool split_ok)
 // The plan a call takes on the current device.  A sequence is split when the SMs hold
 // three scans per head and at least two solve CTAs per head beside them (the two
 // segments' scans take twice the solve's output per period; with fewer solve SMs the
-// split runs slower than one chain: 264 vs 124 us at 32 heads, T = 4096, on 152 SMs),
-// and the output is the plain o (the gated norm of the fused epilogue cannot be
-// corrected afterwards).
+// split runs slower than one chain: 258 vs 151 us at 32 heads, T = 4096, and 5.1 vs
+// 3.1 ms at T = 131072, on 152 SMs), and the output is the plain o (a gated norm applied
+// to the blocks as they are scanned cannot be corrected afterwards).
 ChunkPlan device_plan(int num_seqs, int total, int Nv, bool allow_split, int* sms_out) {
   int sms = 0;
   const bool fused = num_seqs == 1 && fused_device(&sms) && sms > Nv;
