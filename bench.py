@@ -224,6 +224,33 @@ def cpu_baseline(inp, budget_s=12.0, name='prefill_t4096'):
                       % (ntok, name, inp.shape.Nv, dt)}
 
 
+def cpu_baseline_decode(dinp, budget_s=3.0):
+    """Oracle tokens/s of the fused decode step (one token per sequence) on a bounded number
+    of the workload's sequences."""
+    import numpy as np
+    import oracle as O
+    sh = dinp.shape
+    f64 = lambda t: t.detach().to('cpu').double().numpy()  # noqa: E731
+    args = [f64(t) for t in (dinp.mixed_qkv, dinp.conv_w, dinp.conv_state, dinp.a, dinp.b, dinp.A_log,
+                             dinp.dt_bias, dinp.S0, dinp.z, dinp.norm_w)]
+
+    def run(n):
+        sub = [x[:n] if i in (0, 2, 3, 4, 7, 8) else x for i, x in enumerate(args)]
+        O.decode_step(*sub, sh.Nk, sh.Nv, sh.Dk, sh.Dv)
+
+    n = 4
+    t0 = time.perf_counter()
+    run(n)
+    dt = time.perf_counter() - t0
+    n = int(max(1, min(dinp.num_seqs, n * budget_s / max(dt, 1e-3))))
+    t0 = time.perf_counter()
+    run(n)
+    dt = time.perf_counter() - t0
+    return {'value': n / dt, 'unit': 'tokens/s', 'cores': cpu_threads(), 'kind': 'oracle',
+            'sample': 'fp64 NumPy oracle decode step (conv update, gates, recurrence, gated RMSNorm) '
+                      'for %d of the %d sequences of decode_b256, %.1f s' % (n, dinp.num_seqs, dt)}
+
+
 # Kernels of this library per call on the tensor-core path: conv_gating launches one (with no
 # conv state in, its tiled pass writes the new state); chunk prefill launches one for a single
 # sequence (the cooperative solve + scan launch) and two for a packed batch (solve, then scan);
@@ -638,6 +665,7 @@ def run_ours(args):
         line[key] = res
     if ws == 1 and not args.no_cpu_baseline:
         line['cpu_baseline'] = cpu_baseline(inp)
+        line['decode']['cpu_baseline'] = cpu_baseline_decode(dinp)
     print(json.dumps(line))
     if dist is not None:
         dist.destroy_process_group()
