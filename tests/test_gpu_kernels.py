@@ -131,6 +131,29 @@ def test_conv_gating_state_out_without_state_in(lengths):
     gdn.check_device_error()
 
 
+@pytest.mark.parametrize('bias,state', [(True, True), (False, False), (False, True)],
+                         ids=['bias_state', 'plain', 'state'])
+@pytest.mark.parametrize('odt', [torch.float32, torch.bfloat16], ids=['f32', 'bf16'])
+def test_conv_gating_tiled_64_wide_heads(bias, state, odt):
+    """The tiled bf16 kernel with 64-wide q/k heads (8 lanes per head in the L2 norm) on a
+    shape whose channels fill whole 1024-channel blocks (Nk = 8, Nv = 16: C = 2048), with and
+    without bias and conv state, ragged and empty sequences, every channel block rotating
+    over the CTAs."""
+    shape = I.MixerShape(8, 16, 64, 64)
+    lengths = [1, 40, 0, 3, 130, 17, 64, 2]
+    inp = _conv_case(shape, torch.bfloat16, lengths, seed=15, state=state, bias=bias)
+    cu = inp.cu_seqlens()
+    (q, k, v, g, beta), cs_out = _run_conv(inp, cu, odt, state=state)
+    ref = _oracle_conv(inp, cu, state=state)
+    tol = TOL_F32 if odt == torch.float32 else TOL_BF16
+    for name, got in (('q', q), ('k', k), ('v', v)):
+        assert_close(np64(got), ref[name], tol, what=name)
+    for name, got in (('g', g), ('beta', beta)):
+        assert_close(np64(got), ref[name], TOL_F32, what=name)
+    np.testing.assert_array_equal(np64(cs_out), ref['conv_state'])
+    gdn.check_device_error()
+
+
 def test_conv_gating_equal_batches_no_state():
     shape = SHAPES[0]
     inp = _conv_case(shape, torch.bfloat16, [33, 33, 33], seed=13, state=False, bias=False)
