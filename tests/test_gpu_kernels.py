@@ -368,7 +368,8 @@ def test_mixer_prefill_small_end_to_end(fuse_norm):
 
 
 @pytest.mark.parametrize('odt', [torch.float32, torch.bfloat16], ids=['f32', 'bf16'])
-@pytest.mark.parametrize('lengths', [[300], [130, 0, 64, 7]], ids=['one_seq', 'packed'])
+@pytest.mark.parametrize('lengths', [[300], [40], [64], [130, 0, 64, 7]],
+                         ids=['one_seq', 'one_partial_chunk', 'one_full_chunk', 'packed'])
 def test_chunk_prefill_gated_norm(lengths, odt):
     """Chunk prefill with the gated RMSNorm in its epilogue: against the oracle
     (recurrence, then the norm) and against the two separate calls.  One
