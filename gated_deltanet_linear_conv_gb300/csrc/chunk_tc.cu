@@ -904,6 +904,17 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
     return wsb + (t * p.Nv + h) * TILE_T_BYTES;
   };
 
+  // The initial state arrives by four 16 KB bulk copies, issued by thread 0 as soon as their
+  // mbarrier is initialised (a thread's 128 dependent-free column loads from global memory
+  // took about 10 us at the start of a launch): rows 32q .. 32q + 31 into the second stage
+  // buffer (q < 3) and into the head of the second v buffer (q = 3), away from the operand
+  // rows zeroed below.  Both are first written by the loads of chunk 1, which wait until the
+  // state role has moved the state into tensor memory (s0c).  (The host requires every
+  // pointer to be 16-byte aligned, as the copies do.)
+  const bool s0_bulk = sg.S0 != nullptr && !sg.identity;
+  auto s0_part = [&](int q) -> uint8_t* {
+    return sm + (q < 3 ? K2_ST + STAGE_BYTES + (uint32_t)q * 16384u : K2_VT + 32768u);
+  };
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&B->stl[i], 1);
@@ -922,6 +933,10 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
     B->abort = 0;
     B->odone = 0;
     fence_barrier_init();
+    if (s0_bulk) {
+      mbar_arrive_expect_tx(&B->s0f, 65536);
+      for (int q = 0; q < 4; ++q) bulk_load(s0_part(q), sg.S0 + (size_t)q * 32 * DV, 16384, &B->s0f);
+    }
     prefetch_tmap(tmk);
     prefetch_tmap(tmv);
     prefetch_tmap(tmo);
@@ -939,20 +954,6 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
   const uint32_t lane_base = tbase + ((uint32_t)((warp & 3) * 32) << 16);
   const uint32_t sb = smem_u32(sm);
 
-  // The initial state arrives by four 16 KB bulk copies issued before any role starts (a
-  // thread's 128 dependent-free column loads from global memory took about 10 us at the
-  // start of a launch): rows 32q .. 32q + 31 into the second stage buffer (q < 3) and into
-  // the head of the second v buffer (q = 3).  Both are first written by the loads of chunk
-  // 1, which wait until the state role has moved the state into tensor memory (s0c).  (The
-  // host requires every pointer to be 16-byte aligned, as the copies do.)
-  const bool s0_bulk = sg.S0 != nullptr && !sg.identity;
-  auto s0_part = [&](int q) -> uint8_t* {
-    return sm + (q < 3 ? K2_ST + STAGE_BYTES + (uint32_t)q * 16384u : K2_VT + 32768u);
-  };
-  if (tid == 0 && s0_bulk) {
-    mbar_arrive_expect_tx(&B->s0f, 65536);
-    for (int q = 0; q < 4; ++q) bulk_load(s0_part(q), sg.S0 + (size_t)q * 32 * DV, 16384, &B->s0f);
-  }
 
   // loads of a chunk: v tiles and T diag(beta) (for [U~^T | 0]), and the stage
   auto issue_vt = [&](int c) {
@@ -1602,157 +1603,130 @@ __global__ void __launch_bounds__(NT3, 1)
 chunk_fused_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo,
                    const __grid_constant__ CUtensorMap tmz, const __grid_constant__ CUtensorMap tmr, ChunkArgs p,
-                   SplitArgs sp, int nscan, int nitems, int skip, int* flags, int ngroups) {
+                   SplitArgs sp, int nscan, int nitems, int* flags, int ngroups) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = tc::smem_aligned<1024>(smem_raw);
-  if ((int)blockIdx.x < nscan) {
-    const int role = blockIdx.x / p.Nv, h = blockIdx.x % p.Nv;
-    if (skip > 0 && role < 2) {
-      // The first chunk of this CTA's segment is solved here, by warps 0-3 in the shared
-      // and tensor memory the scan has not taken yet: alone on its SM the item is ready
-      // well before a solve group sharing an SM with others would deliver it.  The solve
-      // groups start after the segments' first chunks.
-      const int c = role == 0 ? 0 : sp.m;
-      uint64_t* bar = reinterpret_cast<uint64_t*>(sm + S1_BAR);
-      uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S1_BAR + 16);
-      const int tid = threadIdx.x;
+  // The solve CTAs' code comes first in the kernel: code near a kernel's entry runs at full
+  // speed on its first pass, code further in is fetched on demand at its first pass (on a
+  // GB300 about 14 us per 32 KB with a cold L2), and each solve SM's first item (the early
+  // chunks every scan waits for) would pay that.  The scans meanwhile set up, load their
+  // initial state and wait for chunk 0.
+  if ((int)blockIdx.x >= nscan) {
+    const int g = threadIdx.x >> 7, tid = threadIdx.x & 127;
+    uint8_t* gsm = sm + g * S1_GROUP;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(gsm + S1_BAR);
+    volatile int* item_slot = reinterpret_cast<volatile int*>(gsm + S1_BAR + 32);   // two slots
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S1_BAR + 16);        // in group 0's slice
+    const uint32_t barid = 1 + g;
+    if (tid == 0) {
+      mbar_init(bar, 1);
+      fence_barrier_init();
+    }
+    if (threadIdx.x < 32) tmem_alloc(tslot, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tslot + 128u * (uint32_t)g;
+    int* counter = flags + nitems;
+    uint32_t ph = 0;
+    if (g < ngroups) {
+      // Items are claimed two ahead: the next item's gate values and tiles load under the
+      // current one, and the claim of the one after (a global atomic) is in flight meanwhile.
+      // The first two items of every group are fixed: group i (numbered group-major over the
+      // CTAs, so that consecutive items go to different SMs) takes items i and G + i, G the
+      // number of groups; the counter hands out the items after 2G.  (With two atomic claims
+      // per group at the start, an item of an early chunk could become some group's second
+      // item and wait for its first.)
+      const int nsolve = (int)gridDim.x - nscan;
+      const int G = ngroups * nsolve;
       if (tid == 0) {
-        mbar_init(bar, 1);
-        fence_barrier_init();
+        const int gi = g * nsolve + ((int)blockIdx.x - nscan);
+        item_slot[0] = gi;
+        item_slot[1] = G + gi;
       }
-      if (tid < 32) tmem_alloc_keep(tslot, 128);   // the scan allocates (and relinquishes) next
-      tc_fence_before();
-      __syncthreads();
-      tc_fence_after();
-      if (tid < 128) {
-        SolveAhead ahead{false, false, 0.f, -1, 0, 0};
-        uint32_t ph = 0;
-        const bool ok = solve_item(sm, tid, 1, bar, ph, *tslot, &tmq, &tmk, p, c, h, ahead, -1, 0,
-                                   (size_t)(role * sp.ring), nullptr, 0);
-        if (tid == 0) st_flag(flags + (size_t)c * p.Nv + h, ok ? 1 : -1);
+      named_sync(barid, 128);
+      int item = item_slot[0], next = item_slot[1];
+      SolveAhead ahead{false, false, 0.f, -1, 0, 0};
+      int par = 0;
+      while (item < nitems) {
+        const int after = tid == 0 && next < nitems ? 2 * G + claim_item(counter) : nitems;   // read after the item
+        int c, h, nc = -1, nh = 0;
+        item_chunk(sp, p.Nv, item, c, h);
+        if (next < nitems) item_chunk(sp, p.Nv, next, nc, nh);
+        // the chunk's ring position, and the chunk that used it before (same segment)
+        const int seg = sp.nseg == 2 && c >= sp.m ? 1 : 0, cl = c - seg * sp.m;
+        const int* rel = cl >= sp.ring ? flags + (size_t)(c - sp.ring) * p.Nv + h : nullptr;
+        const bool ok = solve_item(gsm, tid, barid, bar, ph, tbase, &tmq, &tmk, p, c, h, ahead, nc, nh,
+                                   (size_t)(seg * sp.ring + cl % sp.ring), rel, seg ? 3 : 2);
+        if (tid == 0) {
+          st_flag(flags + (size_t)c * p.Nv + h, ok ? 1 : -1);   // tiles visible (see solve_item)
+          item_slot[par] = after;
+        }
+        if (!ok) break;
+        named_sync(barid, 128);
+        item = next;
+        next = item_slot[par];
+        par ^= 1;
       }
-      tc_fence_before();
-      __syncthreads();
-      if (tid < 32) tmem_dealloc(*tslot, 128);
-      if (tid == 0) mbar_inval(bar);
-      __syncthreads();
+    } else if (p.side_norm && g == 2) {
+      // The side norm: the third group of every solve CTA applies the gated RMSNorm to the
+      // output blocks in chunk order, each once the scan has published it (its o rows sit in
+      // the output buffer), claiming blocks from a counter of their own.  A block that is not
+      // published within the wait bound (a failed scan) ends the group with the device error.
+      int* ncount = flags + nitems + 1;
+      const int* oflags = flags + nitems + 2;
+      float w[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) w[i] = p.norm_w[8 * (tid & 15) + i];
+      for (;;) {
+        if (tid == 0) {
+          int it = atomicAdd(ncount, 1);
+          if (it < nitems && !wait_count(oflags + it, 1, p.wait_ns)) {
+            raise_error(p.err, kDevErrTimeout);
+            it = -1;
+          }
+          item_slot[0] = it;
+        }
+        named_sync(barid, 128);
+        const int it = item_slot[0];
+        named_sync(barid, 128);              // (the slot is written again next round)
+        if (it < 0 || it >= nitems) break;
+        const int c0 = (it / p.Nv) * CT;
+        norm_rows<Tout, 128, 8>(p, c0, min(CT, p.total - c0), it % p.Nv, tid, w);
+      }
     }
-    ScanSeg sg = whole_seq(p, h, 0, &tmo);
-    sg.ring = sp.ring;
-    sg.tile0 = role == 0 ? 0 : sp.ring;            // the second segment's ring follows the first's
-    sg.release = true;
-    if (sp.nseg == 2) {
-      const size_t hs = (size_t)h * DK * DV;
-      if (role == 0) {                       // first segment: the caller's initial state
-        sg.c_end = sp.m;
-        sg.ST = sp.S_mid + hs;
-      } else if (role == 1) {                // second segment from a zero state
-        sg.c_begin = sp.m;
-        sg.S0 = nullptr;
-        sg.ST = sp.Bst + hs;
-      } else {                               // second segment's transition map
-        sg.c_begin = sp.m;
-        sg.S0 = nullptr;
-        sg.identity = true;
-        sg.zero_v = true;
-        sg.ST = sp.Phi + hs;
-        sg.out = sp.R;
-        sg.out_bf16 = true;
-        sg.tmo = &tmr;
-        sg.row_off = sp.m * CT;
-      }
-    }
-    scan_body<Tout, NORM>(sm, &tmk, &tmv, sg, &tmz, p, h, 0, flags);
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x < 32) tmem_dealloc(*tslot, 512);
     return;
   }
-  const int g = threadIdx.x >> 7, tid = threadIdx.x & 127;
-  uint8_t* gsm = sm + g * S1_GROUP;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(gsm + S1_BAR);
-  volatile int* item_slot = reinterpret_cast<volatile int*>(gsm + S1_BAR + 32);   // two slots
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S1_BAR + 16);        // in group 0's slice
-  const uint32_t barid = 1 + g;
-  if (tid == 0) {
-    mbar_init(bar, 1);
-    fence_barrier_init();
-  }
-  if (threadIdx.x < 32) tmem_alloc(tslot, 512);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tbase = *tslot + 128u * (uint32_t)g;
-  int* counter = flags + nitems;
-  const int ntotal = nitems;             // (chunk, value head) items of the call
-  nitems -= skip;                        // items claimed here: those after the self-solved chunks
-  uint32_t ph = 0;
-  if (g < ngroups) {
-    // Items are claimed two ahead: the next item's gate values and tiles load under the
-    // current one, and the claim of the one after (a global atomic) is in flight meanwhile.
-    // The first two items of every group are fixed: group i (numbered group-major over the
-    // CTAs, so that consecutive items go to different SMs) takes items i and G + i, G the
-    // number of groups; the counter hands out the items after 2G.  (With two atomic claims
-    // per group at the start, an item of an early chunk could become some group's second
-    // item and wait for its first.)
-    const int nsolve = (int)gridDim.x - nscan;
-    const int G = ngroups * nsolve;
-    if (tid == 0) {
-      const int gi = g * nsolve + ((int)blockIdx.x - nscan);
-      item_slot[0] = gi;
-      item_slot[1] = G + gi;
-    }
-    named_sync(barid, 128);
-    int item = item_slot[0], next = item_slot[1];
-    SolveAhead ahead{false, false, 0.f, -1, 0, 0};
-    int par = 0;
-    while (item < nitems) {
-      const int after = tid == 0 && next < nitems ? 2 * G + claim_item(counter) : nitems;   // read after the item
-      int c, h, nc = -1, nh = 0;
-      item_chunk(sp, p.Nv, item + skip, c, h);
-      if (next < nitems) item_chunk(sp, p.Nv, next + skip, nc, nh);
-      // the chunk's ring position, and the chunk that used it before (same segment)
-      const int seg = sp.nseg == 2 && c >= sp.m ? 1 : 0, cl = c - seg * sp.m;
-      const int* rel = cl >= sp.ring ? flags + (size_t)(c - sp.ring) * p.Nv + h : nullptr;
-      const bool ok = solve_item(gsm, tid, barid, bar, ph, tbase, &tmq, &tmk, p, c, h, ahead, nc, nh,
-                                 (size_t)(seg * sp.ring + cl % sp.ring), rel, seg ? 3 : 2);
-      if (tid == 0) {
-        st_flag(flags + (size_t)c * p.Nv + h, ok ? 1 : -1);   // tiles visible (see solve_item)
-        item_slot[par] = after;
-      }
-      if (!ok) break;
-      named_sync(barid, 128);
-      item = next;
-      next = item_slot[par];
-      par ^= 1;
-    }
-  } else if (p.side_norm && g == 2) {
-    // The side norm: the third group of every solve CTA applies the gated RMSNorm to the
-    // output blocks in chunk order, each once the scan has published it (its o rows sit in
-    // the output buffer), claiming blocks from a counter of their own.  A block that is not
-    // published within the wait bound (a failed scan) ends the group with the device error.
-    int* ncount = flags + ntotal + 1;
-    const int* oflags = flags + ntotal + 2;
-    float w[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) w[i] = p.norm_w[8 * (tid & 15) + i];
-    for (;;) {
-      if (tid == 0) {
-        int it = atomicAdd(ncount, 1);
-        if (it < ntotal && !wait_count(oflags + it, 1, p.wait_ns)) {
-          raise_error(p.err, kDevErrTimeout);
-          it = -1;
-        }
-        item_slot[0] = it;
-      }
-      named_sync(barid, 128);
-      const int it = item_slot[0];
-      named_sync(barid, 128);              // (the slot is written again next round)
-      if (it < 0 || it >= ntotal) break;
-      const int c0 = (it / p.Nv) * CT;
-      norm_rows<Tout, 128, 8>(p, c0, min(CT, p.total - c0), it % p.Nv, tid, w);
+  const int role = (int)blockIdx.x / p.Nv, h = (int)blockIdx.x % p.Nv;
+  ScanSeg sg = whole_seq(p, h, 0, &tmo);
+  sg.ring = sp.ring;
+  sg.tile0 = role == 0 ? 0 : sp.ring;            // the second segment's ring follows the first's
+  sg.release = true;
+  if (sp.nseg == 2) {
+    const size_t hs = (size_t)h * DK * DV;
+    if (role == 0) {                       // first segment: the caller's initial state
+      sg.c_end = sp.m;
+      sg.ST = sp.S_mid + hs;
+    } else if (role == 1) {                // second segment from a zero state
+      sg.c_begin = sp.m;
+      sg.S0 = nullptr;
+      sg.ST = sp.Bst + hs;
+    } else {                               // second segment's transition map
+      sg.c_begin = sp.m;
+      sg.S0 = nullptr;
+      sg.identity = true;
+      sg.zero_v = true;
+      sg.ST = sp.Phi + hs;
+      sg.out = sp.R;
+      sg.out_bf16 = true;
+      sg.tmo = &tmr;
+      sg.row_off = sp.m * CT;
     }
   }
-  tc_fence_before();
-  __syncthreads();
-  if (threadIdx.x < 32) tmem_dealloc(*tslot, 512);
+  scan_body<Tout, NORM>(sm, &tmk, &tmv, sg, &tmz, p, h, 0, flags);
 }
 
 // ---------------------------------------------------------------------------
@@ -2131,9 +2105,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs& args, cudaStream_t s) {
     const double per_scan = (double)(sms - nscan) / (double)(sp.nseg * p.Nv);
     int ngroups = per_scan >= 5.3 ? 1 : 2;
     if (p.no_solve) ngroups = 0;           // test hook: no flag is ever published
-    // the scan CTAs of the first and of the second segment solve their first chunk themselves
-    int skip = p.no_solve ? 0 : sp.nseg * p.Nv;
-    void* args[] = {&mq, &mk, &mv, &mo, &mz, &mr, &pc, &sp, &nscan, &nitems, &skip, &flags, &ngroups};
+    void* args[] = {&mq, &mk, &mv, &mo, &mz, &mr, &pc, &sp, &nscan, &nitems, &flags, &ngroups};
     const void* fn = fused_kernels()[p.out_bf16 ? 0 : 2];
     e = cudaLaunchCooperativeKernel(fn, dim3(sms), dim3(NT3), args, K3_SMEM, s);
     if (e != cudaSuccess || sp.nseg == 1) return e;

@@ -172,13 +172,6 @@ __device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
                : "memory");
   asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
 }
-// Allocation by one full warp that keeps the CTA's permit to allocate again later
-// (a CTA relinquishes it with its last allocation, tmem_alloc above).
-__device__ __forceinline__ void tmem_alloc_keep(uint32_t* slot, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
-               "r"(ncols)
-               : "memory");
-}
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
