@@ -956,26 +956,44 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
 
 
   // loads of a chunk: v tiles and T diag(beta) (for [U~^T | 0]), and the stage
-  auto issue_vt = [&](int c) {
+  // Each buffer's mbarrier expects all of its bytes with the first of its copies, so that
+  // the parts may be issued apart: the v tiles (issue_v) and the solve's T diag(beta)
+  // (issue_tb); the k tiles (issue_k) and the solve's [-W; Q~] and P tiles (issue_ws).
+  auto issue_v = [&](int c) {
     const int t = bos + c * CT;
     const uint32_t vt = K2_VT + (uint32_t)(c & 1) * 32768u;
     uint64_t* bar = &B->vt[c & 1];
     mbar_arrive_expect_tx(bar, 2 * 8192 + 8192);
     tma_load_2d(sm + vt, tmv, bar, h * DV, t);
     tma_load_2d(sm + vt + 8192, tmv, bar, h * DV + 64, t);
-    bulk_load(sm + vt + 16384, ws_tile(c) + WS_TB, 8192, bar);
+  };
+  auto issue_tb = [&](int c) {
+    const uint32_t vt = K2_VT + (uint32_t)(c & 1) * 32768u;
+    bulk_load(sm + vt + 16384, ws_tile(c) + WS_TB, 8192, &B->vt[c & 1]);
+  };
+  auto issue_vt = [&](int c) {
+    issue_v(c);
+    issue_tb(c);
     return true;
   };
-  auto issue_stage = [&](int c) {
+  auto issue_k = [&](int c) {
     const int t = bos + c * CT;
     const uint32_t st = K2_ST + (uint32_t)(c & 1) * STAGE_BYTES;
     uint64_t* bar = &B->stl[c & 1];
-    const uint8_t* src = ws_tile(c);
     mbar_arrive_expect_tx(bar, 32768 + 8192 + 512 + 2 * 8192);
-    bulk_load(sm + st, src + WS_QW, 32768, bar);
-    bulk_load(sm + st + SG_P, src + WS_P, 8192 + 512, bar);
     tma_load_2d(sm + st + SG_K, tmk, bar, hk * DK, t);
     tma_load_2d(sm + st + SG_K + 8192, tmk, bar, hk * DK + 64, t);
+  };
+  auto issue_ws = [&](int c) {
+    const uint32_t st = K2_ST + (uint32_t)(c & 1) * STAGE_BYTES;
+    uint64_t* bar = &B->stl[c & 1];
+    const uint8_t* src = ws_tile(c);
+    bulk_load(sm + st, src + WS_QW, 32768, bar);
+    bulk_load(sm + st + SG_P, src + WS_P, 8192 + 512, bar);
+  };
+  auto issue_stage = [&](int c) {
+    issue_k(c);
+    issue_ws(c);
     return true;
   };
   // With `flags` (the fused launch) one LOADER thread (warp 9) awaits each chunk's
@@ -990,21 +1008,31 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
   if (warp == 9 && !self_load) {
     // ============================== LOADER ==============================
     if (lane == 0) {
-      int st_issued = 0, vt_issued = 0;
+      int st_issued = 0, vt_issued = 0, tb_issued = 0, ws_issued = 0;
       bool ok = true;
       for (int c = 0; c < n && ok; ++c) {
-        // the v tiles first: their buffer frees (the [U~^T | 0] product of chunk c - 2) a
-        // period before the stage buffer does
-        ok = wait_flag(flags + (size_t)(slot0 + c) * p.Nv + h, wc);
+        // The v tiles first: their buffer frees (the [U~^T | 0] product of chunk c - 2) a
+        // period before the stage buffer does.  The tiles read from q, k and v are issued
+        // before the chunk's flag is awaited, the solve's tiles after it (the early chunks'
+        // flags are set well after the scan has set up).
         if (!sg.zero_v) {
           // v tiles free (for c = 1: the state's copy in that buffer was read)
-          if (ok && (c >= 2 || (c == 1 && s0_bulk)))
+          if (c >= 2 || (c == 1 && s0_bulk))
             ok = c >= 2 ? wait_bar(&B->ready[c & 1], ((c - 2) >> 1) & 1, wc) : wait_bar(&B->s0c, 0, wc);
           if (!ok) break;
-          issue_vt(c);
+          issue_v(c);
           vt_issued = c + 1;
         }
+        if (c < 2) {             // the stage buffers start free (for c = 1 after the wait above)
+          issue_k(c);
+          st_issued = c + 1;
+        }
+        ok = wait_flag(flags + (size_t)(slot0 + c) * p.Nv + h, wc);
         if (!ok) break;
+        if (!sg.zero_v) {
+          issue_tb(c);
+          tb_issued = c + 1;
+        }
         if (c >= 2) ok = wait_bar(&B->ob[c & 1], ((c - 2) >> 1) & 1, wc);           // stage free
         if (!ok) break;
         if (sg.release && c >= 2) {
@@ -1015,10 +1043,14 @@ __device__ void scan_body(uint8_t* sm, const CUtensorMap* tmk, const CUtensorMap
           int* rel = flags_rw + (size_t)(slot0 + c - 2) * p.Nv + h;
           asm volatile("red.relaxed.gpu.global.add.s32 [%0], 1;" ::"l"(rel) : "memory");
         }
-        issue_stage(c);        // (for c = 1 after the v tiles' wait for the state's copy above)
-        st_issued = c + 1;
+        if (c >= 2) issue_k(c);
+        issue_ws(c);
+        st_issued = ws_issued = c + 1;
       }
       if (!ok) {     // let the copies in flight land (the waits are bounded)
+        // a buffer whose q/k/v tiles were issued but whose solve tiles never will be
+        if (vt_issued > tb_issued) mbar_complete_tx(&B->vt[tb_issued & 1], 8192);
+        if (st_issued > ws_issued) mbar_complete_tx(&B->stl[ws_issued & 1], 32768 + 8192 + 512);
         for (int k = max(st_issued - 2, 0); k < st_issued; ++k) mbar_wait(&B->stl[k & 1], (k >> 1) & 1, WAIT_LIMIT);
         for (int k = max(vt_issued - 2, 0); k < vt_issued; ++k) mbar_wait(&B->vt[k & 1], (k >> 1) & 1, WAIT_LIMIT);
       }
