@@ -70,3 +70,22 @@ def test_code_hash_ignores_comments_only():
     c = "int f(int x) {\n  return x + 2;\n}\n"
     assert bench.code_hash(a) == bench.code_hash(b)
     assert bench.code_hash(a) != bench.code_hash(c)
+
+
+def test_clock_summary_takes_the_busy_samples():
+    sys.path.insert(0, ROOT)
+    import bench
+    lines = [
+        '0, 1200, 2070, 150.0, 0x0, Not Active, Not Active, Not Active, Not Active, 0\n',     # idle
+        '0, 2070, 2070, 240.0, 0x0, Not Active, Not Active, Not Active, Not Active, 97\n',
+        '0, 2055, 2070, 260.0, 0x4, Not Active, Not Active, Not Active, Active, 100\n',
+        '0, 2070, 2070, 230.0, 0x0, Not Active, Not Active, Not Active, Not Active, 64\n',
+        'garbage line\n',
+    ]
+    r = bench.summarize_clocks(lines)
+    assert r['samples'] == 4 and r['samples_under_load'] == 3
+    assert r['sm_mhz'] == 2070.0 and r['sm_max_mhz'] == 2070.0
+    assert r['reasons'] == ['sw_power_cap'] and r['power_w_max'] == 260.0
+    # no utilization counter (or none busy): every sample counts
+    r = bench.summarize_clocks([ln.rsplit(',', 1)[0] + ', [N/A]\n' for ln in lines[:2]])
+    assert r['samples'] == 2 and r['samples_under_load'] == 2 and r['sm_mhz'] == (1200 + 2070) / 2
