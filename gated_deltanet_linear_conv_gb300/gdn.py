@@ -321,7 +321,7 @@ def mixer_prefill(mixed_qkv, conv_w, a, b, A_log, dt_bias, z, norm_w, Nk, Nv, Dk
     (and shapes that run on the tensor cores: bf16, 128-wide heads) the chunk prefill and
     the norm are one call (gdn_chunk_prefill_gated_norm).  By default (None) that call is
     taken for a single sequence, where the norm runs beside the sequential scan and the
-    call measured faster than the two separate ones on a GB300 (120.9 vs 111.1 + 18.9 us at
+    call measured faster than the two separate ones on a GB300 (119.2 vs 111.1 + 18.9 us at
     4096 tokens); packed batches take the two calls (their fused form applies the norm in
     the scan's output epilogue, which paces the scan).
 

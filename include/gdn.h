@@ -225,7 +225,7 @@ int gdn_chunk_prefill(const gdn_dims* dims, const int32_t* cu_seqlens,
  *   y[t, h] = o[t, h] / sqrt(mean(o[t, h]^2) + norm_eps) * norm_w * silu(z[t, h])
  * One sequence (the cooperative launch): the scan stores o into y and spare
  * solve groups normalise each 64-token block in place once it has landed, beside
- * the scan of later chunks (on one GB300, 120.9 us against 111.1 + 18.9 us for
+ * the scan of later chunks (on one GB300, 119.2 us against 111.1 + 18.9 us for
  * gdn_chunk_prefill + gdn_gated_rmsnorm at 4096 tokens, 32 heads).  Packed
  * batches apply the norm in the scan's output epilogue (o is never stored; for
  * bf16 y the gate norm_w * silu(z) is evaluated in bf16x2 arithmetic), which is
